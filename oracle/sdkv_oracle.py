@@ -10,7 +10,8 @@ Readings where the pages are silent (each listed in the design notes):
   * window query t sits at position q_pos0 + t and sees keys 0..q_pos0+t;
   * integer budgets: largest-remainder apportionment, ties to the lower flat
     head index; a cap moves the excess to uncapped heads in proportion to s;
-  * top-K order: score descending, then index ascending; NaN ranks last;
+  * top-K order: score descending, then index ascending; -0.0 equals +0.0;
+    NaN ranks below every number, -inf included;
   * an empty selected list gives o = 0 and lse = -inf;
   * lse is the natural-log log-sum-exp of the scaled logits.
 """
@@ -173,7 +174,8 @@ def select_topk(scores, n: int, cand_lo: int, cand_hi: int, n_sink: int, n_recen
 
     K = k_h - n_sink - n_recent with k_h = offsets[i+1] - offsets[i].  Candidates
     are [cand_lo, cand_hi); they are ranked by score descending, equal scores
-    by lower index first, NaN last.  The list is ascending.  Returns the flat
+    by lower index first; NaN ranks below every number (-inf included).
+    The list is ascending.  Returns the flat
     int32 index array (CSR values for `offsets`).
     """
     sc = to_f64(scores)
@@ -191,8 +193,9 @@ def select_topk(scores, n: int, cand_lo: int, cand_hi: int, n_sink: int, n_recen
             if K < 0 or K > cand_hi - cand_lo:
                 raise ValueError("list length does not fit sinks + candidates + recent")
             s = sc[b, h, cand_lo:cand_hi]
-            key = np.where(np.isnan(s), np.inf, -s)           # NaN after everything
-            order = np.lexsort((cand, key))                   # primary -score, then index
+            nan = np.isnan(s)
+            key = np.where(nan, 0.0, -s)
+            order = np.lexsort((cand, key, nan))              # numbers first, -score, then index
             top = np.sort(cand[order[:K]])
             lst = np.concatenate([np.arange(0, n_sink), top, np.arange(n - n_recent, n)])
             out[offsets[i]: offsets[i + 1]] = lst.astype(np.int32)

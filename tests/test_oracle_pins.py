@@ -260,6 +260,9 @@ def test_select_keep_all_and_ties():
 def test_select_nan_ranks_last_and_bad_sizes():
     sc = np.array([[[0.1, np.nan, 0.3, 0.2]]])
     assert list(oracle.select_topk(sc, 4, 0, 4, 0, 0, [0, 3])) == [0, 2, 3]
+    sc = np.array([[[np.nan, -np.inf, 0.3, -0.0, 0.0]]])
+    assert list(oracle.select_topk(sc, 5, 0, 5, 0, 0, [0, 3])) == [2, 3, 4]
+    assert list(oracle.select_topk(sc, 5, 0, 5, 0, 0, [0, 4])) == [1, 2, 3, 4]
     with pytest.raises(ValueError):
         oracle.select_topk(sc, 4, 0, 4, 0, 0, [0, 5])
 
