@@ -1,0 +1,226 @@
+/*
+ * sdkv.h -- C ABI of the sparse-KV decode attention library (libsdkv.so).
+ *
+ * The library computes the decode-step attention hot path of per-head sparse
+ * KV selection on an NVIDIA GB300 (sm_103a):
+ *
+ *   sdkv_head_budgets        per-head cache budgets (host)
+ *   sdkv_score_obs_window    observation-window scores of every cached key
+ *   sdkv_select_topk         sinks + top-K + recent window, as ascending lists
+ *   sdkv_sparse_decode_attn  attention of one query per head over its list
+ *   sdkv_dense_verify_attn   attention of gamma causal queries over the cache
+ *
+ * Conventions shared by every call:
+ *  - Pointers marked "device" are CUDA device pointers, "host" are host
+ *    pointers.  The caller owns every buffer; the library never allocates,
+ *    frees or synchronises (except sdkv_workspace_status, which is a
+ *    synchronous diagnostic).
+ *  - GPU calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL = the legacy default stream).  They may be captured in CUDA graphs.
+ *  - Tensors are bf16 (2-byte bfloat16) unless stated.  Device pointers must
+ *    be 16-byte aligned.  The head dimension d must be 64 or 128.
+ *  - K and V caches have the logical shape [B][Hkv][n_cap][d] with the head
+ *    dimension contiguous; kv_strides = {batch, head, row} strides in
+ *    ELEMENTS, each a multiple of 8 (16 bytes), row stride >= d.
+ *  - GQA: query head hq reads KV head hq / (Hq / Hkv) (contiguous groups);
+ *    Hq must be a multiple of Hkv.
+ *  - Workspace: every GPU call takes a device scratch buffer `ws` of at least
+ *    sdkv_workspace_size(...) bytes.  Its first SDKV_WS_HEADER_BYTES hold a
+ *    device status word and per-head counters: they must be zero before the
+ *    first call that uses the buffer (e.g. cudaMemset once after allocation),
+ *    and every call leaves the counters at zero again.  Calls that may run at
+ *    the same time must use different workspaces.
+ *  - Return value: SDKV_OK or a negative SDKV_ERR_* code; a human-readable
+ *    message for the last failure of the calling thread is returned by
+ *    sdkv_last_error().  Argument errors are detected on the host before any
+ *    launch.  Errors that only the device can see (an index outside the
+ *    cache, a list that does not fit, a wait that ran out) set the status
+ *    word in the workspace header; the call still completes and its outputs
+ *    for the affected heads are unspecified.  Read and clear it with
+ *    sdkv_workspace_status.
+ *
+ * Sources (the pages this library follows):
+ *  [StD]       "Sparse-to-Dense: A Free Lunch for Lossless Acceleration of
+ *              Video Understanding in LLMs", sections 3.1-3.3.
+ *  [ByteCross] "Where Activation Sparsity and KV-Cache Sparsity Cross in LLM
+ *              Decoding", sections "The Byte Crossover", "Speedup Across
+ *              Context", "The Attention Baseline".
+ *  [SparseMM]  "小谈SparseMM，利用多模态大模型中视觉头的稀疏性优化KV Cache",
+ *              methodology section (budget formulas, observation window).
+ */
+#ifndef SDKV_H
+#define SDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SDKV_OK                   0
+#define SDKV_ERR_INVALID_ARG     -1  /* bad pointer, size, stride or alignment */
+#define SDKV_ERR_UNSUPPORTED     -2  /* shape outside what the kernels implement (d, group size ...) */
+#define SDKV_ERR_CUDA            -3  /* a CUDA runtime/driver call failed */
+#define SDKV_ERR_WORKSPACE       -4  /* ws_bytes smaller than sdkv_workspace_size */
+
+/* device status word values (see sdkv_workspace_status) */
+#define SDKV_DEV_OK               0
+#define SDKV_DEV_TIMEOUT          1  /* a bounded wait inside a kernel ran out (about 1 s) */
+#define SDKV_DEV_BAD_INDEX        2  /* a list entry outside [0, n_cap) */
+#define SDKV_DEV_BAD_LIST         3  /* list lengths do not fit sinks + candidates + recent */
+
+#define SDKV_WS_HEADER_BYTES   256   /* status word + reserved; counters follow */
+
+/* operation ids for sdkv_workspace_size */
+#define SDKV_OP_SCORE             1
+#define SDKV_OP_SELECT            2
+#define SDKV_OP_SPARSE_DECODE     3
+#define SDKV_OP_DENSE_VERIFY      4
+
+/*
+ * Per-head cache budgets.  [SparseMM] methodology: with N heads, total budget
+ * B, local window w and uniform share rho,
+ *     r        = rho (B - N w) / N
+ *     B_remain = B - N w - rho (B - N w)
+ *     b_i      = w + r + B_remain * s_i / sum_j s_j
+ * The real b_i are turned into integers that sum to B exactly by
+ * largest-remainder apportionment (ties to the lower index i).  If cap > 0 no
+ * head gets more than cap: the excess of capped heads is shared among the
+ * others in proportion to s, repeated until none exceeds the cap.  sum(s) is a
+ * float64 sum in index order; all-zero scores count as uniform.  The top-K
+ * count of head i is then b_i - w (the local window is kept apart).
+ *
+ *   s       host float[n_heads], finite, >= 0 (flat index layer * H + head)
+ *   total_B budget B, >= n_heads * w
+ *   w       local window per head, >= 0
+ *   rho     uniform share in [0, 1]
+ *   cap     per-head maximum (e.g. the cache length) or 0 for none;
+ *           cap * n_heads must be >= B
+ *   b_out   host int32[n_heads] (written)
+ * Host only, synchronous.  Returns SDKV_ERR_INVALID_ARG on bad input.
+ */
+int sdkv_head_budgets(const float* s, int32_t n_heads, int64_t total_B, int32_t w,
+                      double rho, int32_t cap, int32_t* b_out);
+
+/*
+ * Bytes of workspace an operation needs for the given shape.
+ *   op = SDKV_OP_SCORE:         (B, Hq, Hkv, d, n, W)       W = window length
+ *   op = SDKV_OP_SELECT:        (B, 0, Hkv, 0, n, 0)
+ *   op = SDKV_OP_SPARSE_DECODE: (B, Hq, Hkv, d, 0, 0)
+ *   op = SDKV_OP_DENSE_VERIFY:  (B, Hq, Hkv, d, n, gamma)   n = n_prefix + gamma
+ * Queries the current device's SM count.  Returns 0 for an invalid request.
+ */
+size_t sdkv_workspace_size(int32_t op, int32_t B, int32_t Hq, int32_t Hkv, int32_t d,
+                           int32_t n, int32_t gamma_or_W);
+
+/*
+ * Observation-window scores.  [StD] 3.2 (mean attention of the text queries
+ * to each key, GQA scores summed over the group) and [SparseMM] observation
+ * window (last 32 queries):
+ *     score[b][h][j] = (1/W) sum_{g in group(h)} sum_{t<W} P[b][h*G+g][t][j]
+ *     P[.][t][j]     = softmax over keys j <= q_pos0 + t of scale * q_t . k_j
+ * Window query t sits at position q_pos0 + t and sees keys 0 .. q_pos0 + t;
+ * keys it cannot see contribute 0.
+ *
+ *   q_obs     device bf16 [B][Hq][W][d], contiguous
+ *   k         device bf16 K cache (see conventions), rows 0 .. n-1 are read
+ *   k_strides host int64[3] element strides {batch, head, row}
+ *   n         keys scored, 1 <= n
+ *   W         window length, 1 <= W; q_pos0 >= 0 and q_pos0 + W <= n
+ *   scale     logit scale (usually 1/sqrt(d))
+ *   scores    device float [B][Hkv][n], contiguous (written)
+ * Needs Hq/Hkv * W <= 4096.
+ */
+int sdkv_score_obs_window(const void* q_obs, const void* k, const int64_t k_strides[3],
+                          int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t n,
+                          int32_t W, int32_t q_pos0, float scale, float* scores,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Top-K selection and list assembly.  [StD] 3.2 argTopK over the candidate
+ * (visual) keys; [SparseMM] K = r + b_score, the local window kept apart;
+ * [ByteCross] "Speedup Across Context": four sinks plus the highest-scoring
+ * entries of each KV head.
+ * For every (b, h), with k_h = offsets[bh+1] - offsets[bh] and
+ * K_h = k_h - n_sink - n_recent, the list indices[offsets[bh] .. +k_h) is
+ *     [0, n_sink)  +  top K_h of [cand_lo, cand_hi)  +  [n - n_recent, n)
+ * in ascending order.  Candidates rank by score descending, equal scores by
+ * lower index first; -0.0 equals +0.0; NaN ranks below every number.
+ *
+ *   scores   device float [B][Hkv][n] (as written by sdkv_score_obs_window)
+ *   cand_lo, cand_hi  candidate range; needs
+ *            0 <= n_sink <= cand_lo <= cand_hi <= n - n_recent
+ *   offsets  device int32 [B*Hkv + 1], non-decreasing
+ *   indices  device int32 [offsets[B*Hkv]] (written)
+ * A head whose K_h is outside [0, cand_hi - cand_lo] sets SDKV_DEV_BAD_LIST and
+ * its list is left unwritten.
+ */
+int sdkv_select_topk(const float* scores, int32_t B, int32_t Hkv, int32_t n,
+                     int32_t cand_lo, int32_t cand_hi, int32_t n_sink, int32_t n_recent,
+                     const int32_t* offsets, int32_t* indices,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Sparse decode attention over per-head index lists.  [StD] 3.2: the sparse
+ * model loads only the retained KV entries; [ByteCross] "The Byte Crossover":
+ * unselected entries stay allocated but unread.  For each (b, hq), with S the
+ * list of KV head h = hq / G:
+ *     o[b][hq]   = sum_{j in S} softmax_j(scale q . k_j) v_j
+ *     lse[b][hq] = log sum_{j in S} exp(scale q . k_j)        (natural log)
+ * An empty list gives o = 0 and lse = -inf.  Split-K over chunks of the lists
+ * with a log-sum-exp combine; fp32 accumulation, bf16 output.
+ *
+ *   q        device bf16 [B][Hq][d], contiguous
+ *   k, v     device bf16 caches (see conventions), kv_strides shared
+ *   n_cap    rows per head present in k and v; list entries must lie in
+ *            [0, n_cap) (others set SDKV_DEV_BAD_INDEX and read row 0)
+ *   offsets, indices  device int32 CSR lists per (b, h), as from sdkv_select_topk
+ *   o        device bf16 [B][Hq][d] (written)
+ *   lse      device float [B][Hq] (written) or NULL
+ * Needs Hq/Hkv <= 32 and B*Hkv <= 65536.
+ */
+int sdkv_sparse_decode_attn(const void* q, const void* k, const void* v,
+                            const int64_t kv_strides[3], int32_t n_cap,
+                            const int32_t* offsets, const int32_t* indices,
+                            int32_t B, int32_t Hq, int32_t Hkv, int32_t d, float scale,
+                            void* o, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Dense multi-query verify attention.  [StD] 3.1: the dense model verifies the
+ * gamma drafted tokens in parallel with one read of the full cache;
+ * [ByteCross] "The Attention Baseline": split-K dense decode.  The cache holds
+ * n_prefix + gamma rows; query t (t < gamma) sits at position n_prefix + t and
+ * attends keys 0 .. n_prefix + t:
+ *     o[b][hq][t]   = sum_{j <= n_prefix+t} softmax_j(scale q_t . k_j) v_j
+ *     lse[b][hq][t] = log sum_{j <= n_prefix+t} exp(scale q_t . k_j)
+ * gamma = 1 with n_prefix = n - 1 is the dense decode over n keys.
+ *
+ *   q        device bf16 [B][Hq][gamma][d], contiguous
+ *   k, v     device bf16 caches with at least n_prefix + gamma rows
+ *   o        device bf16 [B][Hq][gamma][d] (written)
+ *   lse      device float [B][Hq][gamma] (written) or NULL
+ * Needs (Hq/Hkv) * gamma <= 64, n_prefix >= 0, gamma >= 1.
+ */
+int sdkv_dense_verify_attn(const void* q, const void* k, const void* v,
+                           const int64_t kv_strides[3], int32_t B, int32_t Hq, int32_t Hkv,
+                           int32_t d, int32_t n_prefix, int32_t gamma, float scale,
+                           void* o, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Synchronous diagnostic: waits for `stream`, copies the device status word of
+ * the workspace to *status (one of SDKV_DEV_*), then clears it.
+ */
+int sdkv_workspace_status(void* ws, int32_t* status, void* stream);
+
+/* Message of the calling thread's last failed call ("" if none). */
+const char* sdkv_last_error(void);
+
+/* Library ABI version (major * 100 + minor). */
+int32_t sdkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDKV_H */

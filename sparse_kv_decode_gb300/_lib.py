@@ -1,0 +1,232 @@
+"""ctypes binding of libsdkv.so: argument marshalling only.
+
+Every function mirrors one C entry point of include/sdkv.h (same name without
+the `sdkv_` prefix).  Tensors are torch tensors: PyTorch supplies device memory
+and the current CUDA stream; all computation runs in the library's kernels.
+There is no fallback: if the library is missing or a call fails, an exception
+is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libsdkv.so")
+
+SDKV_OK = 0
+SDKV_ERR_INVALID_ARG = -1
+SDKV_ERR_UNSUPPORTED = -2
+SDKV_ERR_CUDA = -3
+SDKV_ERR_WORKSPACE = -4
+
+SDKV_DEV_OK = 0
+SDKV_DEV_TIMEOUT = 1
+SDKV_DEV_BAD_INDEX = 2
+SDKV_DEV_BAD_LIST = 3
+
+OP_SCORE = 1
+OP_SELECT = 2
+OP_SPARSE_DECODE = 3
+OP_DENSE_VERIFY = 4
+
+_c_i32 = ctypes.c_int32
+_c_i64 = ctypes.c_int64
+_c_vp = ctypes.c_void_p
+_c_sz = ctypes.c_size_t
+_c_f = ctypes.c_float
+_I64x3 = ctypes.c_int64 * 3
+
+
+class SdkvError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__("sdkv error %d: %s" % (code, msg))
+        self.code = code
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libsdkv.so (raises if it was not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libsdkv.so not built: run `python -m sparse_kv_decode_gb300.build` "
+                          "(or __graft_entry__.build())")
+    L = ctypes.CDLL(LIB_PATH)
+    L.sdkv_version.restype = _c_i32
+    L.sdkv_last_error.restype = ctypes.c_char_p
+    L.sdkv_head_budgets.argtypes = [ctypes.POINTER(ctypes.c_float), _c_i32, _c_i64, _c_i32,
+                                    ctypes.c_double, _c_i32, ctypes.POINTER(_c_i32)]
+    L.sdkv_head_budgets.restype = ctypes.c_int
+    L.sdkv_workspace_size.argtypes = [_c_i32] * 7
+    L.sdkv_workspace_size.restype = _c_sz
+    L.sdkv_score_obs_window.argtypes = [_c_vp, _c_vp, _I64x3, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
+                                        _c_i32, _c_i32, _c_f, _c_vp, _c_vp, _c_sz, _c_vp]
+    L.sdkv_score_obs_window.restype = ctypes.c_int
+    L.sdkv_select_topk.argtypes = [_c_vp, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
+                                   _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]
+    L.sdkv_select_topk.restype = ctypes.c_int
+    L.sdkv_sparse_decode_attn.argtypes = [_c_vp, _c_vp, _c_vp, _I64x3, _c_i32, _c_vp, _c_vp, _c_i32,
+                                          _c_i32, _c_i32, _c_i32, _c_f, _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]
+    L.sdkv_sparse_decode_attn.restype = ctypes.c_int
+    L.sdkv_dense_verify_attn.argtypes = [_c_vp, _c_vp, _c_vp, _I64x3, _c_i32, _c_i32, _c_i32, _c_i32,
+                                         _c_i32, _c_i32, _c_f, _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]
+    L.sdkv_dense_verify_attn.restype = ctypes.c_int
+    L.sdkv_workspace_status.argtypes = [_c_vp, ctypes.POINTER(_c_i32), _c_vp]
+    L.sdkv_workspace_status.restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _check(rc: int):
+    if rc != SDKV_OK:
+        raise SdkvError(rc, lib().sdkv_last_error().decode())
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def _stream(t=None) -> int:
+    dev = t.device if t is not None else None
+    return torch.cuda.current_stream(dev).cuda_stream
+
+
+def _need(t: torch.Tensor, name: str, dtype, cuda=True):
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if cuda and not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+
+
+def _kv_strides(k: torch.Tensor):
+    if k.dim() != 4 or k.stride(3) != 1:
+        raise ValueError("K/V must be [B][Hkv][rows][d] with d contiguous")
+    return _I64x3(k.stride(0), k.stride(1), k.stride(2))
+
+
+def version() -> int:
+    return int(lib().sdkv_version())
+
+
+def workspace_size(op: int, B: int, Hq: int, Hkv: int, d: int, n: int, gamma_or_w: int) -> int:
+    return int(lib().sdkv_workspace_size(op, B, Hq, Hkv, d, n, gamma_or_w))
+
+
+def new_workspace(nbytes: int, device) -> torch.Tensor:
+    """A zeroed workspace buffer (uint8) of at least `nbytes`, 256-byte rounded."""
+    nbytes = max(256, (int(nbytes) + 255) // 256 * 256)
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device)
+
+
+def workspace_status(ws: torch.Tensor) -> int:
+    st = _c_i32(0)
+    _check(lib().sdkv_workspace_status(ctypes.c_void_p(ws.data_ptr()), ctypes.byref(st),
+                                       ctypes.c_void_p(_stream(ws))))
+    return int(st.value)
+
+
+def head_budgets(s, total_B: int, w: int, rho: float, cap: int = 0) -> np.ndarray:
+    """sdkv_head_budgets on host arrays; returns int32 budgets."""
+    s = np.ascontiguousarray(np.asarray(s, dtype=np.float32).ravel())
+    out = np.zeros(s.size, dtype=np.int32)
+    _check(lib().sdkv_head_budgets(s.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), s.size,
+                                   int(total_B), int(w), float(rho), int(cap),
+                                   out.ctypes.data_as(ctypes.POINTER(_c_i32))))
+    return out
+
+
+def score_obs_window(q_obs: torch.Tensor, k: torch.Tensor, n: int, q_pos0: int, scale: float,
+                     scores: torch.Tensor | None = None, ws: torch.Tensor | None = None) -> torch.Tensor:
+    _need(q_obs, "q_obs", torch.bfloat16)
+    _need(k, "k", torch.bfloat16)
+    if not q_obs.is_contiguous():
+        raise ValueError("q_obs must be contiguous [B][Hq][W][d]")
+    B, Hq, W, d = q_obs.shape
+    Hkv = k.shape[1]
+    if scores is None:
+        scores = torch.empty((B, Hkv, n), dtype=torch.float32, device=q_obs.device)
+    _need(scores, "scores", torch.float32)
+    if ws is None:
+        ws = new_workspace(workspace_size(OP_SCORE, B, Hq, Hkv, d, n, W), q_obs.device)
+    _check(lib().sdkv_score_obs_window(q_obs.data_ptr(), k.data_ptr(), _kv_strides(k), B, Hq, Hkv, d, n,
+                                       W, q_pos0, scale, scores.data_ptr(), ws.data_ptr(), ws.numel(),
+                                       _stream(q_obs)))
+    return scores
+
+
+def select_topk(scores: torch.Tensor, n: int, cand_lo: int, cand_hi: int, n_sink: int, n_recent: int,
+                offsets: torch.Tensor, total: int, indices: torch.Tensor | None = None,
+                ws: torch.Tensor | None = None) -> torch.Tensor:
+    """`total` = offsets[-1] (list entries to allocate when `indices` is None)."""
+    _need(scores, "scores", torch.float32)
+    _need(offsets, "offsets", torch.int32)
+    if not scores.is_contiguous():
+        raise ValueError("scores must be contiguous [B][Hkv][n]")
+    B, Hkv = scores.shape[0], scores.shape[1]
+    if indices is None:
+        indices = torch.empty(max(int(total), 1), dtype=torch.int32, device=scores.device)
+    _need(indices, "indices", torch.int32)
+    if ws is None:
+        ws = new_workspace(workspace_size(OP_SELECT, B, 0, Hkv, 0, n, 0), scores.device)
+    _check(lib().sdkv_select_topk(scores.data_ptr(), B, Hkv, n, cand_lo, cand_hi, n_sink, n_recent,
+                                  offsets.data_ptr(), indices.data_ptr(), ws.data_ptr(), ws.numel(),
+                                  _stream(scores)))
+    return indices
+
+
+def sparse_decode_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, offsets: torch.Tensor,
+                       indices: torch.Tensor, scale: float, o: torch.Tensor | None = None,
+                       lse: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                       want_lse: bool = True):
+    for t, nm in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, nm, torch.bfloat16)
+    _need(offsets, "offsets", torch.int32)
+    _need(indices, "indices", torch.int32)
+    if not q.is_contiguous():
+        raise ValueError("q must be contiguous [B][Hq][d]")
+    if k.stride() != v.stride() or k.shape != v.shape:
+        raise ValueError("K and V must share shape and strides")
+    B, Hq, d = q.shape
+    Hkv, n_cap = k.shape[1], k.shape[2]
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = new_workspace(workspace_size(OP_SPARSE_DECODE, B, Hq, Hkv, d, 0, 0), q.device)
+    _check(lib().sdkv_sparse_decode_attn(q.data_ptr(), k.data_ptr(), v.data_ptr(), _kv_strides(k), n_cap,
+                                         offsets.data_ptr(), indices.data_ptr(), B, Hq, Hkv, d, scale,
+                                         o.data_ptr(), _ptr(lse), ws.data_ptr(), ws.numel(), _stream(q)))
+    return o, lse
+
+
+def dense_verify_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, n_prefix: int, scale: float,
+                      o: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                      ws: torch.Tensor | None = None, want_lse: bool = True):
+    for t, nm in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, nm, torch.bfloat16)
+    if not q.is_contiguous():
+        raise ValueError("q must be contiguous [B][Hq][gamma][d]")
+    if k.stride() != v.stride() or k.shape != v.shape:
+        raise ValueError("K and V must share shape and strides")
+    B, Hq, gamma, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape[2] < n_prefix + gamma:
+        raise ValueError("cache holds fewer than n_prefix + gamma rows")
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, gamma), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = new_workspace(workspace_size(OP_DENSE_VERIFY, B, Hq, Hkv, d, n_prefix + gamma, gamma), q.device)
+    _check(lib().sdkv_dense_verify_attn(q.data_ptr(), k.data_ptr(), v.data_ptr(), _kv_strides(k), B, Hq, Hkv,
+                                        d, n_prefix, gamma, scale, o.data_ptr(), _ptr(lse), ws.data_ptr(),
+                                        ws.numel(), _stream(q)))
+    return o, lse

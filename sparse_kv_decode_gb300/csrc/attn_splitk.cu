@@ -1,0 +1,767 @@
+// Split-K flash-decode attention for one decode step, dense and sparse.
+//
+// Dense (StD 3.1 verify, ByteCross split-K baseline): every CTA takes one
+// (batch, KV head) and one contiguous range of cache rows; all gamma x G query
+// rows of that KV head (the G query heads of the group at the gamma draft
+// positions, causal among the drafts) ride on the same pass over the rows, so
+// the cache is read exactly once.
+// Sparse (StD 3.2, ByteCross "Speedup Across Context"): every CTA takes one
+// chunk of one (batch, KV head)'s selected-index list and gathers those rows.
+//
+// CTA layout: one producer warp streams K and V tiles into a ring of shared
+// memory stages (TMA tensor copies with 128-byte swizzle for dense rows,
+// per-row bulk copies for gathered rows), completing on mbarriers; the
+// consumer warps run QK^T and PV on mma.sync (bf16 in, fp32 accumulate) with
+// an online softmax in the log2 domain.  Each CTA leaves an unnormalised
+// partial (o, m, l) per query row; the last CTA of a head to finish (atomic
+// ticket, no waiting) merges the partials with the log-sum-exp rule
+//     o = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s,   M = max_s m_s.
+#include "sdkv_common.cuh"
+#include "sdkv_internal.h"
+
+#include <algorithm>
+#include <cstring>
+
+namespace sdkv {
+
+struct AttnParams {
+    const bf16* q;
+    const bf16* k;
+    const bf16* v;
+    long long sb, sh, sn;
+    int B, Hq, Hkv, G, gamma, R;
+    bf16* o;
+    float* lse;
+    float scale_log2;
+    // dense
+    int n_prefix, n_total, chunk, nsplit;
+    // sparse
+    const int* offsets;
+    const int* indices;
+    int n_cap, BH, grid_target, min_chunk;
+    // workspace
+    int* status;
+    int* tickets;
+    float* part_o;
+    float* part_ml;
+};
+
+template <int D, int MT, int KW, int TK, int STAGES, bool SPARSE>
+struct AttnCfg {
+    static constexpr int NCW = MT * KW;          // consumer warps
+    static constexpr int NCT = NCW * 32;
+    static constexpr int NT = NCT + 32;          // + one producer warp
+    static constexpr int KPW = TK / KW;          // keys per consumer warp per stage
+    static_assert(KPW % 16 == 0, "keys per warp must be a multiple of 16");
+    static_assert(D == 64 || D == 128, "head dim");
+    static constexpr int ROWB = SPARSE ? (2 * D + 16) : (2 * D);
+    static constexpr int TILE_B = TK * ROWB;
+    static constexpr int QPITCH = 2 * D + 16;
+    static constexpr int ROWS = MT * 16;
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = STAGES * TILE_B;
+    static constexpr int OFF_Q = 2 * STAGES * TILE_B;
+    static constexpr int OFF_ML = OFF_Q + ROWS * QPITCH;
+    static constexpr int ML_FLOATS = KW * ROWS * 2;
+    static constexpr int OFF_BAR = OFF_ML + ML_FLOATS * 4;
+    static constexpr int SMEM = OFF_BAR + 2 * STAGES * 8;
+    static constexpr int SMEM_ALLOC = SMEM + 1024;
+    static constexpr int MRG_B = (KW - 1) * ROWS * D * 4;
+    static_assert(MRG_B <= 2 * STAGES * TILE_B, "merge buffer must fit in the stage buffers");
+    static_assert(SPARSE || (TILE_B % 1024) == 0, "swizzled stages need 1024-byte alignment");
+};
+
+template <int NT>
+__device__ __forceinline__ int block_excl_scan(int v, int* s_scan, int& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_scan[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = (lane < NT / 32) ? s_scan[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < NT / 32) s_scan[lane] = w;
+    }
+    __syncthreads();
+    const int res = (warp ? s_scan[warp - 1] : 0) + x - v;
+    total = s_scan[NT / 32 - 1];
+    __syncthreads();
+    return res;
+}
+
+// Key/value tile address of (row, 16-byte chunk) inside one stage.
+template <int D, int TK, bool SPARSE>
+__device__ __forceinline__ uint32_t tile_addr(uint32_t base, int row, int chunk) {
+    if constexpr (SPARSE) {
+        return pad_addr<2 * D + 16>(base, row, chunk);
+    } else {
+        return sw128_addr<TK>(base, row, chunk);
+    }
+}
+
+template <int D, int MT, int KW, int TK, int STAGES, bool SPARSE>
+__global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
+    attn_splitk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmk,
+                       const __grid_constant__ CUtensorMap tmv) {
+    using C = AttnCfg<D, MT, KW, TK, STAGES, SPARSE>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem =
+        reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t bar_full = sbase + C::OFF_BAR;
+    const uint32_t bar_empty = bar_full + STAGES * 8;
+
+    // work item: bh, key/position range [lo, hi), chunk id, chunks of the head, first chunk of the head
+    __shared__ int s_work[6];
+    __shared__ int s_scan[C::NT / 32];
+    __shared__ int s_tot;
+    __shared__ int s_abort;
+    __shared__ int s_last;
+
+    griddep_wait();
+
+    if constexpr (!SPARSE) {
+        if (tid == 0) {
+            const int bh = blockIdx.x / p.nsplit, sp = blockIdx.x % p.nsplit;
+            s_work[0] = bh;
+            s_work[1] = sp * p.chunk;
+            s_work[2] = min(sp * p.chunk + p.chunk, p.n_total);
+            s_work[3] = blockIdx.x;
+            s_work[4] = p.nsplit;
+            s_work[5] = bh * p.nsplit;
+        }
+    } else {
+        // Chunk plan, identical in every CTA: chunk length Cl = max(min_chunk,
+        // ceil(total / grid_target) rounded up to 16); head i owns
+        // max(1, ceil(k_i / Cl)) consecutive chunk ids.
+        if (tid == 0) {
+            s_tot = p.offsets[p.BH] - p.offsets[0];
+            s_work[0] = -1;
+        }
+        __syncthreads();
+        const int total = max(s_tot, 0);
+        int cl = (total + p.grid_target - 1) / p.grid_target;
+        cl = max(p.min_chunk, (cl + 15) & ~15);
+        const int c = blockIdx.x;
+        int running = 0;
+        for (int base = 0; base < p.BH; base += C::NT) {
+            const int i = base + tid;
+            int nch = 0, kh = 0, start = 0;
+            if (i < p.BH) {
+                start = p.offsets[i];
+                kh = p.offsets[i + 1] - start;
+                if (kh < 0) {
+                    flag_status(p.status, SDKV_DEV_BAD_LIST);
+                    kh = 0;
+                }
+                nch = max(1, (kh + cl - 1) / cl);
+            }
+            int tile_total;
+            const int excl = block_excl_scan<C::NT>(nch, s_scan, tile_total);
+            const int first = running + excl;
+            if (i < p.BH && c >= first && c < first + nch) {
+                const int j = c - first;
+                s_work[0] = i;
+                s_work[1] = start + j * cl;
+                s_work[2] = min(start + (j + 1) * cl, start + kh);
+                s_work[3] = c;
+                s_work[4] = nch;
+                s_work[5] = first;
+            }
+            running += tile_total;
+            __syncthreads();
+            if (s_work[0] >= 0 || running > c) break;
+        }
+    }
+    if (tid == 0) {
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, C::NCW);
+        }
+        fence_mbar_init();
+        s_abort = 0;
+    }
+    __syncthreads();
+    griddep_launch();
+
+    const int bh = s_work[0];
+    if (bh < 0) return;  // no chunk for this CTA (uniform)
+    const int lo = s_work[1], hi = s_work[2];
+    const int cidx = s_work[3], nch = s_work[4], c0 = s_work[5];
+    const int b = bh / p.Hkv, h = bh - (bh / p.Hkv) * p.Hkv;
+    const int nkeys = hi - lo;
+    const int ntiles = (nkeys + TK - 1) / TK;
+
+    // ------------------------------------------------------------------ producer
+    if (warp == C::NCW) {
+        if constexpr (SPARSE) {
+            const bf16* kb = p.k + b * p.sb + h * p.sh;
+            const bf16* vb = p.v + b * p.sb + h * p.sh;
+            for (int t = 0; t < ntiles; ++t) {
+                const int s = t % STAGES;
+                const uint32_t ph = (t / STAGES) & 1;
+                if (t >= STAGES) {
+                    bool ok = mbar_wait(bar_empty + 8 * s, ph ^ 1);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) {
+                        if (lane == 0) {
+                            flag_status(p.status, SDKV_DEV_TIMEOUT);
+                            atomicExch(&s_abort, 1);
+                        }
+                        break;
+                    }
+                }
+                if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * s, TK * 2 * (2 * D));
+                __syncwarp();
+                for (int i = lane; i < TK; i += 32) {
+                    const int pos = min(lo + t * TK + i, hi - 1);
+                    int idx = __ldg(p.indices + pos);
+                    if (static_cast<unsigned>(idx) >= static_cast<unsigned>(p.n_cap)) {
+                        flag_status(p.status, SDKV_DEV_BAD_INDEX);
+                        idx = 0;
+                    }
+                    bulk_g2s(sbase + C::OFF_K + s * C::TILE_B + i * C::ROWB, kb + idx * p.sn, 2 * D,
+                             bar_full + 8 * s);
+                    bulk_g2s(sbase + C::OFF_V + s * C::TILE_B + i * C::ROWB, vb + idx * p.sn, 2 * D,
+                             bar_full + 8 * s);
+                }
+            }
+        } else {
+            if (lane == 0) {
+                prefetch_tmap(&tmk);
+                prefetch_tmap(&tmv);
+                for (int t = 0; t < ntiles; ++t) {
+                    const int s = t % STAGES;
+                    const uint32_t ph = (t / STAGES) & 1;
+                    if (t >= STAGES && !mbar_wait(bar_empty + 8 * s, ph ^ 1)) {
+                        flag_status(p.status, SDKV_DEV_TIMEOUT);
+                        atomicExch(&s_abort, 1);
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar_full + 8 * s, 2 * TK * D * 2);
+                    const int row0 = lo + t * TK;
+#pragma unroll
+                    for (int half = 0; half < D / 64; ++half) {
+                        tma_load_4d(sbase + C::OFF_K + s * C::TILE_B + half * TK * 128, &tmk, half * 64, row0,
+                                    h, b, bar_full + 8 * s);
+                        tma_load_4d(sbase + C::OFF_V + s * C::TILE_B + half * TK * 128, &tmv, half * 64, row0,
+                                    h, b, bar_full + 8 * s);
+                    }
+                }
+            }
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------------ consumers
+    const int cw = warp;
+    const int mi = cw % MT, kw = cw / MT;
+
+    // query rows of this KV head -> shared memory (row r = g * gamma + t)
+    uint8_t* qs = smem + C::OFF_Q;
+    for (int e = tid; e < C::ROWS * (D / 8); e += C::NCT) {
+        const int r = e / (D / 8), c = e % (D / 8);
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (r < p.R) {
+            const int g = r / p.gamma, t = r - (r / p.gamma) * p.gamma;
+            const int hq = h * p.G + g;
+            val = *reinterpret_cast<const uint4*>(p.q + ((static_cast<size_t>(b) * p.Hq + hq) * p.gamma + t) * D +
+                                                  c * 8);
+        }
+        *reinterpret_cast<uint4*>(qs + r * C::QPITCH + c * 16) = val;
+    }
+    named_bar_sync(1, C::NCT);
+
+    uint32_t qa[D / 16][4];
+    {
+        const int row = mi * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+            ldsm_x4(qa[ks], pad_addr<C::QPITCH>(sbase + C::OFF_Q, row, 2 * ks + (lane >> 4)));
+    }
+
+    const int r0 = mi * 16 + (lane >> 2);
+    int lim[2] = {0x7fffffff, 0x7fffffff};
+    if constexpr (!SPARSE) {
+        lim[0] = p.n_prefix + (r0 % p.gamma);
+        lim[1] = p.n_prefix + ((r0 + 8) % p.gamma);
+    }
+
+    float o_acc[D / 8][4];
+#pragma unroll
+    for (int j = 0; j < D / 8; ++j) o_acc[j][0] = o_acc[j][1] = o_acc[j][2] = o_acc[j][3] = 0.f;
+    float m_r[2] = {-INFINITY, -INFINITY};
+    float l_r[2] = {0.f, 0.f};
+    bool aborted = false;
+
+    for (int t = 0; t < ntiles; ++t) {
+        const int s = t % STAGES;
+        const uint32_t ph = (t / STAGES) & 1;
+        if (!mbar_wait(bar_full + 8 * s, ph)) {
+            aborted = true;
+            break;
+        }
+        const uint32_t kst = sbase + C::OFF_K + s * C::TILE_B;
+        const uint32_t vst = sbase + C::OFF_V + s * C::TILE_B;
+#pragma unroll
+        for (int sub = 0; sub < C::KPW / 16; ++sub) {
+            const int krow0 = kw * C::KPW + sub * 16;
+            float sacc[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                uint32_t kb[4];
+                const int row = krow0 + (lane & 7) + ((lane >> 4) << 3);
+                ldsm_x4(kb, tile_addr<D, TK, SPARSE>(kst, row, 2 * ks + ((lane >> 3) & 1)));
+                mma_bf16_16816(sacc[0], qa[ks], kb[0], kb[1]);
+                mma_bf16_16816(sacc[1], qa[ks], kb[2], kb[3]);
+            }
+            // scale into the log2 domain and mask
+            const int cpos = t * TK + krow0 + 2 * (lane & 3);  // position within [lo, hi) of column (0, 0)
+            float x[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int col = cpos + nt * 8 + (e & 1);
+                    bool valid = col < nkeys;
+                    if constexpr (!SPARSE) valid = valid && (lo + col <= lim[e >> 1]);
+                    x[nt][e] = valid ? sacc[nt][e] * p.scale_log2 : -INFINITY;
+                }
+            }
+            // online softmax per row (rows r0 and r0 + 8; a quad shares a row)
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                float mx = fmaxf(fmaxf(x[0][2 * i], x[0][2 * i + 1]), fmaxf(x[1][2 * i], x[1][2 * i + 1]));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                const float mnew = fmaxf(m_r[i], mx);
+                const float muse = (mnew == -INFINITY) ? 0.f : mnew;
+                const float alpha = fast_exp2(m_r[i] - muse);
+                m_r[i] = mnew;
+                l_r[i] *= alpha;
+#pragma unroll
+                for (int j = 0; j < D / 8; ++j) {
+                    o_acc[j][2 * i] *= alpha;
+                    o_acc[j][2 * i + 1] *= alpha;
+                }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    x[nt][2 * i] = fast_exp2(x[nt][2 * i] - muse);
+                    x[nt][2 * i + 1] = fast_exp2(x[nt][2 * i + 1] - muse);
+                    l_r[i] += x[nt][2 * i] + x[nt][2 * i + 1];
+                }
+            }
+            uint32_t pa[4];
+            pa[0] = pack_bf16(x[0][0], x[0][1]);
+            pa[1] = pack_bf16(x[0][2], x[0][3]);
+            pa[2] = pack_bf16(x[1][0], x[1][1]);
+            pa[3] = pack_bf16(x[1][2], x[1][3]);
+#pragma unroll
+            for (int jj = 0; jj < D / 16; ++jj) {
+                uint32_t vb[4];
+                const int row = krow0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+                ldsm_x4_t(vb, tile_addr<D, TK, SPARSE>(vst, row, 2 * jj + (lane >> 4)));
+                mma_bf16_16816(o_acc[2 * jj], pa, vb[0], vb[1]);
+                mma_bf16_16816(o_acc[2 * jj + 1], pa, vb[2], vb[3]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+    }
+    if (aborted && lane == 0) flag_status(p.status, SDKV_DEV_TIMEOUT);
+
+    // -------------------------------------------------- merge the KW key-warps of a row block
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        l_r[i] += __shfl_xor_sync(0xffffffffu, l_r[i], 1);
+        l_r[i] += __shfl_xor_sync(0xffffffffu, l_r[i], 2);
+    }
+    // uniform decision among the consumers: stop if any of them (or the producer) gave up
+    if (named_bar_or(1, C::NCT, aborted || *reinterpret_cast<volatile int*>(&s_abort))) {
+        // drain: give every stage's copies a bounded chance to land before exit
+        if (tid == 0) {
+            for (int s = 0; s < STAGES && s < ntiles; ++s) {
+                const int last_t = ((ntiles - 1 - s) / STAGES) * STAGES + s;
+                mbar_wait(bar_full + 8 * s, (last_t / STAGES) & 1);
+            }
+        }
+        return;
+    }
+    float* ml = reinterpret_cast<float*>(smem + C::OFF_ML);
+    if ((lane & 3) == 0) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            ml[(kw * C::ROWS + r0 + 8 * i) * 2 + 0] = m_r[i];
+            ml[(kw * C::ROWS + r0 + 8 * i) * 2 + 1] = l_r[i];
+        }
+    }
+    named_bar_sync(1, C::NCT);
+    float Mrow[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int k2 = 0; k2 < KW; ++k2) M = fmaxf(M, ml[(k2 * C::ROWS + r0 + 8 * i) * 2]);
+        Mrow[i] = M;
+        const float f = (m_r[i] == -INFINITY) ? 0.f : fast_exp2(m_r[i] - M);
+        l_r[i] *= f;
+#pragma unroll
+        for (int j = 0; j < D / 8; ++j) {
+            o_acc[j][2 * i] *= f;
+            o_acc[j][2 * i + 1] *= f;
+        }
+    }
+    float* mrg = reinterpret_cast<float*>(smem + C::OFF_K);  // stage buffers are free now
+    if (KW > 1 && kw > 0) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            float* dst = mrg + ((kw - 1) * C::ROWS + r0 + 8 * i) * D + 2 * (lane & 3);
+#pragma unroll
+            for (int j = 0; j < D / 8; ++j)
+                *reinterpret_cast<float2*>(dst + 8 * j) = make_float2(o_acc[j][2 * i], o_acc[j][2 * i + 1]);
+            if ((lane & 3) == 0) ml[(kw * C::ROWS + r0 + 8 * i) * 2 + 1] = l_r[i];
+        }
+    }
+    named_bar_sync(1, C::NCT);
+
+    if (kw == 0) {
+#pragma unroll
+        for (int k2 = 1; k2 < KW; ++k2) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const float* src = mrg + ((k2 - 1) * C::ROWS + r0 + 8 * i) * D + 2 * (lane & 3);
+#pragma unroll
+                for (int j = 0; j < D / 8; ++j) {
+                    const float2 v2 = *reinterpret_cast<const float2*>(src + 8 * j);
+                    o_acc[j][2 * i] += v2.x;
+                    o_acc[j][2 * i + 1] += v2.y;
+                }
+                l_r[i] += ml[(k2 * C::ROWS + r0 + 8 * i) * 2 + 1];
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int row = r0 + 8 * i;
+            if (row >= p.R) continue;
+            const int g = row / p.gamma, tt = row - (row / p.gamma) * p.gamma;
+            const size_t orow = (static_cast<size_t>(b) * p.Hq + h * p.G + g) * p.gamma + tt;
+            if (nch == 1) {
+                const float L = l_r[i];
+                const float inv = L > 0.f ? 1.f / L : 0.f;
+                uint32_t* dst = reinterpret_cast<uint32_t*>(p.o + orow * D + 2 * (lane & 3));
+#pragma unroll
+                for (int j = 0; j < D / 8; ++j)
+                    dst[4 * j] = pack_bf16(o_acc[j][2 * i] * inv, o_acc[j][2 * i + 1] * inv);
+                if ((lane & 3) == 0 && p.lse)
+                    p.lse[orow] = L > 0.f ? (Mrow[i] + fast_log2(L)) * kLn2 : -INFINITY;
+            } else {
+                float* po = p.part_o + (static_cast<size_t>(cidx) * p.R + row) * D + 2 * (lane & 3);
+#pragma unroll
+                for (int j = 0; j < D / 8; ++j)
+                    *reinterpret_cast<float2*>(po + 8 * j) = make_float2(o_acc[j][2 * i], o_acc[j][2 * i + 1]);
+                if ((lane & 3) == 0) {
+                    float* pm = p.part_ml + (static_cast<size_t>(cidx) * p.R + row) * 2;
+                    pm[0] = Mrow[i];
+                    pm[1] = l_r[i];
+                }
+            }
+        }
+    }
+    if (nch == 1) return;
+
+    // -------------------------------------------------- last CTA of the head merges the partials
+    __threadfence();
+    named_bar_sync(1, C::NCT);
+    if (tid == 0) {
+        const int old = atomicAdd(p.tickets + bh, 1);
+        s_last = (old == nch - 1);
+    }
+    named_bar_sync(1, C::NCT);
+    if (!s_last) return;
+    __threadfence();
+
+    float* sM = ml;                 // [R] row max
+    float* sIL = ml + C::ML_FLOATS / 2;   // [R] 1 / row sum
+    for (int row = cw; row < p.R; row += C::NCW) {
+        float M = -INFINITY;
+        for (int s = lane; s < nch; s += 32)
+            M = fmaxf(M, __ldcg(p.part_ml + (static_cast<size_t>(c0 + s) * p.R + row) * 2));
+        M = warp_max(M);
+        float L = 0.f;
+        for (int s = lane; s < nch; s += 32) {
+            const float2 ml2 =
+                __ldcg(reinterpret_cast<const float2*>(p.part_ml + (static_cast<size_t>(c0 + s) * p.R + row) * 2));
+            if (ml2.x != -INFINITY) L += ml2.y * fast_exp2(ml2.x - M);
+        }
+        L = warp_sum(L);
+        if (lane == 0) {
+            sM[row] = M;
+            sIL[row] = L > 0.f ? 1.f / L : 0.f;
+            if (p.lse) {
+                const int g = row / p.gamma, tt = row - (row / p.gamma) * p.gamma;
+                const size_t orow = (static_cast<size_t>(b) * p.Hq + h * p.G + g) * p.gamma + tt;
+                p.lse[orow] = L > 0.f ? (M + fast_log2(L)) * kLn2 : -INFINITY;
+            }
+        }
+    }
+    named_bar_sync(1, C::NCT);
+    for (int e = tid; e < p.R * (D / 4); e += C::NCT) {
+        const int row = e / (D / 4), d4 = e - (e / (D / 4)) * (D / 4);
+        const float M = sM[row];
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        int s = 0;
+        for (; s + 8 <= nch; s += 8) {
+            float mv[8];
+            float4 ov[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const size_t base = static_cast<size_t>(c0 + s + u) * p.R + row;
+                mv[u] = __ldcg(p.part_ml + base * 2);
+                ov[u] = __ldcg(reinterpret_cast<const float4*>(p.part_o + base * D) + d4);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float w = (mv[u] == -INFINITY) ? 0.f : fast_exp2(mv[u] - M);
+                acc.x += w * ov[u].x;
+                acc.y += w * ov[u].y;
+                acc.z += w * ov[u].z;
+                acc.w += w * ov[u].w;
+            }
+        }
+        for (; s < nch; ++s) {
+            const size_t base = static_cast<size_t>(c0 + s) * p.R + row;
+            const float mv = __ldcg(p.part_ml + base * 2);
+            const float4 ov = __ldcg(reinterpret_cast<const float4*>(p.part_o + base * D) + d4);
+            const float w = (mv == -INFINITY) ? 0.f : fast_exp2(mv - M);
+            acc.x += w * ov.x;
+            acc.y += w * ov.y;
+            acc.z += w * ov.z;
+            acc.w += w * ov.w;
+        }
+        const float il = sIL[row];
+        const int g = row / p.gamma, tt = row - (row / p.gamma) * p.gamma;
+        const size_t orow = (static_cast<size_t>(b) * p.Hq + h * p.G + g) * p.gamma + tt;
+        uint2 packed;
+        packed.x = pack_bf16(acc.x * il, acc.y * il);
+        packed.y = pack_bf16(acc.z * il, acc.w * il);
+        *reinterpret_cast<uint2*>(p.o + orow * D + 4 * d4) = packed;
+    }
+    if (tid == 0) atomicExch(p.tickets + bh, 0);
+}
+
+// =====================================================================================
+// host side
+// =====================================================================================
+namespace {
+
+constexpr int kDenseTK = 64;
+constexpr int kDenseStages = 3;
+constexpr int kSparseTK = 64;
+constexpr int kSparseStages = 3;
+
+struct WsLayout {
+    int* status;
+    int* tickets;
+    float* part_o;
+    float* part_ml;
+    size_t bytes;
+};
+
+WsLayout attn_ws_layout(void* ws, int BH, int R, int d, int max_chunks) {
+    const size_t off_tickets = kWsHeader;
+    const size_t off_po = align256(off_tickets + sizeof(int) * static_cast<size_t>(BH));
+    const size_t off_pml = align256(off_po + sizeof(float) * static_cast<size_t>(max_chunks) * R * d);
+    const size_t end = align256(off_pml + sizeof(float) * static_cast<size_t>(max_chunks) * R * 2);
+    WsLayout L{};
+    L.bytes = end;
+    if (ws) {
+        uint8_t* base = static_cast<uint8_t*>(ws);
+        L.status = reinterpret_cast<int*>(base);
+        L.tickets = reinterpret_cast<int*>(base + off_tickets);
+        L.part_o = reinterpret_cast<float*>(base + off_po);
+        L.part_ml = reinterpret_cast<float*>(base + off_pml);
+    }
+    return L;
+}
+
+struct DensePlan {
+    int nsplit, chunk;
+};
+
+DensePlan dense_plan(int BH, int n_total, int num_sms) {
+    const int target = 2 * std::max(num_sms, 1);
+    int nsplit = std::max(1, (target + BH - 1) / BH);
+    const int max_split = (n_total + kDenseTK - 1) / kDenseTK;
+    nsplit = std::min(nsplit, std::max(1, max_split));
+    int chunk = (n_total + nsplit - 1) / nsplit;
+    chunk = ((chunk + kDenseTK - 1) / kDenseTK) * kDenseTK;
+    nsplit = (n_total + chunk - 1) / chunk;
+    return {nsplit, chunk};
+}
+
+int sparse_grid_target(int num_sms) { return 2 * std::max(num_sms, 1); }
+
+template <int D, int MT, int KW, int TK, int STAGES, bool SPARSE>
+cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv, int grid,
+                        cudaStream_t st) {
+    using C = AttnCfg<D, MT, KW, TK, STAGES, SPARSE>;
+    auto kern = attn_splitk_kernel<D, MT, KW, TK, STAGES, SPARSE>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static unsigned long long attr_set = 0;  // one bit per device, per instantiation
+    if (dev >= 64 || !(attr_set & (1ull << dev))) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+        if (e != cudaSuccess) return e;
+        if (dev < 64) attr_set |= (1ull << dev);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(C::NT);
+    cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p, tmk, tmv);
+}
+
+AttnParams make_params(const AttnLaunch& a) {
+    AttnParams p{};
+    p.q = static_cast<const bf16*>(a.q);
+    p.k = static_cast<const bf16*>(a.k);
+    p.v = static_cast<const bf16*>(a.v);
+    p.sb = a.sb;
+    p.sh = a.sh;
+    p.sn = a.sn;
+    p.B = a.B;
+    p.Hq = a.Hq;
+    p.Hkv = a.Hkv;
+    p.G = a.Hq / a.Hkv;
+    p.gamma = a.gamma;
+    p.R = p.G * a.gamma;
+    p.o = static_cast<bf16*>(a.o);
+    p.lse = a.lse;
+    p.scale_log2 = a.scale * kLog2e;
+    return p;
+}
+
+}  // namespace
+
+size_t dense_ws_bytes(int B, int Hq, int Hkv, int d, int n_total, int gamma, int num_sms) {
+    const int BH = B * Hkv;
+    const DensePlan pl = dense_plan(BH, n_total, num_sms);
+    const int R = (Hq / Hkv) * gamma;
+    return attn_ws_layout(nullptr, BH, R, d, BH * pl.nsplit).bytes;
+}
+
+size_t sparse_ws_bytes(int B, int Hq, int Hkv, int d, int num_sms) {
+    const int BH = B * Hkv;
+    const int R = Hq / Hkv;
+    return attn_ws_layout(nullptr, BH, R, d, sparse_grid_target(num_sms) + BH).bytes;
+}
+
+int launch_dense_verify(const AttnLaunch& a, const CUtensorMap* tmk, const CUtensorMap* tmv, int num_sms,
+                        const char** why) {
+    AttnParams p = make_params(a);
+    const int BH = a.B * a.Hkv;
+    p.n_prefix = a.n_prefix;
+    p.n_total = a.n_prefix + a.gamma;
+    const DensePlan pl = dense_plan(BH, p.n_total, num_sms);
+    p.nsplit = pl.nsplit;
+    p.chunk = pl.chunk;
+    WsLayout L = attn_ws_layout(a.ws, BH, p.R, a.d, BH * pl.nsplit);
+    if (a.ws_bytes < L.bytes) {
+        *why = "workspace smaller than sdkv_workspace_size(SDKV_OP_DENSE_VERIFY, ...)";
+        return SDKV_ERR_WORKSPACE;
+    }
+    p.status = L.status;
+    p.tickets = L.tickets;
+    p.part_o = L.part_o;
+    p.part_ml = L.part_ml;
+    const int grid = BH * pl.nsplit;
+    const int MT = (p.R + 15) / 16;
+    cudaError_t e = cudaErrorInvalidValue;
+    if (a.d == 128) {
+        switch (MT) {
+            case 1: e = launch_attn<128, 1, 4, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream); break;
+            case 2: e = launch_attn<128, 2, 2, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream); break;
+            case 3: e = launch_attn<128, 3, 2, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream); break;
+            case 4: e = launch_attn<128, 4, 2, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream); break;
+            default: *why = "(Hq/Hkv) * gamma must be <= 64"; return SDKV_ERR_UNSUPPORTED;
+        }
+    } else {
+        switch (MT) {
+            case 1: e = launch_attn<64, 1, 4, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream); break;
+            case 2: e = launch_attn<64, 2, 2, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream); break;
+            case 3: e = launch_attn<64, 3, 2, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream); break;
+            case 4: e = launch_attn<64, 4, 2, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream); break;
+            default: *why = "(Hq/Hkv) * gamma must be <= 64"; return SDKV_ERR_UNSUPPORTED;
+        }
+    }
+    if (e != cudaSuccess) {
+        *why = cudaGetErrorString(e);
+        return SDKV_ERR_CUDA;
+    }
+    return SDKV_OK;
+}
+
+int launch_sparse_decode(const AttnLaunch& a, int num_sms, const char** why) {
+    AttnParams p = make_params(a);
+    const int BH = a.B * a.Hkv;
+    p.offsets = a.offsets;
+    p.indices = a.indices;
+    p.n_cap = a.n_cap;
+    p.BH = BH;
+    p.grid_target = sparse_grid_target(num_sms);
+    p.min_chunk = kSparseTK;
+    const int max_chunks = p.grid_target + BH;
+    WsLayout L = attn_ws_layout(a.ws, BH, p.R, a.d, max_chunks);
+    if (a.ws_bytes < L.bytes) {
+        *why = "workspace smaller than sdkv_workspace_size(SDKV_OP_SPARSE_DECODE, ...)";
+        return SDKV_ERR_WORKSPACE;
+    }
+    p.status = L.status;
+    p.tickets = L.tickets;
+    p.part_o = L.part_o;
+    p.part_ml = L.part_ml;
+    CUtensorMap dummy;
+    memset(&dummy, 0, sizeof(dummy));
+    const int MT = (p.R + 15) / 16;
+    cudaError_t e = cudaErrorInvalidValue;
+    if (a.d == 128) {
+        switch (MT) {
+            case 1: e = launch_attn<128, 1, 4, kSparseTK, kSparseStages, true>(p, dummy, dummy, max_chunks, a.stream); break;
+            case 2: e = launch_attn<128, 2, 2, kSparseTK, kSparseStages, true>(p, dummy, dummy, max_chunks, a.stream); break;
+            default: *why = "Hq/Hkv must be <= 32"; return SDKV_ERR_UNSUPPORTED;
+        }
+    } else {
+        switch (MT) {
+            case 1: e = launch_attn<64, 1, 4, kSparseTK, kSparseStages, true>(p, dummy, dummy, max_chunks, a.stream); break;
+            case 2: e = launch_attn<64, 2, 2, kSparseTK, kSparseStages, true>(p, dummy, dummy, max_chunks, a.stream); break;
+            default: *why = "Hq/Hkv must be <= 32"; return SDKV_ERR_UNSUPPORTED;
+        }
+    }
+    if (e != cudaSuccess) {
+        *why = cudaGetErrorString(e);
+        return SDKV_ERR_CUDA;
+    }
+    return SDKV_OK;
+}
+
+}  // namespace sdkv

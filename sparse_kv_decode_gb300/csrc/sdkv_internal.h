@@ -1,0 +1,74 @@
+// Host-side interface between the C ABI layer (sdkv_api.cpp) and the kernel
+// translation units.  Not part of the public header.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace sdkv {
+
+struct DeviceInfo {
+    int device = -1;
+    int num_sms = 0;
+};
+DeviceInfo current_device();
+
+// Encode a 4-D bf16 tensor map over a KV cache [B][Hkv][rows][d] (d contiguous)
+// with a box of (64 elements, box_rows, 1, 1) and 128-byte swizzle.
+int encode_kv_tmap(CUtensorMap* map, const void* base, int B, int Hkv, int rows, int d,
+                   const int64_t strides[3], int box_rows);
+
+// ---- split-K attention (attn_splitk.cu) --------------------------------------
+struct AttnLaunch {
+    const void* q;
+    const void* k;
+    const void* v;
+    int64_t sb, sh, sn;
+    int B, Hq, Hkv, d, gamma;
+    void* o;
+    float* lse;
+    float scale;
+    // dense
+    int n_prefix;
+    // sparse
+    const int32_t* offsets;
+    const int32_t* indices;
+    int n_cap;
+    void* ws;
+    size_t ws_bytes;
+    cudaStream_t stream;
+};
+size_t dense_ws_bytes(int B, int Hq, int Hkv, int d, int n_total, int gamma, int num_sms);
+size_t sparse_ws_bytes(int B, int Hq, int Hkv, int d, int num_sms);
+int launch_dense_verify(const AttnLaunch& a, const CUtensorMap* tmk, const CUtensorMap* tmv,
+                        int num_sms, const char** why);
+int launch_sparse_decode(const AttnLaunch& a, int num_sms, const char** why);
+
+// ---- observation-window scoring (score_obs.cu) --------------------------------
+struct ScoreLaunch {
+    const void* q_obs;
+    int B, Hq, Hkv, d, n, W, q_pos0;
+    float scale;
+    float* scores;
+    void* ws;
+    size_t ws_bytes;
+    cudaStream_t stream;
+};
+size_t score_ws_bytes(int B, int Hq, int Hkv, int d, int n, int W, int num_sms);
+int launch_score(const ScoreLaunch& a, const CUtensorMap* tmk, int num_sms, const char** why);
+
+// ---- top-K selection (select_topk.cu) -------------------------------------------
+struct SelectLaunch {
+    const float* scores;
+    int B, Hkv, n, cand_lo, cand_hi, n_sink, n_recent;
+    const int32_t* offsets;
+    int32_t* indices;
+    void* ws;
+    cudaStream_t stream;
+};
+size_t select_ws_bytes(int B, int Hkv, int n);
+int launch_select(const SelectLaunch& a, const char** why);
+
+}  // namespace sdkv

@@ -1,0 +1,277 @@
+"""GPU parity: every hot-path kernel, called through the C ABI, against the fp64
+oracle on the same seeded inputs.  Small cases span several tiles with ragged
+tails; edge cases cover empty and single-entry lists, gamma > 1, odd group
+sizes, both head dims and non-contiguous caches."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_kv_decode_gb300 as sk
+import workloads
+from gpu_common import (assert_attn_close, assert_lse_close, assert_scores_close,
+                        check_selection_gap_rule, csr, f64, scale_of)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_kv_decode_gb300 import build
+    build.build()
+    sk.lib()
+
+
+def _rand(shape, gen, scale=1.0):
+    return (scale * torch.randn(shape, generator=gen)).to(torch.bfloat16)
+
+
+def _status_ok(ws):
+    assert sk.workspace_status(ws) == 0
+
+
+# ---------------------------------------------------------------------------
+# a5 dense verify / decode
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("B,Hq,Hkv,d,n_prefix,gamma", [
+    (1, 4, 4, 64, 1023, 1),       # tiny workload, dense decode
+    (1, 4, 4, 64, 1020, 4),       # tiny workload, gamma = 4 verify
+    (2, 8, 2, 128, 3000, 1),      # GQA 4, ragged tail
+    (1, 32, 8, 128, 5000, 8),     # 32 rows per KV head (two row tiles)
+    (1, 28, 4, 128, 2000, 5),     # video shape: 35 rows (three row tiles)
+    (1, 4, 1, 128, 700, 16),      # 64 rows (four row tiles)
+    (3, 6, 3, 64, 77, 3),         # short cache, fewer keys than a tile per split
+    (1, 2, 2, 128, 0, 1),         # a single key
+])
+def test_dense_verify_matches_oracle(B, Hq, Hkv, d, n_prefix, gamma):
+    g = torch.Generator().manual_seed(B * 1000 + Hq * 10 + gamma)
+    rows = n_prefix + gamma
+    k = _rand((B, Hkv, rows, d), g)
+    v = _rand((B, Hkv, rows, d), g)
+    q = _rand((B, Hq, gamma, d), g, 1.5)
+    ws = sk.new_workspace(sk.workspace_size(sk.OP_DENSE_VERIFY, B, Hq, Hkv, d, rows, gamma), DEV)
+    o, lse = sk.dense_verify_attn(q.to(DEV), k.to(DEV), v.to(DEV), n_prefix, scale_of(d), ws=ws)
+    o_ref, l_ref = oracle.dense_verify(q, k, v, n_prefix)
+    assert_attn_close(o, o_ref, "dense")
+    assert_lse_close(lse, l_ref, "dense")
+    _status_ok(ws)
+
+
+def test_dense_verify_strided_cache_and_repeat_calls():
+    # the cache has spare capacity rows (n_cap > n) and heads interleaved with
+    # batch: strides differ from a packed layout; the same workspace is reused
+    g = torch.Generator().manual_seed(5)
+    B, Hq, Hkv, d, n_prefix, gamma, n_cap = 2, 8, 4, 128, 1500, 3, 1600
+    big = _rand((Hkv, B, n_cap, d), g)
+    k = big.permute(1, 0, 2, 3)
+    v = _rand((Hkv, B, n_cap, d), g).permute(1, 0, 2, 3)
+    q = _rand((B, Hq, gamma, d), g)
+    ws = sk.new_workspace(sk.workspace_size(sk.OP_DENSE_VERIFY, B, Hq, Hkv, d, n_prefix + gamma, gamma), DEV)
+    kd, vd, qd = k.to(DEV), v.to(DEV), q.to(DEV)
+    assert kd.stride() == k.stride()
+    o_ref, l_ref = oracle.dense_verify(q, k, v, n_prefix)
+    for _ in range(3):
+        o, lse = sk.dense_verify_attn(qd, kd, vd, n_prefix, scale_of(d), ws=ws)
+        assert_attn_close(o, o_ref, "dense strided")
+        assert_lse_close(lse, l_ref, "dense strided")
+    _status_ok(ws)
+
+
+def test_verify_equals_sequential_single_decodes_on_gpu():
+    # StD 3.1: the one-pass verify of gamma drafts equals gamma single-token decodes
+    g = torch.Generator().manual_seed(11)
+    B, Hq, Hkv, d, n_prefix, gamma = 1, 32, 8, 128, 4096, 8
+    k = _rand((B, Hkv, n_prefix + gamma, d), g).to(DEV)
+    v = _rand((B, Hkv, n_prefix + gamma, d), g).to(DEV)
+    q = _rand((B, Hq, gamma, d), g).to(DEV)
+    o, lse = sk.dense_verify_attn(q, k, v, n_prefix, scale_of(d))
+    for t in range(gamma):
+        o1, l1 = sk.dense_verify_attn(q[:, :, t:t + 1].contiguous(), k, v, n_prefix + t, scale_of(d))
+        assert (f64(o[:, :, t]) - f64(o1[:, :, 0])).__abs__().max() <= 1e-2
+        assert (f64(lse[:, :, t]) - f64(l1[:, :, 0])).__abs__().max() <= 1e-4
+
+
+# ---------------------------------------------------------------------------
+# a4 sparse decode
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("B,Hq,Hkv,d,n,lens", [
+    (1, 4, 4, 64, 1024, [128, 128, 128, 128]),
+    (1, 32, 8, 128, 4096, [1229] * 8),
+    (2, 4, 4, 128, 3000, [0, 1, 2, 63, 64, 65, 500, 2999]),   # empty, single, tile edges, ragged
+    (1, 28, 4, 128, 2000, [1024, 1025, 1026, 1027]),
+    (1, 64, 2, 128, 1500, [700, 900]),                        # group 32: two row tiles
+    (1, 8, 8, 128, 6000, [3, 5000, 17, 1, 4096, 64, 0, 2048]),
+])
+def test_sparse_decode_matches_oracle(B, Hq, Hkv, d, n, lens):
+    g = torch.Generator().manual_seed(n + Hq)
+    k = _rand((B, Hkv, n, d), g)
+    v = _rand((B, Hkv, n, d), g)
+    q = _rand((B, Hq, d), g, 1.5)
+    offs_d, offs = csr(lens, DEV)
+    _, idx = workloads.random_lists(B, Hkv, n, lens, seed=n)
+    ws = sk.new_workspace(sk.workspace_size(sk.OP_SPARSE_DECODE, B, Hq, Hkv, d, 0, 0), DEV)
+    o, lse = sk.sparse_decode_attn(q.to(DEV), k.to(DEV), v.to(DEV), offs_d, idx.to(DEV), scale_of(d), ws=ws)
+    o_ref, l_ref = oracle.sparse_decode(q, k, v, offs, idx.numpy())
+    assert_attn_close(o, o_ref, "sparse")
+    assert_lse_close(lse, l_ref, "sparse")
+    _status_ok(ws)
+
+
+def test_sparse_keep_all_equals_dense_on_gpu():
+    g = torch.Generator().manual_seed(3)
+    B, Hq, Hkv, d, n = 1, 32, 8, 128, 5000
+    k = _rand((B, Hkv, n, d), g).to(DEV)
+    v = _rand((B, Hkv, n, d), g).to(DEV)
+    q = _rand((B, Hq, d), g).to(DEV)
+    offs_d, _ = csr([n] * (B * Hkv), DEV)
+    idx = torch.arange(n, dtype=torch.int32).repeat(B * Hkv).to(DEV)
+    o_s, l_s = sk.sparse_decode_attn(q, k, v, offs_d, idx, scale_of(d))
+    o_d, l_d = sk.dense_verify_attn(q[:, :, None].contiguous(), k, v, n - 1, scale_of(d))
+    assert (f64(o_s) - f64(o_d[:, :, 0])).__abs__().max() <= 1e-2
+    assert (f64(l_s) - f64(l_d[:, :, 0])).__abs__().max() <= 1e-4
+
+
+def test_sparse_bad_index_is_flagged_not_faulted():
+    g = torch.Generator().manual_seed(9)
+    B, Hq, Hkv, d, n = 1, 4, 2, 128, 256
+    k = _rand((B, Hkv, n, d), g).to(DEV)
+    v = _rand((B, Hkv, n, d), g).to(DEV)
+    q = _rand((B, Hq, d), g).to(DEV)
+    offs_d, _ = csr([3, 3], DEV)
+    idx = torch.tensor([0, 5, n + 7, 1, 2, -4], dtype=torch.int32, device=DEV)
+    ws = sk.new_workspace(sk.workspace_size(sk.OP_SPARSE_DECODE, B, Hq, Hkv, d, 0, 0), DEV)
+    sk.sparse_decode_attn(q, k, v, offs_d, idx, scale_of(d), ws=ws)
+    assert sk.workspace_status(ws) == 2      # SDKV_DEV_BAD_INDEX
+    assert sk.workspace_status(ws) == 0      # cleared by the read
+
+
+# ---------------------------------------------------------------------------
+# a2 window scoring
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("B,Hq,Hkv,d,n,W,q_pos0", [
+    (1, 4, 4, 64, 1024, 32, 992),        # tiny workload
+    (1, 32, 8, 128, 3000, 32, 2968),     # Llama GQA shape, ragged key tail
+    (2, 8, 4, 128, 777, 16, 700),        # window not at the end: later keys unseen
+    (1, 28, 4, 128, 1300, 40, 1260),     # group 7 x window 40 = 280 rows: three row blocks
+    (1, 4, 1, 64, 200, 64, 136),         # 256 rows: two full row blocks
+])
+def test_score_matches_oracle(B, Hq, Hkv, d, n, W, q_pos0):
+    g = torch.Generator().manual_seed(n + W)
+    q_obs = _rand((B, Hq, W, d), g, 1.5)
+    k = _rand((B, Hkv, n, d), g)
+    ws = sk.new_workspace(sk.workspace_size(sk.OP_SCORE, B, Hq, Hkv, d, n, W), DEV)
+    sc = sk.score_obs_window(q_obs.to(DEV), k.to(DEV), n, q_pos0, scale_of(d), ws=ws)
+    ref = oracle.score_obs_window(q_obs, k, n, q_pos0)
+    assert_scores_close(sc, ref, "score")
+    # every window row sums to one, so each KV head's scores sum to G
+    sums = f64(sc).sum(axis=2)
+    assert np.allclose(sums, Hq // Hkv, rtol=1e-4)
+    # deterministic: a second call gives identical bits
+    sc2 = sk.score_obs_window(q_obs.to(DEV), k.to(DEV), n, q_pos0, scale_of(d), ws=ws)
+    assert torch.equal(sc, sc2)
+    _status_ok(ws)
+
+
+# ---------------------------------------------------------------------------
+# a3 selection: on identical fp32 scores the lists must be bit-exact
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n,cand_lo,cand_hi,n_sink,n_recent,K", [
+    (1024, 4, 992, 4, 32, 92),
+    (5000, 4, 4936, 4, 64, 1000),
+    (300, 0, 300, 0, 0, 299),
+    (300, 0, 300, 0, 0, 1),
+    (300, 2, 290, 2, 10, 0),
+    (300, 2, 290, 2, 10, 288),
+    (20000, 0, 19968, 0, 32, 4000),
+])
+def test_select_exact_on_same_scores(n, cand_lo, cand_hi, n_sink, n_recent, K):
+    rng = np.random.default_rng(n + K)
+    B, Hkv = 2, 3
+    sc = rng.lognormal(0, 2, (B, Hkv, n)).astype(np.float32)
+    sc[0, 0] = np.round(sc[0, 0] * 4) / 4            # many exact ties
+    sc[0, 1, ::7] = 0.0
+    sc[0, 1, 1::7] = -0.0                             # -0.0 equals +0.0
+    sc[1, 2, ::5] = np.nan                            # NaN ranks last
+    sc[1, 1, :] = 0.5                                 # all equal
+    kh = n_sink + K + n_recent
+    offs_d, offs = csr([kh] * (B * Hkv), DEV)
+    scd = torch.from_numpy(sc).to(DEV)
+    idx = sk.select_topk(scd, n, cand_lo, cand_hi, n_sink, n_recent, offs_d, int(offs[-1]))
+    want = oracle.select_topk(sc, n, cand_lo, cand_hi, n_sink, n_recent, offs)
+    assert np.array_equal(idx.cpu().numpy()[: len(want)], want)
+
+
+def test_select_ragged_budgets_and_bad_list():
+    rng = np.random.default_rng(1)
+    B, Hkv, n = 1, 5, 4000
+    sc = rng.lognormal(0, 1, (B, Hkv, n)).astype(np.float32)
+    lens = [32, 33, 3968, 100, 2000]
+    offs_d, offs = csr(lens, DEV)
+    idx = sk.select_topk(torch.from_numpy(sc).to(DEV), n, 0, n - 32, 0, 32, offs_d, int(offs[-1]))
+    want = oracle.select_topk(sc, n, 0, n - 32, 0, 32, offs)
+    assert np.array_equal(idx.cpu().numpy(), want)
+    ws = sk.new_workspace(256, DEV)
+    offs_bad, _ = csr([10, 32, 32, 32, 32], DEV)    # 10 < n_recent: does not fit
+    sk.select_topk(torch.from_numpy(sc).to(DEV), n, 0, n - 32, 0, 32, offs_bad, 138, ws=ws)
+    assert sk.workspace_status(ws) == 3             # SDKV_DEV_BAD_LIST
+
+
+# ---------------------------------------------------------------------------
+# the whole path on the tiny and video-shaped workloads (small enough for the oracle)
+# ---------------------------------------------------------------------------
+
+def test_pipeline_tiny_workload():
+    w = workloads.WORKLOADS[1]
+    t = workloads.make_layer(w, 0)
+    gd = {k: v.to(DEV) for k, v in t.items()}
+    n, d, B, Hkv = w.n, w.d, w.batch, w.hkv
+    b = sk.head_budgets(np.ones(B * Hkv, np.float32), B * Hkv * w.keep[0], 0, 1.0)
+    offs_d, offs = csr(b, DEV)
+    sc = sk.score_obs_window(gd["q_obs"], gd["k"], n, w.q_pos0, scale_of(d))
+    idx = sk.select_topk(sc, n, w.cand_lo, w.cand_hi, w.n_sink, w.n_recent, offs_d, int(offs[-1]))
+    o, lse = sk.sparse_decode_attn(gd["q"], gd["k"], gd["v"], offs_d, idx, scale_of(d))
+    s_ref = oracle.score_obs_window(t["q_obs"], t["k"], n, w.q_pos0)
+    assert_scores_close(sc, s_ref, "tiny score")
+    exact = check_selection_gap_rule(idx.cpu().numpy(), offs, s_ref, n, w.cand_lo, w.cand_hi,
+                                     w.n_sink, w.n_recent)
+    assert exact >= 1
+    # attention over the GPU's own lists
+    o_ref, l_ref = oracle.sparse_decode(t["q"], t["k"], t["v"], offs, idx.cpu().numpy())
+    assert_attn_close(o, o_ref, "tiny sparse")
+    assert_lse_close(lse, l_ref, "tiny sparse")
+
+
+def test_pipeline_video_workload_reduced():
+    # video shape (group 7, 256 text window queries over visual frames), one
+    # layer at a reduced frame count so the oracle stays quick
+    w = workloads.WORKLOADS[3]
+    n = 8 * w.frame_tokens + w.text_tokens       # 8 frames + 256 text
+    t = workloads.make_layer(w, 0, n=n)
+    t["q_obs"] = t["q_obs"][:, :, : w.text_tokens].contiguous()
+    gd = {k: v.to(DEV) for k, v in t.items()}
+    m_v = n - w.text_tokens
+    sc = sk.score_obs_window(gd["q_obs"], gd["k"], n, m_v, scale_of(w.d))
+    s_ref = oracle.score_obs_window(t["q_obs"], t["k"], n, m_v)
+    assert_scores_close(sc, s_ref, "video score")
+    kh = w.text_tokens + 768
+    offs_d, offs = csr([kh] * w.hkv, DEV)
+    idx = sk.select_topk(sc, n, 0, m_v, 0, w.text_tokens, offs_d, int(offs[-1]))
+    check_selection_gap_rule(idx.cpu().numpy(), offs, s_ref, n, 0, m_v, 0, w.text_tokens)
+    o, lse = sk.sparse_decode_attn(gd["q"], gd["k"], gd["v"], offs_d, idx, scale_of(w.d))
+    o_ref, l_ref = oracle.sparse_decode(t["q"], t["k"], t["v"], offs, idx.cpu().numpy())
+    assert_attn_close(o, o_ref, "video sparse")
+    # StD verify of gamma = 5 drafts over the whole cache
+    ov, lv = sk.dense_verify_attn(gd["q_ver"], gd["k"], gd["v"], n - w.gamma, scale_of(w.d))
+    ov_ref, lv_ref = oracle.dense_verify(t["q_ver"], t["k"], t["v"], n - w.gamma)
+    assert_attn_close(ov, ov_ref, "video verify")
+    assert_lse_close(lv, lv_ref, "video verify")
