@@ -1,0 +1,543 @@
+#!/usr/bin/env python
+"""Benchmark of the sparse-KV decode hot path on one GB300 (or N replicas).
+
+One step = one pass of the whole path over one batch of synthetic input:
+  a1 head budgets (host)           -> per-head list lengths, copied to the device
+  a2 window scoring, every layer   -> fp32 scores
+  a3 top-K selection, every layer  -> per-head index lists
+  a4 sparse decode, every layer    -> o over the selected rows
+  a5 dense decode (split-K), every layer -> o over the full cache
+Each of a2..a5 is one CUDA graph of the per-layer library calls; CUDA events
+between the phases give each kernel's share of the step.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+instead (the reference arm: a deliberately slow program, on a bounded sample).
+"""
+import os
+
+# The oracle's CPU baseline runs single-threaded BLAS (reported as cores = 1).
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import dataclasses  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import math  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+from sparse_kv_decode_gb300 import byte_account as ba  # noqa: E402
+
+METRIC = "µs/decode-step and achieved HBM GB/s (% of GB300 peak), sparse vs dense attn"
+UNIT = "us/step"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="sdkv", choices=["sdkv", "reference"])
+    ap.add_argument("--workload", default="llama8b_32k")
+    ap.add_argument("--keep-index", type=int, default=0, help="which keep ratio of the workload")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="override the layer count (small profiling cases only; reported in config)")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("timestamp,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench.csv")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self, t0, t1, uuid=None):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                except Exception:
+                    ts = None
+                if uuid and parts[1] and uuid not in parts[1]:
+                    continue
+                rows.append((ts, parts))
+        win = [p for ts, p in rows if ts is None or (t0 - 0.3 <= ts <= t1 + 0.3)] or [p for _, p in rows]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(p[2]) for p in win if p[2].replace(".", "").isdigit()]
+        smax = [float(p[3]) for p in win if p[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for p in win:
+            for nm, val in zip(names, p[6:10]):
+                if val.strip().lower() in ("active", "1", "yes"):
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(win)}
+
+
+# ----------------------------------------------------------------------------- the path
+class Path:
+    """Device buffers and CUDA graphs of one step of the whole hot path."""
+
+    PHASES = ("score", "select", "sparse", "dense")
+
+    def __init__(self, w, keep_index, dev):
+        import sparse_kv_decode_gb300 as sk
+        self.sk = sk
+        self.w = w
+        self.dev = dev
+        L, B, Hq, Hkv, d, n = w.layers, w.batch, w.hq, w.hkv, w.d, w.n
+        self.L, self.B, self.Hq, self.Hkv, self.d, self.n = L, B, Hq, Hkv, d, n
+        self.BH = B * Hkv
+        self.scale = 1.0 / math.sqrt(d)
+        self.layers = [workloads.make_layer(w, l, device=dev) for l in range(L)]
+        # a1 inputs: head scores over the L x Hkv heads of one sequence
+        self.s_heads = workloads.head_scores(w).numpy()
+        if w.keep:
+            k_h = w.keep[keep_index]
+            self.budget_args = (L * Hkv * k_h, w.n_recent, 0.1, n)
+        else:
+            self.budget_args = (w.avg_budget * L * Hkv, w.w_local, w.rho, n)
+        # two pinned staging buffers for the a1 output, so the host never writes
+        # one that a copy still reads
+        self.offs_pinned = [torch.zeros((L, self.BH + 1), dtype=torch.int32).pin_memory() for _ in range(2)]
+        self.offs_done = [None, None]
+        self.flip = 0
+        self.offs_host = self.offs_pinned[0]
+        self.offs_dev = torch.zeros((L, self.BH + 1), dtype=torch.int32, device=dev)
+        self.budgets()
+        self.totals = [int(x) for x in self.offs_host[:, -1]]
+        self.offs_dev.copy_(self.offs_host)
+        self.scores = torch.empty((L, B, Hkv, n), dtype=torch.float32, device=dev)
+        self.idx = torch.empty((L, max(max(self.totals), 1)), dtype=torch.int32, device=dev)
+        self.o_sp = torch.empty((L, B, Hq, d), dtype=torch.bfloat16, device=dev)
+        self.l_sp = torch.empty((L, B, Hq), dtype=torch.float32, device=dev)
+        self.o_de = torch.empty((L, B, Hq, 1, d), dtype=torch.bfloat16, device=dev)
+        self.l_de = torch.empty((L, B, Hq, 1), dtype=torch.float32, device=dev)
+        self.q_de = [lay["q"][:, :, None, :].contiguous() for lay in self.layers]
+        self.ws_score = sk.new_workspace(sk.workspace_size(sk.OP_SCORE, B, Hq, Hkv, d, n, w.window), dev)
+        self.ws_sel = sk.new_workspace(sk.workspace_size(sk.OP_SELECT, B, 0, Hkv, 0, n, 0), dev)
+        self.ws_sp = sk.new_workspace(sk.workspace_size(sk.OP_SPARSE_DECODE, B, Hq, Hkv, d, 0, 0), dev)
+        self.ws_de = sk.new_workspace(sk.workspace_size(sk.OP_DENSE_VERIFY, B, Hq, Hkv, d, n, 1), dev)
+        self.graphs = {}
+
+    def budgets(self):
+        """a1 on the host: budgets of all L x Hkv heads; every sequence of the
+        batch gets lists of the same lengths."""
+        total_B, w_loc, rho, cap = self.budget_args
+        b = self.sk.head_budgets(self.s_heads, total_B, w_loc, rho, cap).reshape(self.L, self.Hkv)
+        per = np.tile(b, (1, self.B))                      # [L][B*Hkv], sequence-major
+        offs = self.offs_host.numpy()
+        offs[:, 0] = 0
+        np.cumsum(per, axis=1, out=offs[:, 1:])
+        return b
+
+    def phase_score(self):
+        w = self.w
+        for l, lay in enumerate(self.layers):
+            self.sk.score_obs_window(lay["q_obs"], lay["k"], self.n, w.q_pos0, self.scale,
+                                     scores=self.scores[l], ws=self.ws_score)
+
+    def phase_select(self):
+        w = self.w
+        for l in range(self.L):
+            self.sk.select_topk(self.scores[l], self.n, w.cand_lo, w.cand_hi, w.n_sink, w.n_recent,
+                                self.offs_dev[l], self.totals[l], indices=self.idx[l], ws=self.ws_sel)
+
+    def phase_sparse(self):
+        for l, lay in enumerate(self.layers):
+            self.sk.sparse_decode_attn(lay["q"], lay["k"], lay["v"], self.offs_dev[l], self.idx[l], self.scale,
+                                       o=self.o_sp[l], lse=self.l_sp[l], ws=self.ws_sp)
+
+    def phase_dense(self):
+        for l, lay in enumerate(self.layers):
+            self.sk.dense_verify_attn(self.q_de[l], lay["k"], lay["v"], self.n - 1, self.scale,
+                                      o=self.o_de[l], lse=self.l_de[l], ws=self.ws_de)
+
+    def capture(self):
+        # eager pass first (sets kernel attributes, checks everything runs)
+        for ph in self.PHASES:
+            getattr(self, "phase_" + ph)()
+        torch.cuda.synchronize()
+        for ph in self.PHASES:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                getattr(self, "phase_" + ph)()
+            self.graphs[ph] = g
+        torch.cuda.synchronize()
+
+    def step(self, evs=None):
+        self.flip ^= 1
+        if self.offs_done[self.flip] is not None:
+            self.offs_done[self.flip].synchronize()
+        self.offs_host = self.offs_pinned[self.flip]
+        self.budgets()
+        self.offs_dev.copy_(self.offs_host, non_blocking=True)
+        ev = torch.cuda.Event()
+        ev.record()
+        self.offs_done[self.flip] = ev
+        for i, ph in enumerate(self.PHASES):
+            if evs is not None:
+                evs[i].record()
+            self.graphs[ph].replay()
+        if evs is not None:
+            evs[len(self.PHASES)].record()
+
+    def launches_per_step(self):
+        return self.L * (2 + 1 + 1 + 1)   # score = 2 kernels, select, sparse, dense
+
+    def alg_bytes_per_layer(self):
+        mean_total = float(np.mean(self.totals))
+        return {
+            "score": ba.score_bytes(self.B, self.Hq, self.Hkv, self.d, self.n, self.w.window),
+            "select": ba.select_bytes(self.B, self.Hkv, self.n, int(mean_total)),
+            "sparse": ba.sparse_decode_bytes(self.B, self.Hq, self.d, int(mean_total)),
+            "dense": ba.dense_verify_bytes(self.B, self.Hq, self.Hkv, self.d, self.n - 1, 1),
+        }
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_kv_decode_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(phase):
+    """DRAM bytes per launch from profiles/dram_traffic.txt, if they were taken
+    with the current kernel sources (same source hash), else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    cur = kernel_source_hash()
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == phase and parts[2] == cur:
+                return float(parts[1])
+    return None
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+def oracle_units(w, layer_fn, n_units, rng_seed=0):
+    """Seconds per unit of the oracle on `n_units` sampled (layer, sequence, KV
+    head) units.  A unit is the whole path of one KV head: its window scores,
+    its top-K list, and the sparse and dense decode of its G query heads."""
+    import oracle
+    L, B, Hkv = w.layers, w.batch, w.hkv
+    G = w.hq // w.hkv
+    rng = np.random.default_rng(rng_seed)
+    units = [(int(rng.integers(L)), int(rng.integers(B)), int(rng.integers(Hkv))) for _ in range(n_units)]
+    kh = w.keep[0] if w.keep else w.avg_budget
+    total = 0.0
+    for (l, b, h) in units:
+        lay = layer_fn(l)
+        kk = lay["k"][b:b + 1, h:h + 1].cpu()
+        vv = lay["v"][b:b + 1, h:h + 1].cpu()
+        qo = lay["q_obs"][b:b + 1, h * G:(h + 1) * G].cpu()
+        qq = lay["q"][b:b + 1, h * G:(h + 1) * G].cpu()
+        t0 = time.perf_counter()
+        sc = oracle.score_obs_window(qo, kk, w.n, w.q_pos0)
+        offs = np.array([0, kh])
+        idx = oracle.select_topk(sc, w.n, w.cand_lo, w.cand_hi, w.n_sink, w.n_recent, offs)
+        oracle.sparse_decode(qq, kk, vv, offs, idx)
+        oracle.dense_verify(qq[:, :, None, :], kk, vv, w.n - 1)
+        total += time.perf_counter() - t0
+    return total / n_units
+
+
+def cpu_baseline(w, layer_fn, seconds):
+    per_unit = oracle_units(w, layer_fn, 1)
+    n_units = max(1, min(64, int(seconds / max(per_unit, 1e-3))))
+    per_unit = oracle_units(w, layer_fn, n_units, rng_seed=1)
+    units_per_step = w.layers * w.batch * w.hkv
+    return {
+        "value": per_unit * units_per_step * 1e6,
+        "unit": UNIT,
+        "cores": 1,
+        "kind": "oracle",
+        "sample": "%d (layer, sequence, KV head) units of the %s workload, each the whole path for one KV "
+                  "head (scores, top-K list, sparse and dense decode of its %d query heads), fp64 numpy, "
+                  "one BLAS thread; scaled by %d units per step" % (n_units, w.name, w.hq // w.hkv,
+                                                                    units_per_step),
+    }
+
+
+# ----------------------------------------------------------------------------- arms
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = workloads.by_name(args.workload)
+    cache = {}
+
+    def layer_fn(l):
+        if l not in cache:
+            cache.clear()
+            cache[l] = workloads.make_layer(w, l, device="cpu")
+        return cache[l]
+
+    warm = max(args.warmup, 3)
+    samples = []
+    for i in range(warm + args.steps):
+        per = oracle_units(w, layer_fn, 2, rng_seed=100 + i)
+        if i >= warm:
+            samples.append(per)
+    units_per_step = w.layers * w.batch * w.hkv
+    us = float(np.mean(samples)) * units_per_step * 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": warm, "ms_per_step": us / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "note": "fp64 CPU oracle; each step times 2 sampled (layer, "
+                   "sequence, KV head) units of the whole path and scales to the full step"},
+        "cpu_baseline": {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "2 (layer, sequence, KV head) units per step, scaled by %d" % units_per_step},
+        "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def run_e2e(path, K, world):
+    """The same step through the public API with the inputs in pinned host
+    memory: every step copies all layers' K, V, window queries and decode
+    queries to the device and reads the decode outputs back."""
+    host = []
+    h2d = 0
+    for lay in path.layers:
+        hl = {}
+        for name in ("k", "v", "q_obs", "q"):
+            t = torch.empty(lay[name].shape, dtype=lay[name].dtype, pin_memory=True)
+            t.copy_(lay[name])
+            hl[name] = t
+            h2d += t.numel() * t.element_size()
+        host.append(hl)
+    outs = [path.o_sp, path.l_sp, path.o_de, path.l_de]
+    out_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+
+    def step():
+        for lay, hl in zip(path.layers, host):
+            for name in ("k", "v", "q_obs", "q"):
+                lay[name].copy_(hl[name], non_blocking=True)
+        for l, lay in enumerate(path.layers):
+            path.q_de[l].copy_(lay["q"][:, :, None, :], non_blocking=True)
+        path.step()
+        for o, oh in zip(outs, out_host):
+            oh.copy_(o, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    s.record()
+    for _ in range(K):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(s.elapsed_time(e), world)
+    return {"value": ms / K * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": K}
+
+
+def run_sdkv(args, world, rank, local):
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for --impl sdkv")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workloads.by_name(args.workload)
+    if args.layers:
+        w = dataclasses.replace(w, layers=args.layers)
+    hbm_peak, peak_kind = peaks()
+    path = Path(w, args.keep_index, dev)
+    path.capture()
+    warm = max(args.warmup, 3)
+    K = args.steps
+    for _ in range(warm):
+        path.step()
+    torch.cuda.synchronize()
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler()
+    time.sleep(0.25)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(Path.PHASES) + 1)] for _ in range(K)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record()
+    for i in range(K):
+        path.step(evs[i])
+    end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    clocks = sampler.stop(t0, t1, uuid)
+    total_ms = max_over_ranks(start.elapsed_time(end), world)
+    phase_ms = {ph: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)) / K
+                for j, ph in enumerate(Path.PHASES)}
+    us_step = total_ms / K * 1e3
+
+    # device-side status words must be clean
+    for wsb in (path.ws_score, path.ws_sel, path.ws_sp, path.ws_de):
+        st = path.sk.workspace_status(wsb)
+        if st != 0:
+            raise SystemExit("device status %d raised during the bench" % st)
+
+    alg = path.alg_bytes_per_layer()
+    L = path.L
+    breakdown = {}
+    for ph in Path.PHASES:
+        per_layer_us = phase_ms[ph] * 1e3 / L
+        gbs = alg[ph] / (per_layer_us * 1e-6) / 1e9
+        breakdown[ph] = {"us_per_step": phase_ms[ph] * 1e3, "us_per_layer": per_layer_us,
+                         "alg_bytes_per_layer": alg[ph], "gbs": gbs,
+                         "frac_of_measured_hbm": gbs / hbm_peak, "frac_of_8tbs_nominal": gbs / NOMINAL_HBM_GBS}
+    dominant = max(Path.PHASES, key=lambda ph: phase_ms[ph])
+    dom = breakdown[dominant]
+    kernel_names = {"score": "sdkv_score_obs_window (score_kernel pass 1 + pass 2)",
+                    "select": "sdkv_select_topk (select_topk_kernel)",
+                    "sparse": "sdkv_sparse_decode_attn (attn_splitk_kernel, gathered)",
+                    "dense": "sdkv_dense_verify_attn (attn_splitk_kernel, dense)"}
+    roofline = {"bound": "hbm", "achieved": dom["gbs"], "peak": hbm_peak, "unit": "GB/s",
+                "frac": dom["gbs"] / hbm_peak, "traffic": traffic_from_profiles(dominant),
+                "kernel": kernel_names[dominant], "peak_kind": peak_kind,
+                "alg_bytes_per_launch": dom["alg_bytes_per_layer"], "us_per_launch": dom["us_per_layer"]}
+    keep = ("%d" % w.keep[args.keep_index]) if w.keep else "ragged SparseMM budgets"
+    line = {
+        "metric": METRIC, "value": us_step, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": warm,
+        "ms_per_step": us_step / 1e3, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "%s: %d layers x (%d q / %d KV heads, d=%d), batch %d, context %d, window %d, "
+                               "keep %s per head (%d sinks + %d recent + top-K)" % (
+                                   w.name, w.layers, w.hq, w.hkv, w.d, w.batch, w.n, w.window, keep,
+                                   w.n_sink, w.n_recent),
+                   "l2": "inputs larger than L2: %d distinct layers, %.2f GB of K/V per step" % (
+                       L, L * 2 * w.batch * w.hkv * w.n * w.d * 2 / 1e9),
+                   "step": "a1 budgets (host) + a2 score + a3 select + a4 sparse decode + a5 dense decode, "
+                           "all layers; a2..a5 one CUDA graph each"},
+        "sparse_vs_dense": {
+            "sparse_us_per_step": breakdown["sparse"]["us_per_step"],
+            "dense_us_per_step": breakdown["dense"]["us_per_step"],
+            "speedup": breakdown["dense"]["us_per_step"] / breakdown["sparse"]["us_per_step"],
+            "byte_bound": alg["dense"] / alg["sparse"],
+            "sparse_frac_of_measured_hbm": breakdown["sparse"]["frac_of_measured_hbm"],
+            "dense_frac_of_measured_hbm": breakdown["dense"]["frac_of_measured_hbm"],
+            "sparse_frac_of_8tbs": breakdown["sparse"]["frac_of_8tbs_nominal"],
+            "dense_frac_of_8tbs": breakdown["dense"]["frac_of_8tbs_nominal"],
+        },
+        "breakdown": breakdown,
+        "roofline": roofline,
+        "gpu_launches": path.launches_per_step() * K,
+        "clocks": clocks,
+    }
+    if not args.no_e2e:
+        line["e2e"] = run_e2e(path, min(K, 5), world)
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, lambda l: path.layers[l], args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_sdkv(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
