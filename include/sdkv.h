@@ -208,6 +208,37 @@ int sdkv_dense_verify_attn(const void* q, const void* k, const void* v,
                            void* o, float* lse, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Dense multi-query verify attention that allocates nothing.  The pages have
+ * no counterpart of this call; it exists for callers that cannot hand the
+ * library a workspace: programs whose device memory is owned by a pool they
+ * cannot draw from at this point (an inference server that fixes its memory
+ * at start-up, a plugin host that forbids cudaMalloc, a latency-critical loop
+ * where an allocation's implicit synchronisation would stall the stream).
+ *
+ * Computes exactly what sdkv_dense_verify_attn computes, with the same
+ * arguments except ws / ws_bytes.  Its scratch (split-K partials, per-head
+ * counters, status word) lives in one fixed device array of
+ * SDKV_NOALLOC_SCRATCH_BYTES inside the library, present on every GPU that
+ * loads the library until the process exits.  A shape that needs more scratch
+ * than that returns SDKV_ERR_UNSUPPORTED (use sdkv_dense_verify_attn then).
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any
+ *    stream capture.
+ *  - Each call clears the counters and status word it needs (an asynchronous
+ *    memset on `stream`, not an allocation) and calls no cudaMalloc/cudaFree.
+ *  - Every call on a device uses that device's one copy of the array: calls
+ *    that may overlap on the same GPU (for example on different streams) race
+ *    on it and give wrong results.  Serialise them.
+ * Device-side errors set the array's status word, which this API does not
+ * expose; argument errors are reported as for sdkv_dense_verify_attn.
+ */
+#define SDKV_NOALLOC_SCRATCH_BYTES (8u << 20)   /* 8 MiB */
+int sdkv_dense_verify_attn_noalloc(const void* q, const void* k, const void* v,
+                                   const int64_t kv_strides[3], int32_t B, int32_t Hq,
+                                   int32_t Hkv, int32_t d, int32_t n_prefix, int32_t gamma,
+                                   float scale, void* o, float* lse, void* stream);
+
+/*
  * Synchronous diagnostic: waits for `stream`, copies the device status word of
  * the workspace to *status (one of SDKV_DEV_*), then clears it.
  */

@@ -78,6 +78,9 @@ def lib() -> ctypes.CDLL:
     L.sdkv_dense_verify_attn.argtypes = [_c_vp, _c_vp, _c_vp, _I64x3, _c_i32, _c_i32, _c_i32, _c_i32,
                                          _c_i32, _c_i32, _c_f, _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]
     L.sdkv_dense_verify_attn.restype = ctypes.c_int
+    L.sdkv_dense_verify_attn_noalloc.argtypes = [_c_vp, _c_vp, _c_vp, _I64x3, _c_i32, _c_i32, _c_i32, _c_i32,
+                                                 _c_i32, _c_i32, _c_f, _c_vp, _c_vp, _c_vp]
+    L.sdkv_dense_verify_attn_noalloc.restype = ctypes.c_int
     L.sdkv_workspace_status.argtypes = [_c_vp, ctypes.POINTER(_c_i32), _c_vp]
     L.sdkv_workspace_status.restype = ctypes.c_int
     _lib = L
@@ -229,4 +232,25 @@ def dense_verify_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, n_prefi
     _check(lib().sdkv_dense_verify_attn(q.data_ptr(), k.data_ptr(), v.data_ptr(), _kv_strides(k), B, Hq, Hkv,
                                         d, n_prefix, gamma, scale, o.data_ptr(), _ptr(lse), ws.data_ptr(),
                                         ws.numel(), _stream(q)))
+    return o, lse
+
+
+def dense_verify_attn_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, n_prefix: int, scale: float,
+                              o: torch.Tensor, lse: torch.Tensor | None = None):
+    """sdkv_dense_verify_attn_noalloc: the dense verify with the library's fixed
+    scratch array instead of a workspace.  The caller passes the outputs; this
+    wrapper allocates nothing either."""
+    for t, nm in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
+        _need(t, nm, torch.bfloat16)
+    if not q.is_contiguous() or not o.is_contiguous():
+        raise ValueError("q and o must be contiguous [B][Hq][gamma][d]")
+    if k.stride() != v.stride() or k.shape != v.shape:
+        raise ValueError("K and V must share shape and strides")
+    B, Hq, gamma, d = q.shape
+    Hkv = k.shape[1]
+    if k.shape[2] < n_prefix + gamma:
+        raise ValueError("cache holds fewer than n_prefix + gamma rows")
+    _check(lib().sdkv_dense_verify_attn_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), _kv_strides(k), B, Hq,
+                                                Hkv, d, n_prefix, gamma, scale, o.data_ptr(), _ptr(lse),
+                                                _stream(q)))
     return o, lse

@@ -21,6 +21,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 
 namespace sdkv {
 
@@ -762,6 +763,64 @@ int launch_sparse_decode(const AttnLaunch& a, int num_sms, const char** why) {
         return SDKV_ERR_CUDA;
     }
     return SDKV_OK;
+}
+
+// -------------------------------------------------------------------------------------
+// Scratch for callers that cannot allocate device memory (see
+// sdkv_dense_verify_attn_noalloc): a fixed array in the library's own device
+// image.  Every GPU that loads the library holds it until the process exits.
+// The array's name in host code is only a host-side stand-in; the device address
+// comes from cudaGetSymbolAddress, once per device, with that device current.
+// -------------------------------------------------------------------------------------
+static __device__ __align__(256) uint8_t g_noalloc_scratch[SDKV_NOALLOC_SCRATCH_BYTES];
+
+int dense_verify_noalloc(const AttnLaunch& a_in, const CUtensorMap* tmk, const CUtensorMap* tmv, int num_sms,
+                         const char** why) {
+    static std::mutex mu;
+    static void* dev_ptr[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        *why = cudaGetErrorString(e);
+        return SDKV_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= 64) {
+        *why = "device ordinal above 63";
+        return SDKV_ERR_UNSUPPORTED;
+    }
+    const size_t need = dense_ws_bytes(a_in.B, a_in.Hq, a_in.Hkv, a_in.d, a_in.n_prefix + a_in.gamma, a_in.gamma,
+                                       num_sms);
+    if (need > static_cast<size_t>(SDKV_NOALLOC_SCRATCH_BYTES)) {
+        *why = "shape needs more scratch than the fixed SDKV_NOALLOC_SCRATCH_BYTES array of "
+               "sdkv_dense_verify_attn_noalloc holds (use sdkv_dense_verify_attn with a workspace)";
+        return SDKV_ERR_UNSUPPORTED;
+    }
+    void* ptr = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!dev_ptr[dev]) {
+            void* p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+            if (e != cudaSuccess || p == nullptr) {
+                *why = e != cudaSuccess ? cudaGetErrorString(e) : "cudaGetSymbolAddress returned null";
+                return SDKV_ERR_CUDA;
+            }
+            dev_ptr[dev] = p;
+        }
+        ptr = dev_ptr[dev];
+    }
+    // The array keeps the previous call's contents: the status word and the
+    // per-head counters must start at zero.
+    e = cudaMemsetAsync(ptr, 0, kWsHeader + align256(sizeof(int) * static_cast<size_t>(a_in.B) * a_in.Hkv),
+                        a_in.stream);
+    if (e != cudaSuccess) {
+        *why = cudaGetErrorString(e);
+        return SDKV_ERR_CUDA;
+    }
+    AttnLaunch a = a_in;
+    a.ws = ptr;
+    a.ws_bytes = SDKV_NOALLOC_SCRATCH_BYTES;
+    return launch_dense_verify(a, tmk, tmv, num_sms, why);
 }
 
 }  // namespace sdkv

@@ -352,6 +352,49 @@ int sdkv_dense_verify_attn(const void* q, const void* k, const void* v, const in
     return SDKV_OK;
 }
 
+int sdkv_dense_verify_attn_noalloc(const void* q, const void* k, const void* v, const int64_t kv_strides[3],
+                                   int32_t B, int32_t Hq, int32_t Hkv, int32_t d, int32_t n_prefix, int32_t gamma,
+                                   float scale, void* o, float* lse, void* stream) {
+    int rc = check_heads(B, Hq, Hkv, d);
+    if (rc) return rc;
+    if (!q || !o) return fail(SDKV_ERR_INVALID_ARG, "null q or o");
+    if (!aligned16(q) || !aligned16(o)) return fail(SDKV_ERR_INVALID_ARG, "q/o not 16-byte aligned");
+    if (!v) return fail(SDKV_ERR_INVALID_ARG, "null V pointer");
+    if ((rc = check_kv(k, v, kv_strides, d))) return rc;
+    if (n_prefix < 0 || gamma < 1) return fail(SDKV_ERR_INVALID_ARG, "need n_prefix >= 0 and gamma >= 1");
+    if (static_cast<int64_t>(n_prefix) + gamma > 0x7fffffff) return fail(SDKV_ERR_INVALID_ARG, "cache too long");
+    if (static_cast<int64_t>(Hq / Hkv) * gamma > 64) return fail(SDKV_ERR_UNSUPPORTED, "(Hq/Hkv) * gamma must be <= 64");
+    if (!std::isfinite(scale)) return fail(SDKV_ERR_INVALID_ARG, "scale must be finite");
+    const DeviceInfo dev = current_device();
+    if (dev.num_sms <= 0) return fail(SDKV_ERR_CUDA, "no CUDA device");
+    const int n_total = n_prefix + gamma;
+    CUtensorMap tmk, tmv;
+    if ((rc = encode_kv_tmap(&tmk, k, B, Hkv, n_total, d, kv_strides, 64))) return rc;
+    if ((rc = encode_kv_tmap(&tmv, v, B, Hkv, n_total, d, kv_strides, 64))) return rc;
+    AttnLaunch a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.sb = kv_strides[0];
+    a.sh = kv_strides[1];
+    a.sn = kv_strides[2];
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.d = d;
+    a.gamma = gamma;
+    a.o = o;
+    a.lse = lse;
+    a.scale = scale;
+    a.n_prefix = n_prefix;
+    a.stream = static_cast<cudaStream_t>(stream);
+    const char* why = "";
+    rc = dense_verify_noalloc(a, &tmk, &tmv, dev.num_sms, &why);
+    if (rc) return fail(rc, why);
+    g_last_error.clear();
+    return SDKV_OK;
+}
+
 int sdkv_workspace_status(void* ws, int32_t* status, void* stream) {
     if (!ws || !status) return fail(SDKV_ERR_INVALID_ARG, "null pointer");
     cudaStream_t st = static_cast<cudaStream_t>(stream);

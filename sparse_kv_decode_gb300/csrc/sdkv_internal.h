@@ -45,6 +45,9 @@ size_t sparse_ws_bytes(int B, int Hq, int Hkv, int d, int num_sms);
 int launch_dense_verify(const AttnLaunch& a, const CUtensorMap* tmk, const CUtensorMap* tmv,
                         int num_sms, const char** why);
 int launch_sparse_decode(const AttnLaunch& a, int num_sms, const char** why);
+// dense verify with its scratch in the library's fixed device array (no allocation)
+int dense_verify_noalloc(const AttnLaunch& a, const CUtensorMap* tmk, const CUtensorMap* tmv, int num_sms,
+                         const char** why);
 
 // ---- observation-window scoring (score_obs.cu) --------------------------------
 struct ScoreLaunch {
