@@ -51,11 +51,13 @@ template <int D, int MT, int KW, int TK, int STAGES, bool SPARSE>
 struct AttnCfg {
     static constexpr int NCW = MT * KW;          // consumer warps
     static constexpr int NCT = NCW * 32;
-    static constexpr int NT = NCT + 32;          // + one producer warp
+    static constexpr int NPW = SPARSE ? 2 : 1;   // producer warps (gathering rows needs more issuers)
+    static constexpr int NT = NCT + NPW * 32;
     static constexpr int KPW = TK / KW;          // keys per consumer warp per stage
     static_assert(KPW % 16 == 0, "keys per warp must be a multiple of 16");
     static_assert(D == 64 || D == 128, "head dim");
-    static constexpr int ROWB = SPARSE ? (2 * D + 16) : (2 * D);
+    static_assert(!SPARSE || TK == 32 * NPW, "one list entry per producer lane per tile");
+    static constexpr int ROWB = 2 * D;
     static constexpr int TILE_B = TK * ROWB;
     static constexpr int QPITCH = 2 * D + 16;
     static constexpr int ROWS = MT * 16;
@@ -69,7 +71,7 @@ struct AttnCfg {
     static constexpr int SMEM_ALLOC = SMEM + 1024;
     static constexpr int MRG_B = (KW - 1) * ROWS * D * 4;
     static_assert(MRG_B <= 2 * STAGES * TILE_B, "merge buffer must fit in the stage buffers");
-    static_assert(SPARSE || (TILE_B % 1024) == 0, "swizzled stages need 1024-byte alignment");
+    static_assert((TILE_B % 1024) == 0, "swizzled stages need 1024-byte alignment");
 };
 
 template <int NT>
@@ -99,14 +101,11 @@ __device__ __forceinline__ int block_excl_scan(int v, int* s_scan, int& total) {
     return res;
 }
 
-// Key/value tile address of (row, 16-byte chunk) inside one stage.
+// Key/value tile address of (row, 16-byte chunk) inside one stage: the 128-byte
+// swizzled layout TMA writes for dense tiles; gathered rows are placed the same way.
 template <int D, int TK, bool SPARSE>
 __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int row, int chunk) {
-    if constexpr (SPARSE) {
-        return pad_addr<2 * D + 16>(base, row, chunk);
-    } else {
-        return sw128_addr<TK>(base, row, chunk);
-    }
+    return sw128_addr<TK>(base, row, chunk);
 }
 
 template <int D, int MT, int KW, int TK, int STAGES, bool SPARSE>
@@ -145,6 +144,12 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
         // Chunk plan, identical in every CTA: chunk length Cl = max(min_chunk,
         // ceil(total / grid_target) rounded up to 16); head i owns
         // max(1, ceil(k_i / Cl)) consecutive chunk ids.
+        // the first tile of heads is loaded together with the total (one round trip)
+        int start = 0, kh = 0;
+        if (tid < p.BH) {
+            start = p.offsets[tid];
+            kh = p.offsets[tid + 1] - start;
+        }
         if (tid == 0) {
             s_tot = p.offsets[p.BH] - p.offsets[0];
             s_work[0] = -1;
@@ -157,10 +162,12 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
         int running = 0;
         for (int base = 0; base < p.BH; base += C::NT) {
             const int i = base + tid;
-            int nch = 0, kh = 0, start = 0;
-            if (i < p.BH) {
+            int nch = 0;
+            if (base > 0 && i < p.BH) {
                 start = p.offsets[i];
                 kh = p.offsets[i + 1] - start;
+            }
+            if (i < p.BH) {
                 if (kh < 0) {
                     flag_status(p.status, SDKV_DEV_BAD_LIST);
                     kh = 0;
@@ -187,7 +194,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
     if (tid == 0) {
 #pragma unroll
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_full + 8 * s, SPARSE ? C::NPW * 32 : 1);
             mbar_init(bar_empty + 8 * s, C::NCW);
         }
         fence_mbar_init();
@@ -205,11 +212,28 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
     const int ntiles = (nkeys + TK - 1) / TK;
 
     // ------------------------------------------------------------------ producer
-    if (warp == C::NCW) {
+    if (warp >= C::NCW) {
         if constexpr (SPARSE) {
+            // Gather: the NPW producer warps own 32 tile rows each; lane j of a warp
+            // holds the list entry of its warp's row j (loaded one tile ahead), and
+            // CPR lanes copy one row as CPR 16-byte chunks per instruction.
+            constexpr int CPR = D / 8;           // 16-byte chunks per row
+            constexpr int RPI = 32 / CPR;        // rows per warp instruction
+            const int pw = warp - C::NCW;
             const bf16* kb = p.k + b * p.sb + h * p.sh;
             const bf16* vb = p.v + b * p.sb + h * p.sh;
+            auto load_idx = [&](int t) -> int {
+                const int pos = min(lo + t * TK + pw * 32 + lane, hi - 1);
+                int idx = (t < ntiles) ? __ldg(p.indices + pos) : 0;
+                if (static_cast<unsigned>(idx) >= static_cast<unsigned>(p.n_cap)) {
+                    flag_status(p.status, SDKV_DEV_BAD_INDEX);
+                    idx = 0;
+                }
+                return idx;
+            };
+            int idx_cur = load_idx(0);
             for (int t = 0; t < ntiles; ++t) {
+                const int idx_next = load_idx(t + 1);
                 const int s = t % STAGES;
                 const uint32_t ph = (t / STAGES) & 1;
                 if (t >= STAGES) {
@@ -223,21 +247,22 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
                         break;
                     }
                 }
-                if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * s, TK * 2 * (2 * D));
-                __syncwarp();
-                for (int i = lane; i < TK; i += 32) {
-                    const int pos = min(lo + t * TK + i, hi - 1);
-                    int idx = __ldg(p.indices + pos);
-                    if (static_cast<unsigned>(idx) >= static_cast<unsigned>(p.n_cap)) {
-                        flag_status(p.status, SDKV_DEV_BAD_INDEX);
-                        idx = 0;
-                    }
-                    bulk_g2s(sbase + C::OFF_K + s * C::TILE_B + i * C::ROWB, kb + idx * p.sn, 2 * D,
-                             bar_full + 8 * s);
-                    bulk_g2s(sbase + C::OFF_V + s * C::TILE_B + i * C::ROWB, vb + idx * p.sn, 2 * D,
-                             bar_full + 8 * s);
+                const uint32_t kst = sbase + C::OFF_K + s * C::TILE_B;
+                const uint32_t vst = sbase + C::OFF_V + s * C::TILE_B;
+                const int chunk = lane % CPR;
+#pragma unroll 4
+                for (int it = 0; it < 32 / RPI; ++it) {
+                    const int rw = it * RPI + lane / CPR;     // row within this warp's 32
+                    const int idx = __shfl_sync(0xffffffffu, idx_cur, rw);
+                    const int row = pw * 32 + rw;
+                    const size_t off = static_cast<size_t>(idx) * p.sn + chunk * 8;
+                    cp_async_16(tile_addr<D, TK, SPARSE>(kst, row, chunk), kb + off);
+                    cp_async_16(tile_addr<D, TK, SPARSE>(vst, row, chunk), vb + off);
                 }
+                cp_async_mbar_arrive(bar_full + 8 * s);
+                idx_cur = idx_next;
             }
+            cp_async_wait_all();
         } else {
             if (lane == 0) {
                 prefetch_tmap(&tmk);
@@ -494,70 +519,95 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
     if (!s_last) return;
     __threadfence();
 
-    float* sM = ml;                 // [R] row max
-    float* sIL = ml + C::ML_FLOATS / 2;   // [R] 1 / row sum
+    // (1) per row: M = max_s m_s and L = sum_s 2^(m_s - M) l_s, one warp per row,
+    //     each lane merging its splits online, then a butterfly merge of the lanes
+    float* sM = ml;                        // [R] row max
+    float* sIL = ml + C::ML_FLOATS / 2;    // [R] 1 / row sum
     for (int row = cw; row < p.R; row += C::NCW) {
-        float M = -INFINITY;
-        for (int s = lane; s < nch; s += 32)
-            M = fmaxf(M, __ldcg(p.part_ml + (static_cast<size_t>(c0 + s) * p.R + row) * 2));
-        M = warp_max(M);
-        float L = 0.f;
+        float mm = -INFINITY, ll = 0.f;
         for (int s = lane; s < nch; s += 32) {
-            const float2 ml2 =
+            const float2 v2 =
                 __ldcg(reinterpret_cast<const float2*>(p.part_ml + (static_cast<size_t>(c0 + s) * p.R + row) * 2));
-            if (ml2.x != -INFINITY) L += ml2.y * fast_exp2(ml2.x - M);
+            if (v2.x == -INFINITY) continue;
+            if (v2.x > mm) {
+                ll = ll * fast_exp2(mm - v2.x) + v2.y;
+                mm = v2.x;
+            } else {
+                ll += v2.y * fast_exp2(v2.x - mm);
+            }
         }
-        L = warp_sum(L);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, mm, o);
+            const float l2 = __shfl_xor_sync(0xffffffffu, ll, o);
+            const float M = fmaxf(mm, m2);
+            if (M != -INFINITY) {
+                ll = (mm == -INFINITY ? 0.f : ll * fast_exp2(mm - M)) + (m2 == -INFINITY ? 0.f : l2 * fast_exp2(m2 - M));
+                mm = M;
+            }
+        }
         if (lane == 0) {
-            sM[row] = M;
-            sIL[row] = L > 0.f ? 1.f / L : 0.f;
+            sM[row] = mm;
+            sIL[row] = ll > 0.f ? 1.f / ll : 0.f;
             if (p.lse) {
                 const int g = row / p.gamma, tt = row - (row / p.gamma) * p.gamma;
                 const size_t orow = (static_cast<size_t>(b) * p.Hq + h * p.G + g) * p.gamma + tt;
-                p.lse[orow] = L > 0.f ? (M + fast_log2(L)) * kLn2 : -INFINITY;
+                p.lse[orow] = ll > 0.f ? (mm + fast_log2(ll)) * kLn2 : -INFINITY;
             }
         }
     }
     named_bar_sync(1, C::NCT);
+
+    // (2) o = sum_s w_s o_s with w_s = 2^(m_s - M) / L: the partial rows of a batch
+    //     of splits are staged into shared memory with cp.async (all in flight at
+    //     once), then each thread adds its (row, 4-dim) slots into an fp32
+    //     accumulator in shared memory.
+    constexpr int AREA = 2 * STAGES * C::TILE_B;   // the stage buffers are free now
+    float* acc = reinterpret_cast<float*>(smem + C::OFF_K);            // [R][D]
+    const int acc_b = p.R * D * 4;
+    const int per_split = p.R * D * 4 + p.R * 4;
+    const int batch = max(1, (AREA - acc_b - 16) / per_split);
+    float* wts = acc + p.R * D;                                         // [batch][R]
+    const int wts_b = ((batch * p.R * 4) + 15) & ~15;
+    uint8_t* stage = reinterpret_cast<uint8_t*>(wts) + wts_b;          // [batch][R][D]
+    const uint32_t stage_s = smem_u32(stage);
+    for (int e = tid; e < p.R * D; e += C::NCT) acc[e] = 0.f;
+    for (int s0 = 0; s0 < nch; s0 += batch) {
+        const int nb = min(batch, nch - s0);
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(p.part_o + static_cast<size_t>(c0 + s0) * p.R * D);
+        const int n16 = nb * p.R * (D / 4);
+        for (int e = tid; e < n16; e += C::NCT) cp_async_16(stage_s + e * 16, src + static_cast<size_t>(e) * 16);
+        for (int e = tid; e < nb * p.R; e += C::NCT) {
+            const int sl = e / p.R, row = e - (e / p.R) * p.R;
+            const float m = __ldcg(p.part_ml + (static_cast<size_t>(c0 + s0 + sl) * p.R + row) * 2);
+            wts[e] = (m == -INFINITY) ? 0.f : fast_exp2(m - sM[row]) * sIL[row];
+        }
+        cp_async_wait_all();
+        named_bar_sync(1, C::NCT);
+        const float4* st4 = reinterpret_cast<const float4*>(stage);
+        for (int e = tid; e < p.R * (D / 4); e += C::NCT) {
+            const int row = e / (D / 4);
+            float4 a4 = reinterpret_cast<float4*>(acc)[e];
+            for (int sl = 0; sl < nb; ++sl) {
+                const float w = wts[sl * p.R + row];
+                const float4 v4 = st4[sl * p.R * (D / 4) + e];
+                a4.x += w * v4.x;
+                a4.y += w * v4.y;
+                a4.z += w * v4.z;
+                a4.w += w * v4.w;
+            }
+            reinterpret_cast<float4*>(acc)[e] = a4;
+        }
+        named_bar_sync(1, C::NCT);
+    }
     for (int e = tid; e < p.R * (D / 4); e += C::NCT) {
         const int row = e / (D / 4), d4 = e - (e / (D / 4)) * (D / 4);
-        const float M = sM[row];
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        int s = 0;
-        for (; s + 8 <= nch; s += 8) {
-            float mv[8];
-            float4 ov[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const size_t base = static_cast<size_t>(c0 + s + u) * p.R + row;
-                mv[u] = __ldcg(p.part_ml + base * 2);
-                ov[u] = __ldcg(reinterpret_cast<const float4*>(p.part_o + base * D) + d4);
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const float w = (mv[u] == -INFINITY) ? 0.f : fast_exp2(mv[u] - M);
-                acc.x += w * ov[u].x;
-                acc.y += w * ov[u].y;
-                acc.z += w * ov[u].z;
-                acc.w += w * ov[u].w;
-            }
-        }
-        for (; s < nch; ++s) {
-            const size_t base = static_cast<size_t>(c0 + s) * p.R + row;
-            const float mv = __ldcg(p.part_ml + base * 2);
-            const float4 ov = __ldcg(reinterpret_cast<const float4*>(p.part_o + base * D) + d4);
-            const float w = (mv == -INFINITY) ? 0.f : fast_exp2(mv - M);
-            acc.x += w * ov.x;
-            acc.y += w * ov.y;
-            acc.z += w * ov.z;
-            acc.w += w * ov.w;
-        }
-        const float il = sIL[row];
+        const float4 a4 = reinterpret_cast<const float4*>(acc)[e];
         const int g = row / p.gamma, tt = row - (row / p.gamma) * p.gamma;
         const size_t orow = (static_cast<size_t>(b) * p.Hq + h * p.G + g) * p.gamma + tt;
         uint2 packed;
-        packed.x = pack_bf16(acc.x * il, acc.y * il);
-        packed.y = pack_bf16(acc.z * il, acc.w * il);
+        packed.x = pack_bf16(a4.x, a4.y);
+        packed.y = pack_bf16(a4.z, a4.w);
         *reinterpret_cast<uint2*>(p.o + orow * D + 4 * d4) = packed;
     }
     if (tid == 0) atomicExch(p.tickets + bh, 0);

@@ -8,11 +8,20 @@
 //           (x = scale * log2(e) * q.k); partial (m, l) per key split, merged by
 //           the last split CTA of the row block (atomic ticket) into (M, 1/L);
 //   pass 2: per key, sum over rows of 2^(x - M) / L.
-// Both passes: one producer warp streams K tiles with TMA (128-byte swizzle)
-// into an mbarrier ring; four consumer warps each own 32 window rows and run
-// QK^T on mma.sync.  A CTA covers 128 rows (one row block) and one key split;
-// more rows (large groups or windows) use more row blocks, whose partial key
-// sums are added in a fixed order by the last row block (deterministic).
+//
+// Both passes run the 128-row x 128-key x d contraction on the 5th-generation
+// tensor cores (tcgen05.mma, bf16 in, fp32 accumulators in tensor memory):
+//   pass 1: A = window rows (M = 128), B = key tile (N = 128): accumulator lane =
+//           row, so each epilogue thread owns one row and its statistics;
+//   pass 2: A = key tile (M = 128), B = window rows (N = 128): accumulator lane =
+//           key, so each epilogue thread sums its key's 128 row probabilities.
+// Warp roles: warp 0 streams the window rows once and the key tiles through a
+// ring of shared-memory stages with TMA (128-byte swizzle); warp 1 allocates
+// tensor memory and one of its threads issues the MMAs into two accumulator
+// buffers; warps 2..9 read the accumulators (tcgen05.ld) and do the softmax
+// arithmetic.  Every wait is bounded.  A CTA covers 128 window rows (one row
+// block) and one key split; larger groups or windows use more row blocks, whose
+// partial key sums are added in a fixed order by the last one (deterministic).
 #include "sdkv_common.cuh"
 #include "sdkv_internal.h"
 
@@ -21,7 +30,6 @@
 namespace sdkv {
 
 struct ScoreParams {
-    const bf16* q;
     int B, Hq, Hkv, G, W, R, n, q_pos0, BH, n_mg, nsplit, chunk;
     float scale_log2, inv_w;
     float* scores;
@@ -35,35 +43,48 @@ struct ScoreParams {
 
 template <int D>
 struct ScoreCfg {
-    static constexpr int NCW = 4;                 // consumer warps
-    static constexpr int MPW = 2;                 // 16-row tiles per consumer warp
-    static constexpr int ROWS = NCW * MPW * 16;   // 128 rows per CTA
-    static constexpr int NCT = NCW * 32;
-    static constexpr int NT = NCT + 32;
-    static constexpr int TK = 64;
-    static constexpr int STAGES = 4;
+    static constexpr int ROWS = 128;              // window rows per CTA (MMA M or N)
+    static constexpr int TK = 128;                // keys per tile (MMA N or M)
+    static constexpr int STAGES = 3;
+    static constexpr int HALVES = D / 64;         // 128-byte K-blocks per row
+    static constexpr int NEPI = 8;                // epilogue warps
+    static constexpr int NET = NEPI * 32;
+    static constexpr int NT = NET + 64;           // + producer warp + MMA warp
     static constexpr int TILE_B = TK * D * 2;
-    static constexpr int QPITCH = 2 * D + 16;
-    static constexpr int OFF_K = 0;
-    static constexpr int OFF_Q = STAGES * TILE_B;
-    static constexpr int OFF_RED = OFF_Q + ROWS * QPITCH;
-    static constexpr int OFF_BAR = OFF_RED + 2 * NCW * TK * 4;
-    static constexpr int SMEM = OFF_BAR + 2 * STAGES * 8;
+    static constexpr int Q_B = ROWS * D * 2;
+    static constexpr int HALF_B = TK * 128;       // one 64-wide K-block of a 128-row operand
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = Q_B;
+    static constexpr int OFF_CB = OFF_K + STAGES * TILE_B;     // pass 2: -M per row
+    static constexpr int OFF_CI = OFF_CB + ROWS * 4;           // pass 2: 1/L per row
+    static constexpr int OFF_LIM = OFF_CI + ROWS * 4;          // last visible key per row
+    static constexpr int OFF_RED = OFF_LIM + ROWS * 4;         // [2][TK] half sums / [ROWS][2] stats
+    static constexpr int OFF_BAR = OFF_RED + 2 * TK * 4;
+    static constexpr int NBAR = 2 * STAGES + 1 + 2 + 2;
+    static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
+    static constexpr int SMEM = OFF_TMEM + 16;
     static constexpr int SMEM_ALLOC = SMEM + 1024;
-    static_assert(TILE_B % 1024 == 0, "swizzled stage alignment");
+    static constexpr uint32_t TMEM_COLS = 2 * TK;  // two accumulator buffers
+    static constexpr uint32_t IDESC = idesc_bf16_f32(128, 128);
+    static_assert(ROWS == 128 && TK == 128, "one 128x128 MMA shape for both passes");
 };
 
 template <int D, bool PASS2>
-__global__ void __launch_bounds__(ScoreCfg<D>::NT)
-    score_kernel(const __grid_constant__ ScoreParams p, const __grid_constant__ CUtensorMap tmk) {
+__global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
+    score_kernel(const __grid_constant__ ScoreParams p, const __grid_constant__ CUtensorMap tmk,
+                 const __grid_constant__ CUtensorMap tmq) {
     using C = ScoreCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem =
         reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t bar_full = sbase + C::OFF_BAR;
-    const uint32_t bar_empty = bar_full + C::STAGES * 8;
+    const uint32_t bar_kfull = sbase + C::OFF_BAR;
+    const uint32_t bar_kempty = bar_kfull + 8 * C::STAGES;
+    const uint32_t bar_q = bar_kempty + 8 * C::STAGES;
+    const uint32_t bar_tfull = bar_q + 8;
+    const uint32_t bar_tempty = bar_tfull + 16;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM);
     __shared__ int s_abort;
     __shared__ int s_last;
 
@@ -75,267 +96,290 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT)
     const int lo = sp * p.chunk;
     const int hi = min(lo + p.chunk, p.n);
     const int ntiles = (hi - lo + C::TK - 1) / C::TK;
+    const int row_base = mg * C::ROWS;   // first window row (of R = G * W) of this CTA
 
     griddep_wait();
     if (tid == 0) {
 #pragma unroll
         for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, C::NCW);
+            mbar_init(bar_kfull + 8 * s, 1);
+            mbar_init(bar_kempty + 8 * s, 1);
+        }
+        mbar_init(bar_q, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_tfull + 8 * i, 1);
+            mbar_init(bar_tempty + 8 * i, C::NEPI);
         }
         fence_mbar_init();
         s_abort = 0;
     }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
     griddep_launch();
+    volatile int* abort_flag = &s_abort;
 
-    // ------------------------------------------------------------------ producer
-    if (warp == C::NCW) {
+    if (warp == 0) {
+        // ---------------------------------------------------------- TMA producer
         if (lane == 0) {
             prefetch_tmap(&tmk);
+            prefetch_tmap(&tmq);
+            // window rows of this row block: rows (b*Hq + h*G)*W + row_base ... +127 of
+            // the flattened [B*Hq*W][d] window queries (contiguous per KV head)
+            const int qrow0 = (b * p.Hq + h * p.G) * p.W + row_base;
+            mbar_arrive_expect_tx(bar_q, C::Q_B);
+#pragma unroll
+            for (int hf = 0; hf < C::HALVES; ++hf)
+                tma_load_2d(sbase + C::OFF_Q + hf * C::HALF_B, &tmq, hf * 64, qrow0, bar_q);
             for (int t = 0; t < ntiles; ++t) {
                 const int s = t % C::STAGES;
-                const uint32_t ph = (t / C::STAGES) & 1;
-                if (t >= C::STAGES && !mbar_wait(bar_empty + 8 * s, ph ^ 1)) {
+                if (t >= C::STAGES && !mbar_wait(bar_kempty + 8 * s, ((t / C::STAGES) & 1) ^ 1)) {
                     flag_status(p.status, SDKV_DEV_TIMEOUT);
-                    atomicExch(&s_abort, 1);
+                    *abort_flag = 1;
                     break;
                 }
-                mbar_arrive_expect_tx(bar_full + 8 * s, C::TILE_B);
+                if (*abort_flag) break;
+                mbar_arrive_expect_tx(bar_kfull + 8 * s, C::TILE_B);
 #pragma unroll
-                for (int half = 0; half < D / 64; ++half)
-                    tma_load_4d(sbase + C::OFF_K + s * C::TILE_B + half * C::TK * 128, &tmk, half * 64,
-                                lo + t * C::TK, h, b, bar_full + 8 * s);
+                for (int hf = 0; hf < C::HALVES; ++hf)
+                    tma_load_4d(sbase + C::OFF_K + s * C::TILE_B + hf * C::HALF_B, &tmk, hf * 64, lo + t * C::TK,
+                                h, b, bar_kfull + 8 * s);
             }
         }
-        return;
-    }
-
-    // ------------------------------------------------------------------ consumers
-    const int row_base = mg * C::ROWS;  // first window row (of R = G * W) of this CTA
-    uint8_t* qs = smem + C::OFF_Q;
-    for (int e = tid; e < C::ROWS * (D / 8); e += C::NCT) {
-        const int lr = e / (D / 8), c = e % (D / 8);
-        const int r = row_base + lr;
-        uint4 val = make_uint4(0u, 0u, 0u, 0u);
-        if (r < p.R) {
-            const int g = r / p.W, t = r - (r / p.W) * p.W;
-            const int hq = h * p.G + g;
-            val = *reinterpret_cast<const uint4*>(p.q + ((static_cast<size_t>(b) * p.Hq + hq) * p.W + t) * D +
-                                                  c * 8);
-        }
-        *reinterpret_cast<uint4*>(qs + lr * C::QPITCH + c * 16) = val;
-    }
-    named_bar_sync(1, C::NCT);
-
-    uint32_t qa[C::MPW][D / 16][4];
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            bool ok = mbar_wait(bar_q, 0);
+            for (int t = 0; ok && t < ntiles; ++t) {
+                const int s = t % C::STAGES, buf = t & 1;
+                ok = mbar_wait(bar_kfull + 8 * s, (t / C::STAGES) & 1);
+                if (ok && t >= 2) ok = mbar_wait(bar_tempty + 8 * buf, ((t >> 1) & 1) ^ 1);
+                if (!ok || *abort_flag) break;
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + buf * C::TK;
+                const uint32_t kst = sbase + C::OFF_K + s * C::TILE_B;
 #pragma unroll
-    for (int mt = 0; mt < C::MPW; ++mt) {
-        const int row = warp * (C::MPW * 16) + mt * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-            ldsm_x4(qa[mt][ks], pad_addr<C::QPITCH>(sbase + C::OFF_Q, row, 2 * ks + (lane >> 4)));
-    }
-
-    // rows of this thread: (mt, i) -> local row warp*32 + mt*16 + lane/4 + 8i
-    int lim[C::MPW][2];
-    float rM[C::MPW][2], rIL[C::MPW][2];  // pass 2: row max and 1/sum
-    float m_r[C::MPW][2], l_r[C::MPW][2]; // pass 1: running stats (this thread's columns)
-#pragma unroll
-    for (int mt = 0; mt < C::MPW; ++mt) {
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int r = row_base + warp * (C::MPW * 16) + mt * 16 + (lane >> 2) + 8 * i;
-            const int t = r % p.W;
-            lim[mt][i] = (r < p.R) ? p.q_pos0 + t : -1;
-            m_r[mt][i] = -INFINITY;
-            l_r[mt][i] = 0.f;
-            rM[mt][i] = 0.f;
-            rIL[mt][i] = 0.f;
-            if (PASS2 && r < p.R) {
-                const float2 st = __ldcg(reinterpret_cast<const float2*>(p.st_final + (static_cast<size_t>(bh) * p.R + r) * 2));
-                rM[mt][i] = st.x;
-                rIL[mt][i] = st.y;
-            }
-        }
-    }
-    float* red = reinterpret_cast<float*>(smem + C::OFF_RED);  // [2][NCW][TK]
-    bool aborted = false;
-
-    for (int t = 0; t < ntiles; ++t) {
-        const int s = t % C::STAGES;
-        const uint32_t ph = (t / C::STAGES) & 1;
-        const bool bad = !mbar_wait(bar_full + 8 * s, ph);
-        if (bad) aborted = true;
-        if (!PASS2 && bad) break;  // pass 1 has no barrier inside the loop
-        const uint32_t kst = sbase + C::OFF_K + s * C::TILE_B;
-        float* redb = red + (t & 1) * (C::NCW * C::TK);
-#pragma unroll 1
-        for (int sub = 0; sub < (bad ? 0 : C::TK / 16); ++sub) {
-            const int krow0 = sub * 16;
-            float sacc[C::MPW][2][4];
-#pragma unroll
-            for (int mt = 0; mt < C::MPW; ++mt)
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) sacc[mt][nt][0] = sacc[mt][nt][1] = sacc[mt][nt][2] = sacc[mt][nt][3] = 0.f;
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                uint32_t kb[4];
-                const int row = krow0 + (lane & 7) + ((lane >> 4) << 3);
-                ldsm_x4(kb, sw128_addr<C::TK>(kst, row, 2 * ks + ((lane >> 3) & 1)));
-#pragma unroll
-                for (int mt = 0; mt < C::MPW; ++mt) {
-                    mma_bf16_16816(sacc[mt][0], qa[mt][ks], kb[0], kb[1]);
-                    mma_bf16_16816(sacc[mt][1], qa[mt][ks], kb[2], kb[3]);
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks >> 2) * C::HALF_B + (ks & 3) * 32;
+                    const uint64_t qd = sw128_kmajor_desc(sbase + C::OFF_Q + off);
+                    const uint64_t kd = sw128_kmajor_desc(kst + off);
+                    if (PASS2)
+                        tc_mma_bf16(d_tmem, kd, qd, C::IDESC, ks > 0);
+                    else
+                        tc_mma_bf16(d_tmem, qd, kd, C::IDESC, ks > 0);
                 }
+                tc_commit(bar_kempty + 8 * s);    // the stage is free once these MMAs are done
+                tc_commit(bar_tfull + 8 * buf);   // and the accumulator is ready
             }
-            const int key0 = lo + t * C::TK + krow0 + 2 * (lane & 3);
+            if (!ok) {
+                flag_status(p.status, SDKV_DEV_TIMEOUT);
+                *abort_flag = 1;
+            }
+        }
+    } else {
+        // ---------------------------------------------------------- epilogue
+        const int ew = warp - 2;
+        const int quad = warp & 3;          // tensor-memory lanes 32*quad .. +31
+        const int half = ew >> 2;           // accumulator columns half*64 .. +63
+        const int tl = 32 * quad + lane;    // accumulator lane of this thread
+        float* cb = reinterpret_cast<float*>(smem + C::OFF_CB);
+        float* ci = reinterpret_cast<float*>(smem + C::OFF_CI);
+        int* lim = reinterpret_cast<int*>(smem + C::OFF_LIM);
+        float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
+        const int et = ew * 32 + lane;      // 0 .. NET-1
+        if (et < C::ROWS) {
+            const int r = row_base + et;
+            lim[et] = (r < p.R) ? p.q_pos0 + r % p.W : -1;
+            if (PASS2) {
+                float2 st = make_float2(INFINITY, 0.f);   // rows past R: -M = -inf, 1/L = 0
+                if (r < p.R)
+                    st = __ldcg(reinterpret_cast<const float2*>(p.st_final + (static_cast<size_t>(bh) * p.R + r) * 2));
+                cb[et] = -st.x;
+                ci[et] = st.y;
+            }
+        }
+        named_bar_sync(1, C::NET);
+        const float c = p.scale_log2;
+        // pass 1 state (row tl)
+        const int my_lim = lim[tl];
+        float m_run = -INFINITY, l_run = 0.f;
+        bool aborted = false;
+
+        for (int t = 0; t < ntiles; ++t) {
+            const int buf = t & 1;
+            const bool bad = !mbar_wait(bar_tfull + 8 * buf, (t >> 1) & 1);
+            if (bad) aborted = true;
+            uint32_t v[64];
+            if (!bad) {
+                tc_fence_after();
+                const uint32_t ta = tmem + (static_cast<uint32_t>(32 * quad) << 16) + buf * C::TK + half * 64;
+                tmem_ld32(ta, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+                tmem_ld32(ta + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+                tmem_wait_ld();
+                tc_fence_before();
+            }
+            __syncwarp();
+            if (lane == 0 && !bad) mbar_arrive(bar_tempty + 8 * buf);
+            const int key0 = lo + t * C::TK;
             if constexpr (!PASS2) {
+                if (bad) break;
+                if (my_lim >= 0) {
+                    // columns are keys key0 + half*64 + i
+                    const int kfirst = key0 + half * 64;
+                    const bool full = (kfirst + 63 < hi) && (kfirst + 63 <= my_lim);
+                    float mx = -INFINITY;
+                    if (full) {
 #pragma unroll
-                for (int mt = 0; mt < C::MPW; ++mt) {
+                        for (int i = 0; i < 64; ++i) mx = fmaxf(mx, __uint_as_float(v[i]));
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        float x[4];
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const int nt = q4 >> 1, e = q4 & 1;
-                            const int key = key0 + nt * 8 + e;
-                            const bool valid = key < hi && key <= lim[mt][i];
-                            x[q4] = valid ? sacc[mt][nt][2 * i + e] * p.scale_log2 : -INFINITY;
+                        for (int i = 0; i < 64; ++i) {
+                            const int key = kfirst + i;
+                            const float x = (key < hi && key <= my_lim) ? __uint_as_float(v[i]) : -INFINITY;
+                            v[i] = __float_as_uint(x);
+                            mx = fmaxf(mx, x);
                         }
-                        const float tmax = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-                        const float mnew = fmaxf(m_r[mt][i], tmax);
-                        if (mnew != -INFINITY) {
-                            l_r[mt][i] = l_r[mt][i] * fast_exp2(m_r[mt][i] - mnew) + fast_exp2(x[0] - mnew) +
-                                         fast_exp2(x[1] - mnew) + fast_exp2(x[2] - mnew) + fast_exp2(x[3] - mnew);
-                            m_r[mt][i] = mnew;
-                        }
+                    }
+                    if (mx != -INFINITY) {
+                        const float mnew = fmaxf(m_run, mx * c);
+                        float acc = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) acc += fast_exp2(fmaf(__uint_as_float(v[i]), c, -mnew));
+                        l_run = l_run * fast_exp2(m_run - mnew) + acc;
+                        m_run = mnew;
                     }
                 }
             } else {
-                float cs[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // [nt][e] column sums of this thread
+                // lane tl is key key0 + tl; columns are window rows half*64 + i
+                const int key = key0 + tl;
+                float acc = 0.f;
+                if (!bad) {
+                    const bool all_rows = key0 + C::TK - 1 <= p.q_pos0;
 #pragma unroll
-                for (int mt = 0; mt < C::MPW; ++mt) {
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            const int nt = q4 >> 1, e = q4 & 1;
-                            const int key = key0 + nt * 8 + e;
-                            const bool valid = key < hi && key <= lim[mt][i];
-                            const float x = sacc[mt][nt][2 * i + e] * p.scale_log2 - rM[mt][i];
-                            cs[nt][e] += valid ? fast_exp2(x) * rIL[mt][i] : 0.f;
+                    for (int i = 0; i < 64; i += 4) {
+                        const float4 b4 = *reinterpret_cast<const float4*>(cb + half * 64 + i);
+                        const float4 c4 = *reinterpret_cast<const float4*>(ci + half * 64 + i);
+                        float e0 = fast_exp2(fmaf(__uint_as_float(v[i + 0]), c, b4.x)) * c4.x;
+                        float e1 = fast_exp2(fmaf(__uint_as_float(v[i + 1]), c, b4.y)) * c4.y;
+                        float e2 = fast_exp2(fmaf(__uint_as_float(v[i + 2]), c, b4.z)) * c4.z;
+                        float e3 = fast_exp2(fmaf(__uint_as_float(v[i + 3]), c, b4.w)) * c4.w;
+                        if (!all_rows) {
+                            const int4 l4 = *reinterpret_cast<const int4*>(lim + half * 64 + i);
+                            e0 = key <= l4.x ? e0 : 0.f;
+                            e1 = key <= l4.y ? e1 : 0.f;
+                            e2 = key <= l4.z ? e2 : 0.f;
+                            e3 = key <= l4.w ? e3 : 0.f;
                         }
+                        acc += (e0 + e1) + (e2 + e3);
                     }
                 }
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        float v = cs[nt][e];
-                        v += __shfl_xor_sync(0xffffffffu, v, 4);
-                        v += __shfl_xor_sync(0xffffffffu, v, 8);
-                        v += __shfl_xor_sync(0xffffffffu, v, 16);
-                        cs[nt][e] = v;
-                    }
-                if (lane < 4) {
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
-                        *reinterpret_cast<float2*>(redb + warp * C::TK + krow0 + nt * 8 + 2 * lane) =
-                            make_float2(cs[nt][0], cs[nt][1]);
-                }
-            }
-        }
-        __syncwarp();
-        if (lane == 0 && !bad) mbar_arrive(bar_empty + 8 * s);
-        if constexpr (PASS2) {
-            // one barrier per stage; it also makes a timeout in any warp stop all of them
-            if (named_bar_or(1, C::NCT, bad)) break;
-            if (tid < C::TK) {
-                float v = 0.f;
-#pragma unroll
-                for (int w = 0; w < C::NCW; ++w) v += redb[w * C::TK + tid];
-                const int key = lo + t * C::TK + tid;
-                if (key < hi) {
+                float* rb = red + buf * C::TK;
+                if (half == 1) rb[tl] = acc;
+                // one barrier per tile; it also stops every epilogue warp if any timed out
+                if (named_bar_or(1, C::NET, bad)) break;
+                if (half == 0 && key < hi) {
+                    const float v2 = acc + rb[tl];
                     if (p.n_mg == 1)
-                        p.scores[static_cast<size_t>(bh) * p.n + key] = v * p.inv_w;
+                        p.scores[static_cast<size_t>(bh) * p.n + key] = v2 * p.inv_w;
                     else
-                        p.sc_part[(static_cast<size_t>(mg) * p.BH + bh) * p.n + key] = v;
+                        p.sc_part[(static_cast<size_t>(mg) * p.BH + bh) * p.n + key] = v2;
                 }
             }
         }
-    }
-    if (aborted && lane == 0) flag_status(p.status, SDKV_DEV_TIMEOUT);
-    if (named_bar_or(1, C::NCT, aborted || *reinterpret_cast<volatile int*>(&s_abort))) {
-        if (tid == 0) {
-            for (int s = 0; s < C::STAGES && s < ntiles; ++s) {
-                const int last_t = ((ntiles - 1 - s) / C::STAGES) * C::STAGES + s;
-                mbar_wait(bar_full + 8 * s, (last_t / C::STAGES) & 1);
+        if (aborted && lane == 0) {
+            flag_status(p.status, SDKV_DEV_TIMEOUT);
+            *abort_flag = 1;
+        }
+        const bool stop = named_bar_or(1, C::NET, aborted || *abort_flag);
+        if (!stop) {
+            if constexpr (!PASS2) {
+                // merge the two column halves of each row, store the split's partial
+                if (half == 1) {
+                    red[2 * tl] = m_run;
+                    red[2 * tl + 1] = l_run;
+                }
+                named_bar_sync(1, C::NET);
+                if (half == 0) {
+                    const float m2 = red[2 * tl], l2 = red[2 * tl + 1];
+                    const float M = fmaxf(m_run, m2);
+                    float L = 0.f;
+                    if (M != -INFINITY)
+                        L = (m_run == -INFINITY ? 0.f : l_run * fast_exp2(m_run - M)) +
+                            (m2 == -INFINITY ? 0.f : l2 * fast_exp2(m2 - M));
+                    const int r = row_base + tl;
+                    if (r < p.R)
+                        *reinterpret_cast<float2*>(p.st_part + ((static_cast<size_t>(bh) * p.nsplit + sp) * p.R + r) * 2) =
+                            make_float2(M, L);
+                }
+                __threadfence();
+                named_bar_sync(1, C::NET);
+                if (et == 0) {
+                    const int old = atomicAdd(p.tick1 + bh * p.n_mg + mg, 1);
+                    s_last = (old == p.nsplit - 1);
+                }
+                named_bar_sync(1, C::NET);
+                if (s_last) {
+                    __threadfence();
+                    const int r = row_base + et;   // one thread per row
+                    if (et < C::ROWS && r < p.R) {
+                        const float* base = p.st_part + (static_cast<size_t>(bh) * p.nsplit * p.R + r) * 2;
+                        const size_t stride = static_cast<size_t>(p.R) * 2;
+                        float mm = -INFINITY, ll = 0.f;
+#pragma unroll 4
+                        for (int s = 0; s < p.nsplit; ++s) {
+                            const float2 v2 = __ldcg(reinterpret_cast<const float2*>(base + s * stride));
+                            if (v2.x == -INFINITY) continue;
+                            if (v2.x > mm) {
+                                ll = ll * fast_exp2(mm - v2.x) + v2.y;
+                                mm = v2.x;
+                            } else {
+                                ll += v2.y * fast_exp2(v2.x - mm);
+                            }
+                        }
+                        *reinterpret_cast<float2*>(p.st_final + (static_cast<size_t>(bh) * p.R + r) * 2) =
+                            make_float2(mm, ll > 0.f ? 1.f / ll : 0.f);
+                    }
+                    if (et == 0) atomicExch(p.tick1 + bh * p.n_mg + mg, 0);
+                }
+            } else if (p.n_mg > 1) {
+                __threadfence();
+                named_bar_sync(1, C::NET);
+                if (et == 0) {
+                    const int old = atomicAdd(p.tick2 + bh * p.nsplit + sp, 1);
+                    s_last = (old == p.n_mg - 1);
+                }
+                named_bar_sync(1, C::NET);
+                if (s_last) {
+                    __threadfence();
+                    for (int key = lo + et; key < hi; key += C::NET) {
+                        float v2 = 0.f;
+                        for (int g2 = 0; g2 < p.n_mg; ++g2)
+                            v2 += __ldcg(p.sc_part + (static_cast<size_t>(g2) * p.BH + bh) * p.n + key);
+                        p.scores[static_cast<size_t>(bh) * p.n + key] = v2 * p.inv_w;
+                    }
+                    if (et == 0) atomicExch(p.tick2 + bh * p.nsplit + sp, 0);
+                }
             }
         }
-        return;
     }
 
-    if constexpr (!PASS2) {
-        // merge the quad's column subsets into one (m, l) per row, store the split's partial
-#pragma unroll
-        for (int mt = 0; mt < C::MPW; ++mt) {
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                float m = m_r[mt][i];
-                float M = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-                M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
-                float l = (m == -INFINITY) ? 0.f : l_r[mt][i] * fast_exp2(m - M);
-                l += __shfl_xor_sync(0xffffffffu, l, 1);
-                l += __shfl_xor_sync(0xffffffffu, l, 2);
-                const int r = row_base + warp * (C::MPW * 16) + mt * 16 + (lane >> 2) + 8 * i;
-                if ((lane & 3) == 0 && r < p.R)
-                    *reinterpret_cast<float2*>(p.st_part + ((static_cast<size_t>(bh) * p.nsplit + sp) * p.R + r) * 2) =
-                        make_float2(M, l);
-            }
+    // ------------------------------------------------------------------ teardown
+    if (*abort_flag && tid == 0) {
+        // let copies in flight land before the CTA's shared memory goes away (bounded)
+        for (int s = 0; s < C::STAGES && s < ntiles; ++s) {
+            const int last_t = ((ntiles - 1 - s) / C::STAGES) * C::STAGES + s;
+            mbar_wait(bar_kfull + 8 * s, (last_t / C::STAGES) & 1);
         }
-        __threadfence();
-        named_bar_sync(1, C::NCT);
-        if (tid == 0) {
-            const int old = atomicAdd(p.tick1 + bh * p.n_mg + mg, 1);
-            s_last = (old == p.nsplit - 1);
-        }
-        named_bar_sync(1, C::NCT);
-        if (!s_last) return;
-        __threadfence();
-        const int r = row_base + tid;  // one consumer thread per row
-        if (tid < C::ROWS && r < p.R) {
-            const float* base = p.st_part + (static_cast<size_t>(bh) * p.nsplit * p.R + r) * 2;
-            const size_t stride = static_cast<size_t>(p.R) * 2;
-            float M = -INFINITY;
-            for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, __ldcg(base + s * stride));
-            float L = 0.f;
-            for (int s = 0; s < p.nsplit; ++s) {
-                const float2 ml = __ldcg(reinterpret_cast<const float2*>(base + s * stride));
-                if (ml.x != -INFINITY) L += ml.y * fast_exp2(ml.x - M);
-            }
-            *reinterpret_cast<float2*>(p.st_final + (static_cast<size_t>(bh) * p.R + r) * 2) =
-                make_float2(M, L > 0.f ? 1.f / L : 0.f);
-        }
-        if (tid == 0) atomicExch(p.tick1 + bh * p.n_mg + mg, 0);
-    } else {
-        if (p.n_mg == 1) return;
-        __threadfence();
-        named_bar_sync(1, C::NCT);
-        if (tid == 0) {
-            const int old = atomicAdd(p.tick2 + bh * p.nsplit + sp, 1);
-            s_last = (old == p.n_mg - 1);
-        }
-        named_bar_sync(1, C::NCT);
-        if (!s_last) return;
-        __threadfence();
-        for (int key = lo + tid; key < hi; key += C::NCT) {
-            float v = 0.f;
-            for (int g2 = 0; g2 < p.n_mg; ++g2)
-                v += __ldcg(p.sc_part + (static_cast<size_t>(g2) * p.BH + bh) * p.n + key);
-            p.scores[static_cast<size_t>(bh) * p.n + key] = v * p.inv_w;
-        }
-        if (tid == 0) atomicExch(p.tick2 + bh * p.nsplit + sp, 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
     }
 }
 
@@ -353,9 +397,9 @@ ScorePlan score_plan(int B, int Hq, int Hkv, int n, int W, int num_sms) {
     ScorePlan pl{};
     const int BH = B * Hkv;
     const int R = (Hq / Hkv) * W;
-    constexpr int ROWS = 128, TK = 64;
+    constexpr int ROWS = 128, TK = 128;
     pl.n_mg = (R + ROWS - 1) / ROWS;
-    const int target = 2 * std::max(num_sms, 1);
+    const int target = std::max(num_sms, 1);   // one CTA per SM (tensor memory + 130 KB of stages)
     int nsplit = std::max(1, (target + BH * pl.n_mg - 1) / (BH * pl.n_mg));
     nsplit = std::min(nsplit, std::max(1, (n + TK - 1) / TK));
     int chunk = (n + nsplit - 1) / nsplit;
@@ -379,7 +423,8 @@ ScorePlan score_plan(int B, int Hq, int Hkv, int n, int W, int num_sms) {
 }
 
 template <int D, bool PASS2>
-cudaError_t launch_score_pass(const ScoreParams& p, const CUtensorMap& tmk, int grid, cudaStream_t st) {
+cudaError_t launch_score_pass(const ScoreParams& p, const CUtensorMap& tmk, const CUtensorMap& tmq, int grid,
+                              cudaStream_t st) {
     using C = ScoreCfg<D>;
     auto kern = score_kernel<D, PASS2>;
     int dev = 0;
@@ -401,7 +446,7 @@ cudaError_t launch_score_pass(const ScoreParams& p, const CUtensorMap& tmk, int 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, p, tmk);
+    return cudaLaunchKernelEx(&cfg, kern, p, tmk, tmq);
 }
 
 }  // namespace
@@ -411,7 +456,8 @@ size_t score_ws_bytes(int B, int Hq, int Hkv, int d, int n, int W, int num_sms) 
     return score_plan(B, Hq, Hkv, n, W, num_sms).bytes;
 }
 
-int launch_score(const ScoreLaunch& a, const CUtensorMap* tmk, int num_sms, const char** why) {
+int launch_score(const ScoreLaunch& a, const CUtensorMap* tmk, const CUtensorMap* tmq, int num_sms,
+                 const char** why) {
     const ScorePlan pl = score_plan(a.B, a.Hq, a.Hkv, a.n, a.W, num_sms);
     if (a.ws_bytes < pl.bytes) {
         *why = "workspace smaller than sdkv_workspace_size(SDKV_OP_SCORE, ...)";
@@ -419,7 +465,6 @@ int launch_score(const ScoreLaunch& a, const CUtensorMap* tmk, int num_sms, cons
     }
     uint8_t* ws = static_cast<uint8_t*>(a.ws);
     ScoreParams p{};
-    p.q = static_cast<const bf16*>(a.q_obs);
     p.B = a.B;
     p.Hq = a.Hq;
     p.Hkv = a.Hkv;
@@ -444,11 +489,11 @@ int launch_score(const ScoreLaunch& a, const CUtensorMap* tmk, int num_sms, cons
     const int grid = p.BH * pl.n_mg * pl.nsplit;
     cudaError_t e;
     if (a.d == 128) {
-        e = launch_score_pass<128, false>(p, *tmk, grid, a.stream);
-        if (e == cudaSuccess) e = launch_score_pass<128, true>(p, *tmk, grid, a.stream);
+        e = launch_score_pass<128, false>(p, *tmk, *tmq, grid, a.stream);
+        if (e == cudaSuccess) e = launch_score_pass<128, true>(p, *tmk, *tmq, grid, a.stream);
     } else {
-        e = launch_score_pass<64, false>(p, *tmk, grid, a.stream);
-        if (e == cudaSuccess) e = launch_score_pass<64, true>(p, *tmk, grid, a.stream);
+        e = launch_score_pass<64, false>(p, *tmk, *tmq, grid, a.stream);
+        if (e == cudaSuccess) e = launch_score_pass<64, true>(p, *tmk, *tmq, grid, a.stream);
     }
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);

@@ -105,6 +105,24 @@ int encode_kv_tmap(CUtensorMap* map, const void* base, int B, int Hkv, int rows,
     return SDKV_OK;
 }
 
+int encode_rows_tmap(CUtensorMap* map, const void* base, int64_t rows, int d, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return fail(SDKV_ERR_CUDA, "cuTensorMapEncodeTiled not available from the driver");
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+    cuuint64_t gstr[1] = {static_cast<cuuint64_t>(d) * 2};
+    cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, gstr, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        char msg[96];
+        std::snprintf(msg, sizeof(msg), "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+        return fail(SDKV_ERR_CUDA, msg);
+    }
+    return SDKV_OK;
+}
+
 }  // namespace sdkv
 
 using namespace sdkv;
@@ -232,11 +250,12 @@ int sdkv_score_obs_window(const void* q_obs, const void* k, const int64_t k_stri
     const DeviceInfo dev = current_device();
     if (dev.num_sms <= 0) return fail(SDKV_ERR_CUDA, "no CUDA device");
     if ((rc = check_ws(ws, ws_bytes, score_ws_bytes(B, Hq, Hkv, d, n, W, dev.num_sms)))) return rc;
-    CUtensorMap tmk;
-    if ((rc = encode_kv_tmap(&tmk, k, B, Hkv, n, d, k_strides, 64))) return rc;
+    CUtensorMap tmk, tmq;
+    if ((rc = encode_kv_tmap(&tmk, k, B, Hkv, n, d, k_strides, 128))) return rc;
+    if ((rc = encode_rows_tmap(&tmq, q_obs, static_cast<int64_t>(B) * Hq * W, d, 128))) return rc;
     ScoreLaunch a{q_obs, B, Hq, Hkv, d, n, W, q_pos0, scale, scores, ws, ws_bytes, static_cast<cudaStream_t>(stream)};
     const char* why = "";
-    rc = launch_score(a, &tmk, dev.num_sms, &why);
+    rc = launch_score(a, &tmk, &tmq, dev.num_sms, &why);
     if (rc) return fail(rc, why);
     g_last_error.clear();
     return SDKV_OK;

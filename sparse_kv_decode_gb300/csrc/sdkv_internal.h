@@ -60,7 +60,10 @@ struct ScoreLaunch {
     cudaStream_t stream;
 };
 size_t score_ws_bytes(int B, int Hq, int Hkv, int d, int n, int W, int num_sms);
-int launch_score(const ScoreLaunch& a, const CUtensorMap* tmk, int num_sms, const char** why);
+int launch_score(const ScoreLaunch& a, const CUtensorMap* tmk, const CUtensorMap* tmq, int num_sms,
+                 const char** why);
+// 2-D bf16 tensor map over rows x d (row pitch d), box (64, box_rows), 128-byte swizzle
+int encode_rows_tmap(CUtensorMap* map, const void* base, int64_t rows, int d, int box_rows);
 
 // ---- top-K selection (select_topk.cu) -------------------------------------------
 struct SelectLaunch {
