@@ -49,29 +49,30 @@ struct AttnParams {
 
 template <int D, int MT, int KW, int TK, int STAGES, bool SPARSE>
 struct AttnCfg {
-    static constexpr int NCW = MT * KW;          // consumer warps
+    static constexpr int NCW = MT * KW;          // consumer warps: row tiles x key groups
     static constexpr int NCT = NCW * 32;
     static constexpr int NPW = SPARSE ? 2 : 1;   // producer warps (gathering rows needs more issuers)
     static constexpr int NT = NCT + NPW * 32;
     static constexpr int KPW = TK / KW;          // keys per consumer warp per stage
     static_assert(KPW % 16 == 0, "keys per warp must be a multiple of 16");
+    static_assert(D % (4 * KW) == 0, "each key group reduces a slice of the head dims");
     static_assert(D == 64 || D == 128, "head dim");
     static_assert(!SPARSE || TK == 32 * NPW, "one list entry per producer lane per tile");
     static constexpr int ROWB = 2 * D;
     static constexpr int TILE_B = TK * ROWB;
     static constexpr int QPITCH = 2 * D + 16;
     static constexpr int ROWS = MT * 16;
+    static constexpr int MPITCH = D + 8;         // merge rows: conflict-free 64-bit stores
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = STAGES * TILE_B;
     static constexpr int OFF_Q = 2 * STAGES * TILE_B;
-    static constexpr int OFF_ML = OFF_Q + ROWS * QPITCH;
-    static constexpr int ML_FLOATS = KW * ROWS * 2;
-    static constexpr int OFF_BAR = OFF_ML + ML_FLOATS * 4;
+    static constexpr int OFF_ML = OFF_Q + ROWS * QPITCH;          // [KW][ROWS] (m, l)
+    static constexpr int OFF_BAR = OFF_ML + KW * ROWS * 2 * 4;
     static constexpr int SMEM = OFF_BAR + 2 * STAGES * 8;
     static constexpr int SMEM_ALLOC = SMEM + 1024;
-    static constexpr int MRG_B = (KW - 1) * ROWS * D * 4;
-    static_assert(MRG_B <= 2 * STAGES * TILE_B, "merge buffer must fit in the stage buffers");
     static_assert((TILE_B % 1024) == 0, "swizzled stages need 1024-byte alignment");
+    static_assert(KW * ROWS * MPITCH * 4 <= 2 * STAGES * TILE_B, "merge rows fit in the stage buffers");
+    static_assert(2 * STAGES * TILE_B >= ROWS * (8 * D + 12) + ROWS * 16 + 128, "combine area");
 };
 
 template <int NT>
@@ -291,6 +292,8 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
     }
 
     // ------------------------------------------------------------------ consumers
+    // Warp cw owns row tile mi = cw % MT and key group kw = cw / MT: keys
+    // [kw*KPW, kw*KPW + KPW) of every stage, all head dims.
     const int cw = warp;
     const int mi = cw % MT, kw = cw / MT;
 
@@ -375,13 +378,15 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
                 const float mnew = fmaxf(m_r[i], mx);
                 const float muse = (mnew == -INFINITY) ? 0.f : mnew;
-                const float alpha = fast_exp2(m_r[i] - muse);
-                m_r[i] = mnew;
-                l_r[i] *= alpha;
+                if (mnew != m_r[i]) {
+                    const float alpha = fast_exp2(m_r[i] - muse);
+                    l_r[i] *= alpha;
 #pragma unroll
-                for (int j = 0; j < D / 8; ++j) {
-                    o_acc[j][2 * i] *= alpha;
-                    o_acc[j][2 * i + 1] *= alpha;
+                    for (int j = 0; j < D / 8; ++j) {
+                        o_acc[j][2 * i] *= alpha;
+                        o_acc[j][2 * i + 1] *= alpha;
+                    }
+                    m_r[i] = mnew;
                 }
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
@@ -408,8 +413,6 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
         if (lane == 0) mbar_arrive(bar_empty + 8 * s);
     }
     if (aborted && lane == 0) flag_status(p.status, SDKV_DEV_TIMEOUT);
-
-    // -------------------------------------------------- merge the KW key-warps of a row block
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         l_r[i] += __shfl_xor_sync(0xffffffffu, l_r[i], 1);
@@ -426,6 +429,11 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
         }
         return;
     }
+
+    // -------------------------------------------------- merge the KW key groups of each row tile
+    // Rows below R only.  Each warp rescales its o to the row max over the groups
+    // and parks it in shared memory (padded rows: conflict-free 64-bit stores);
+    // then group kw sums dims [kw*D/KW, (kw+1)*D/KW) over the groups and writes them.
     float* ml = reinterpret_cast<float*>(smem + C::OFF_ML);
     if ((lane & 3) == 0) {
 #pragma unroll
@@ -435,74 +443,56 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
         }
     }
     named_bar_sync(1, C::NCT);
-    float Mrow[2];
+    float* mrg = reinterpret_cast<float*>(smem + C::OFF_K);  // stage buffers are free now
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
+        const int row = r0 + 8 * i;
+        if (row >= p.R) continue;
         float M = -INFINITY;
 #pragma unroll
-        for (int k2 = 0; k2 < KW; ++k2) M = fmaxf(M, ml[(k2 * C::ROWS + r0 + 8 * i) * 2]);
-        Mrow[i] = M;
+        for (int k2 = 0; k2 < KW; ++k2) M = fmaxf(M, ml[(k2 * C::ROWS + row) * 2]);
         const float f = (m_r[i] == -INFINITY) ? 0.f : fast_exp2(m_r[i] - M);
-        l_r[i] *= f;
+        float* dst = mrg + (kw * C::ROWS + row) * C::MPITCH + 2 * (lane & 3);
 #pragma unroll
-        for (int j = 0; j < D / 8; ++j) {
-            o_acc[j][2 * i] *= f;
-            o_acc[j][2 * i + 1] *= f;
-        }
-    }
-    float* mrg = reinterpret_cast<float*>(smem + C::OFF_K);  // stage buffers are free now
-    if (KW > 1 && kw > 0) {
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            float* dst = mrg + ((kw - 1) * C::ROWS + r0 + 8 * i) * D + 2 * (lane & 3);
-#pragma unroll
-            for (int j = 0; j < D / 8; ++j)
-                *reinterpret_cast<float2*>(dst + 8 * j) = make_float2(o_acc[j][2 * i], o_acc[j][2 * i + 1]);
-            if ((lane & 3) == 0) ml[(kw * C::ROWS + r0 + 8 * i) * 2 + 1] = l_r[i];
-        }
+        for (int j = 0; j < D / 8; ++j)
+            *reinterpret_cast<float2*>(dst + 8 * j) = make_float2(o_acc[j][2 * i] * f, o_acc[j][2 * i + 1] * f);
     }
     named_bar_sync(1, C::NCT);
-
-    if (kw == 0) {
+    {
+        constexpr int SL4 = D / KW / 4;              // float4 per row in this group's dim slice
+        const int nrow = min(16, p.R - mi * 16);     // valid rows of this row tile
+        for (int e = lane; e < nrow * SL4; e += 32) {
+            const int row = mi * 16 + e / SL4;
+            const int d0 = kw * (D / KW) + 4 * (e % SL4);
+            float M = -INFINITY;
 #pragma unroll
-        for (int k2 = 1; k2 < KW; ++k2) {
+            for (int k2 = 0; k2 < KW; ++k2) M = fmaxf(M, ml[(k2 * C::ROWS + row) * 2]);
+            float L = 0.f;
+            float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const float* src = mrg + ((k2 - 1) * C::ROWS + r0 + 8 * i) * D + 2 * (lane & 3);
-#pragma unroll
-                for (int j = 0; j < D / 8; ++j) {
-                    const float2 v2 = *reinterpret_cast<const float2*>(src + 8 * j);
-                    o_acc[j][2 * i] += v2.x;
-                    o_acc[j][2 * i + 1] += v2.y;
-                }
-                l_r[i] += ml[(k2 * C::ROWS + r0 + 8 * i) * 2 + 1];
+            for (int k2 = 0; k2 < KW; ++k2) {
+                const float mk = ml[(k2 * C::ROWS + row) * 2];
+                L += (mk == -INFINITY) ? 0.f : ml[(k2 * C::ROWS + row) * 2 + 1] * fast_exp2(mk - M);
+                const float4 v4 = *reinterpret_cast<const float4*>(mrg + (k2 * C::ROWS + row) * C::MPITCH + d0);
+                a4.x += v4.x;
+                a4.y += v4.y;
+                a4.z += v4.z;
+                a4.w += v4.w;
             }
-        }
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int row = r0 + 8 * i;
-            if (row >= p.R) continue;
             const int g = row / p.gamma, tt = row - (row / p.gamma) * p.gamma;
             const size_t orow = (static_cast<size_t>(b) * p.Hq + h * p.G + g) * p.gamma + tt;
             if (nch == 1) {
-                const float L = l_r[i];
-                const float inv = L > 0.f ? 1.f / L : 0.f;
-                uint32_t* dst = reinterpret_cast<uint32_t*>(p.o + orow * D + 2 * (lane & 3));
-#pragma unroll
-                for (int j = 0; j < D / 8; ++j)
-                    dst[4 * j] = pack_bf16(o_acc[j][2 * i] * inv, o_acc[j][2 * i + 1] * inv);
-                if ((lane & 3) == 0 && p.lse)
-                    p.lse[orow] = L > 0.f ? (Mrow[i] + fast_log2(L)) * kLn2 : -INFINITY;
+                const float il = L > 0.f ? 1.f / L : 0.f;
+                uint2 packed;
+                packed.x = pack_bf16(a4.x * il, a4.y * il);
+                packed.y = pack_bf16(a4.z * il, a4.w * il);
+                *reinterpret_cast<uint2*>(p.o + orow * D + d0) = packed;
+                if (d0 == 0 && p.lse) p.lse[orow] = L > 0.f ? (M + fast_log2(L)) * kLn2 : -INFINITY;
             } else {
-                float* po = p.part_o + (static_cast<size_t>(cidx) * p.R + row) * D + 2 * (lane & 3);
-#pragma unroll
-                for (int j = 0; j < D / 8; ++j)
-                    *reinterpret_cast<float2*>(po + 8 * j) = make_float2(o_acc[j][2 * i], o_acc[j][2 * i + 1]);
-                if ((lane & 3) == 0) {
-                    float* pm = p.part_ml + (static_cast<size_t>(cidx) * p.R + row) * 2;
-                    pm[0] = Mrow[i];
-                    pm[1] = l_r[i];
-                }
+                *reinterpret_cast<float4*>(p.part_o + (static_cast<size_t>(cidx) * p.R + row) * D + d0) = a4;
+                if (d0 == 0)
+                    *reinterpret_cast<float2*>(p.part_ml + (static_cast<size_t>(cidx) * p.R + row) * 2) =
+                        make_float2(M, L);
             }
         }
     }
@@ -519,78 +509,69 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
     if (!s_last) return;
     __threadfence();
 
-    // (1) per row: M = max_s m_s and L = sum_s 2^(m_s - M) l_s, one warp per row,
-    //     each lane merging its splits online, then a butterfly merge of the lanes
-    float* sM = ml;                        // [R] row max
-    float* sIL = ml + C::ML_FLOATS / 2;    // [R] 1 / row sum
-    for (int row = cw; row < p.R; row += C::NCW) {
-        float mm = -INFINITY, ll = 0.f;
-        for (int s = lane; s < nch; s += 32) {
-            const float2 v2 =
-                __ldcg(reinterpret_cast<const float2*>(p.part_ml + (static_cast<size_t>(c0 + s) * p.R + row) * 2));
-            if (v2.x == -INFINITY) continue;
-            if (v2.x > mm) {
-                ll = ll * fast_exp2(mm - v2.x) + v2.y;
-                mm = v2.x;
-            } else {
-                ll += v2.y * fast_exp2(v2.x - mm);
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float m2 = __shfl_xor_sync(0xffffffffu, mm, o);
-            const float l2 = __shfl_xor_sync(0xffffffffu, ll, o);
-            const float M = fmaxf(mm, m2);
-            if (M != -INFINITY) {
-                ll = (mm == -INFINITY ? 0.f : ll * fast_exp2(mm - M)) + (m2 == -INFINITY ? 0.f : l2 * fast_exp2(m2 - M));
-                mm = M;
-            }
-        }
-        if (lane == 0) {
-            sM[row] = mm;
-            sIL[row] = ll > 0.f ? 1.f / ll : 0.f;
-            if (p.lse) {
-                const int g = row / p.gamma, tt = row - (row / p.gamma) * p.gamma;
-                const size_t orow = (static_cast<size_t>(b) * p.Hq + h * p.G + g) * p.gamma + tt;
-                p.lse[orow] = ll > 0.f ? (mm + fast_log2(ll)) * kLn2 : -INFINITY;
-            }
-        }
+    // Partials are merged in batches of splits that fit in the (now idle) stage
+    // buffers.  Per batch, one round trip: the batch's o blocks and (m, l) pairs are
+    // staged with cp.async; then per row the running max / sum are updated online
+    // and o = o * 2^(M_old - M_new) + sum_s 2^(m_s - M_new) o_s is accumulated in
+    // shared memory.
+    constexpr int AREA = 2 * STAGES * C::TILE_B;
+    const int R = p.R;
+    float* acc = reinterpret_cast<float*>(smem + C::OFF_K);              // [R][D]
+    float* rs = acc + R * D;                                              // [R][4]: M, L, factor
+    const int per_split = R * (4 * D + 4 + 8);
+    const int batch = max(1, (AREA - R * D * 4 - R * 16 - 64) / per_split);
+    float* wts = rs + R * 4;                                              // [batch][R]
+    float* mls = wts + ((batch * R + 3) & ~3);                            // [batch][R][2]
+    uint8_t* stage = reinterpret_cast<uint8_t*>(mls + ((batch * R * 2 + 3) & ~3));   // [batch][R][D]
+    const uint32_t stage_s = smem_u32(stage), mls_s = smem_u32(mls);
+    for (int e = tid; e < R * D; e += C::NCT) acc[e] = 0.f;
+    for (int e = tid; e < R; e += C::NCT) {
+        rs[4 * e] = -INFINITY;
+        rs[4 * e + 1] = 0.f;
     }
-    named_bar_sync(1, C::NCT);
-
-    // (2) o = sum_s w_s o_s with w_s = 2^(m_s - M) / L: the partial rows of a batch
-    //     of splits are staged into shared memory with cp.async (all in flight at
-    //     once), then each thread adds its (row, 4-dim) slots into an fp32
-    //     accumulator in shared memory.
-    constexpr int AREA = 2 * STAGES * C::TILE_B;   // the stage buffers are free now
-    float* acc = reinterpret_cast<float*>(smem + C::OFF_K);            // [R][D]
-    const int acc_b = p.R * D * 4;
-    const int per_split = p.R * D * 4 + p.R * 4;
-    const int batch = max(1, (AREA - acc_b - 16) / per_split);
-    float* wts = acc + p.R * D;                                         // [batch][R]
-    const int wts_b = ((batch * p.R * 4) + 15) & ~15;
-    uint8_t* stage = reinterpret_cast<uint8_t*>(wts) + wts_b;          // [batch][R][D]
-    const uint32_t stage_s = smem_u32(stage);
-    for (int e = tid; e < p.R * D; e += C::NCT) acc[e] = 0.f;
     for (int s0 = 0; s0 < nch; s0 += batch) {
         const int nb = min(batch, nch - s0);
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(p.part_o + static_cast<size_t>(c0 + s0) * p.R * D);
-        const int n16 = nb * p.R * (D / 4);
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(p.part_o + static_cast<size_t>(c0 + s0) * R * D);
+        const int n16 = nb * R * (D / 4);
         for (int e = tid; e < n16; e += C::NCT) cp_async_16(stage_s + e * 16, src + static_cast<size_t>(e) * 16);
-        for (int e = tid; e < nb * p.R; e += C::NCT) {
-            const int sl = e / p.R, row = e - (e / p.R) * p.R;
-            const float m = __ldcg(p.part_ml + (static_cast<size_t>(c0 + s0 + sl) * p.R + row) * 2);
-            wts[e] = (m == -INFINITY) ? 0.f : fast_exp2(m - sM[row]) * sIL[row];
-        }
+        const float* msrc = p.part_ml + static_cast<size_t>(c0 + s0) * R * 2;
+        for (int e = tid; e < nb * R; e += C::NCT) cp_async_8(mls_s + e * 8, msrc + 2 * e);
         cp_async_wait_all();
         named_bar_sync(1, C::NCT);
+        for (int row = cw; row < R; row += C::NCW) {
+            float mb = -INFINITY;
+            for (int sl = lane; sl < nb; sl += 32) mb = fmaxf(mb, mls[2 * (sl * R + row)]);
+            mb = warp_max(mb);
+            const float Mold = rs[4 * row];
+            const float Mnew = fmaxf(Mold, mb);
+            float ladd = 0.f;
+            for (int sl = lane; sl < nb; sl += 32) {
+                const float m = mls[2 * (sl * R + row)];
+                const float w = (m == -INFINITY) ? 0.f : fast_exp2(m - Mnew);
+                wts[sl * R + row] = w;
+                ladd += w * mls[2 * (sl * R + row) + 1];
+            }
+            ladd = warp_sum(ladd);
+            if (lane == 0) {
+                const float f = (Mold == -INFINITY) ? 0.f : fast_exp2(Mold - Mnew);
+                rs[4 * row] = Mnew;
+                rs[4 * row + 1] = rs[4 * row + 1] * f + ladd;
+                rs[4 * row + 2] = f;
+            }
+        }
+        named_bar_sync(1, C::NCT);
         const float4* st4 = reinterpret_cast<const float4*>(stage);
-        for (int e = tid; e < p.R * (D / 4); e += C::NCT) {
+        for (int e = tid; e < R * (D / 4); e += C::NCT) {
             const int row = e / (D / 4);
+            const float f = rs[4 * row + 2];
             float4 a4 = reinterpret_cast<float4*>(acc)[e];
+            a4.x *= f;
+            a4.y *= f;
+            a4.z *= f;
+            a4.w *= f;
             for (int sl = 0; sl < nb; ++sl) {
-                const float w = wts[sl * p.R + row];
-                const float4 v4 = st4[sl * p.R * (D / 4) + e];
+                const float w = wts[sl * R + row];
+                const float4 v4 = st4[sl * R * (D / 4) + e];
                 a4.x += w * v4.x;
                 a4.y += w * v4.y;
                 a4.z += w * v4.z;
@@ -600,15 +581,18 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
         }
         named_bar_sync(1, C::NCT);
     }
-    for (int e = tid; e < p.R * (D / 4); e += C::NCT) {
+    for (int e = tid; e < R * (D / 4); e += C::NCT) {
         const int row = e / (D / 4), d4 = e - (e / (D / 4)) * (D / 4);
+        const float L = rs[4 * row + 1];
+        const float il = L > 0.f ? 1.f / L : 0.f;
         const float4 a4 = reinterpret_cast<const float4*>(acc)[e];
         const int g = row / p.gamma, tt = row - (row / p.gamma) * p.gamma;
         const size_t orow = (static_cast<size_t>(b) * p.Hq + h * p.G + g) * p.gamma + tt;
         uint2 packed;
-        packed.x = pack_bf16(a4.x, a4.y);
-        packed.y = pack_bf16(a4.z, a4.w);
+        packed.x = pack_bf16(a4.x * il, a4.y * il);
+        packed.y = pack_bf16(a4.z * il, a4.w * il);
         *reinterpret_cast<uint2*>(p.o + orow * D + 4 * d4) = packed;
+        if (d4 == 0 && p.lse) p.lse[orow] = L > 0.f ? (rs[4 * row] + fast_log2(L)) * kLn2 : -INFINITY;
     }
     if (tid == 0) atomicExch(p.tickets + bh, 0);
 }
