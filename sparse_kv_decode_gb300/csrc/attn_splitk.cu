@@ -36,6 +36,7 @@ struct AttnParams {
     float scale_log2;
     // dense
     int n_prefix, n_total, chunk, nsplit;
+    int cs, ncl;   // cluster size along the splits of a head, clusters per head (cs = 1: no cluster)
     // sparse
     const int* offsets;
     const int* indices;
@@ -67,7 +68,8 @@ struct AttnCfg {
     static constexpr int OFF_V = STAGES * TILE_B;
     static constexpr int OFF_Q = 2 * STAGES * TILE_B;
     static constexpr int OFF_ML = OFF_Q + ROWS * QPITCH;          // [KW][ROWS] (m, l)
-    static constexpr int OFF_BAR = OFF_ML + KW * ROWS * 2 * 4;
+    static constexpr int OFF_XML = OFF_ML + KW * ROWS * 2 * 4;    // [ROWS] (m, l) shown to the cluster
+    static constexpr int OFF_BAR = OFF_XML + ROWS * 2 * 4;
     static constexpr int SMEM = OFF_BAR + 2 * STAGES * 8;
     static constexpr int SMEM_ALLOC = SMEM + 1024;
     static_assert((TILE_B % 1024) == 0, "swizzled stages need 1024-byte alignment");
@@ -136,7 +138,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
             const int bh = blockIdx.x / p.nsplit, sp = blockIdx.x % p.nsplit;
             s_work[0] = bh;
             s_work[1] = sp * p.chunk;
-            s_work[2] = min(sp * p.chunk + p.chunk, p.n_total);
+            s_work[2] = max(sp * p.chunk, min(sp * p.chunk + p.chunk, p.n_total));  // trailing splits may be empty
             s_work[3] = blockIdx.x;
             s_work[4] = p.nsplit;
             s_work[5] = bh * p.nsplit;
@@ -288,6 +290,10 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
                 }
             }
         }
+        if (!SPARSE && p.cs > 1) {   // the two cluster barriers of the consumers' epilogue
+            cluster_sync_all();
+            cluster_sync_all();
+        }
         return;
     }
 
@@ -427,6 +433,10 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
                 mbar_wait(bar_full + 8 * s, (last_t / STAGES) & 1);
             }
         }
+        if (!SPARSE && p.cs > 1) {
+            cluster_sync_all();
+            cluster_sync_all();
+        }
         return;
     }
 
@@ -481,7 +491,11 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
             }
             const int g = row / p.gamma, tt = row - (row / p.gamma) * p.gamma;
             const size_t orow = (static_cast<size_t>(b) * p.Hq + h * p.G + g) * p.gamma + tt;
-            if (nch == 1) {
+            if (!SPARSE && p.cs > 1) {
+                // shown to the cluster: in place of group 0's parked row (read above by this thread only)
+                *reinterpret_cast<float4*>(mrg + row * C::MPITCH + d0) = a4;
+                if (d0 == 0) *reinterpret_cast<float2*>(smem + C::OFF_XML + row * 8) = make_float2(M, L);
+            } else if (nch == 1) {
                 const float il = L > 0.f ? 1.f / L : 0.f;
                 uint2 packed;
                 packed.x = pack_bf16(a4.x * il, a4.y * il);
@@ -494,6 +508,110 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
                     *reinterpret_cast<float2*>(p.part_ml + (static_cast<size_t>(cidx) * p.R + row) * 2) =
                         make_float2(M, L);
             }
+        }
+    }
+    if constexpr (!SPARSE) {
+        if (p.cs > 1) {
+            // ---------------------------------------------- merge the cluster's splits through DSMEM
+            // CTA `rank` of the cluster reduces head dims [rank*D/cs, (rank+1)*D/cs) of
+            // every row over the cs splits of the cluster, reading the peers' rows
+            // from their shared memory; one partial per cluster (or the output, when
+            // one cluster covers the head) goes to global memory.
+            cluster_sync_all();
+            const int CS = p.cs;
+            const uint32_t rank = cluster_ctarank();
+            const int sl4 = D / CS / 4;                      // float4 per row in this slice
+            const int sp = blockIdx.x - (blockIdx.x / p.nsplit) * p.nsplit;
+            const int gcl = bh * p.ncl + sp / CS;            // global cluster index
+            const uint32_t xml_s = sbase + C::OFF_XML, mrg_s = sbase + C::OFF_K;
+            for (int e = tid; e < p.R * sl4; e += C::NCT) {
+                const int row = e / sl4;
+                const int d0 = static_cast<int>(rank) * (D / CS) + 4 * (e - row * sl4);
+                float mc[8], lc[8];
+                float M = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    mc[c] = -INFINITY;
+                    lc[c] = 0.f;
+                    if (c < CS) {
+                        const float2 v = ld_dsmem_f2(dsmem_addr(xml_s + row * 8, c));
+                        mc[c] = v.x;
+                        lc[c] = v.y;
+                        M = fmaxf(M, v.x);
+                    }
+                }
+                float L = 0.f;
+                float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    if (c >= CS || mc[c] == -INFINITY) continue;
+                    const float w = fast_exp2(mc[c] - M);
+                    L += w * lc[c];
+                    const float4 v4 = ld_dsmem_f4(dsmem_addr(mrg_s + (row * C::MPITCH + d0) * 4, c));
+                    a4.x += w * v4.x;
+                    a4.y += w * v4.y;
+                    a4.z += w * v4.z;
+                    a4.w += w * v4.w;
+                }
+                const int g = row / p.gamma, tt = row - (row / p.gamma) * p.gamma;
+                const size_t orow = (static_cast<size_t>(b) * p.Hq + h * p.G + g) * p.gamma + tt;
+                if (p.ncl == 1) {
+                    const float il = L > 0.f ? 1.f / L : 0.f;
+                    uint2 packed;
+                    packed.x = pack_bf16(a4.x * il, a4.y * il);
+                    packed.y = pack_bf16(a4.z * il, a4.w * il);
+                    *reinterpret_cast<uint2*>(p.o + orow * D + d0) = packed;
+                    if (d0 == 0 && p.lse) p.lse[orow] = L > 0.f ? (M + fast_log2(L)) * kLn2 : -INFINITY;
+                } else {
+                    *reinterpret_cast<float4*>(p.part_o + (static_cast<size_t>(gcl) * p.R + row) * D + d0) = a4;
+                    if (e - row * sl4 == 0)   // this rank's copy of the cluster's (M, L)
+                        *reinterpret_cast<float2*>(
+                            p.part_ml + ((static_cast<size_t>(gcl) * CS + rank) * p.R + row) * 2) = make_float2(M, L);
+                }
+            }
+            __threadfence();
+            cluster_sync_all();   // peers may leave only after everyone has read their rows
+            if (p.ncl == 1) return;
+            named_bar_sync(1, C::NCT);
+            if (tid == 0) {
+                const int old = atomicAdd(p.tickets + bh * 8 + rank, 1);
+                s_last = (old == p.ncl - 1);
+            }
+            named_bar_sync(1, C::NCT);
+            if (!s_last) return;
+            __threadfence();
+            // last cluster of the head for this slice: merge the ncl cluster partials
+            for (int e = tid; e < p.R * sl4; e += C::NCT) {
+                const int row = e / sl4;
+                const int d0 = static_cast<int>(rank) * (D / CS) + 4 * (e - row * sl4);
+                float mm = -INFINITY, ll = 0.f;
+                float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int cl = 0; cl < p.ncl; ++cl) {
+                    const size_t gi = static_cast<size_t>(bh) * p.ncl + cl;
+                    const float2 v2 = __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((gi * CS + rank) * p.R + row) * 2));
+                    const float4 o4 = __ldcg(reinterpret_cast<const float4*>(p.part_o + (gi * p.R + row) * D + d0));
+                    if (v2.x == -INFINITY) continue;
+                    const float mnew = fmaxf(mm, v2.x);
+                    const float fa = (mm == -INFINITY) ? 0.f : fast_exp2(mm - mnew);
+                    const float fb = fast_exp2(v2.x - mnew);
+                    ll = ll * fa + v2.y * fb;
+                    a4.x = a4.x * fa + o4.x * fb;
+                    a4.y = a4.y * fa + o4.y * fb;
+                    a4.z = a4.z * fa + o4.z * fb;
+                    a4.w = a4.w * fa + o4.w * fb;
+                    mm = mnew;
+                }
+                const int g = row / p.gamma, tt = row - (row / p.gamma) * p.gamma;
+                const size_t orow = (static_cast<size_t>(b) * p.Hq + h * p.G + g) * p.gamma + tt;
+                const float il = ll > 0.f ? 1.f / ll : 0.f;
+                uint2 packed;
+                packed.x = pack_bf16(a4.x * il, a4.y * il);
+                packed.y = pack_bf16(a4.z * il, a4.w * il);
+                *reinterpret_cast<uint2*>(p.o + orow * D + d0) = packed;
+                if (d0 == 0 && p.lse) p.lse[orow] = ll > 0.f ? (mm + fast_log2(ll)) * kLn2 : -INFINITY;
+            }
+            if (tid == 0) atomicExch(p.tickets + bh * 8 + rank, 0);
+            return;
         }
     }
     if (nch == 1) return;
@@ -606,6 +724,10 @@ constexpr int kDenseTK = 64;
 constexpr int kDenseStages = 3;
 constexpr int kSparseTK = 64;
 constexpr int kSparseStages = 3;
+constexpr int kMaxCluster = 8;     // portable cluster size
+
+// per-head counters: one per head-dim slice of a cluster merge (at most kMaxCluster)
+size_t attn_ticket_bytes(int BH) { return sizeof(int) * static_cast<size_t>(BH) * kMaxCluster; }
 
 struct WsLayout {
     int* status;
@@ -617,7 +739,7 @@ struct WsLayout {
 
 WsLayout attn_ws_layout(void* ws, int BH, int R, int d, int max_chunks) {
     const size_t off_tickets = kWsHeader;
-    const size_t off_po = align256(off_tickets + sizeof(int) * static_cast<size_t>(BH));
+    const size_t off_po = align256(off_tickets + attn_ticket_bytes(BH));
     const size_t off_pml = align256(off_po + sizeof(float) * static_cast<size_t>(max_chunks) * R * d);
     const size_t end = align256(off_pml + sizeof(float) * static_cast<size_t>(max_chunks) * R * 2);
     WsLayout L{};
@@ -633,25 +755,41 @@ WsLayout attn_ws_layout(void* ws, int BH, int R, int d, int max_chunks) {
 }
 
 struct DensePlan {
-    int nsplit, chunk;
+    int nsplit, chunk, cs, ncl;
 };
 
+// Splits per head fill two CTAs per SM.  With enough splits per head they are
+// grouped in clusters of cs CTAs (nsplit a multiple of cs) that merge their
+// partials through distributed shared memory; trailing splits past the cache
+// may be empty.
 DensePlan dense_plan(int BH, int n_total, int num_sms) {
-    const int target = 2 * std::max(num_sms, 1);
-    int nsplit = std::max(1, (target + BH - 1) / BH);
-    const int max_split = (n_total + kDenseTK - 1) / kDenseTK;
-    nsplit = std::min(nsplit, std::max(1, max_split));
+    const int slots = 2 * std::max(num_sms, 1);
+    const int max_split = std::max(1, (n_total + kDenseTK - 1) / kDenseTK);
+    const int per_head = std::min(std::max(1, slots / BH), max_split);
+    DensePlan pl{};
+    pl.cs = per_head >= 16 ? 8 : per_head >= 8 ? 4 : per_head >= 4 ? 2 : 1;
+    if (pl.cs > 1) {
+        pl.nsplit = (per_head / pl.cs) * pl.cs;
+        pl.chunk = (n_total + pl.nsplit - 1) / pl.nsplit;
+        pl.chunk = ((pl.chunk + kDenseTK - 1) / kDenseTK) * kDenseTK;
+        pl.ncl = pl.nsplit / pl.cs;
+        return pl;
+    }
+    int nsplit = std::max(1, (slots + BH - 1) / BH);
+    nsplit = std::min(nsplit, max_split);
     int chunk = (n_total + nsplit - 1) / nsplit;
     chunk = ((chunk + kDenseTK - 1) / kDenseTK) * kDenseTK;
-    nsplit = (n_total + chunk - 1) / chunk;
-    return {nsplit, chunk};
+    pl.nsplit = (n_total + chunk - 1) / chunk;
+    pl.chunk = chunk;
+    pl.ncl = pl.nsplit;
+    return pl;
 }
 
 int sparse_grid_target(int num_sms) { return 2 * std::max(num_sms, 1); }
 
 template <int D, int MT, int KW, int TK, int STAGES, bool SPARSE>
 cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv, int grid,
-                        cudaStream_t st) {
+                        cudaStream_t st, int cluster = 1) {
     using C = AttnCfg<D, MT, KW, TK, STAGES, SPARSE>;
     auto kern = attn_splitk_kernel<D, MT, KW, TK, STAGES, SPARSE>;
     int dev = 0;
@@ -668,11 +806,18 @@ cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tmk, const CUten
     cfg.blockDim = dim3(C::NT);
     cfg.dynamicSmemBytes = C::SMEM_ALLOC;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (cluster > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = cluster;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
     return cudaLaunchKernelEx(&cfg, kern, p, tmk, tmv);
 }
 
@@ -720,6 +865,8 @@ int launch_dense_verify(const AttnLaunch& a, const CUtensorMap* tmk, const CUten
     const DensePlan pl = dense_plan(BH, p.n_total, num_sms);
     p.nsplit = pl.nsplit;
     p.chunk = pl.chunk;
+    p.cs = pl.cs;
+    p.ncl = pl.ncl;
     WsLayout L = attn_ws_layout(a.ws, BH, p.R, a.d, BH * pl.nsplit);
     if (a.ws_bytes < L.bytes) {
         *why = "workspace smaller than sdkv_workspace_size(SDKV_OP_DENSE_VERIFY, ...)";
@@ -734,18 +881,18 @@ int launch_dense_verify(const AttnLaunch& a, const CUtensorMap* tmk, const CUten
     cudaError_t e = cudaErrorInvalidValue;
     if (a.d == 128) {
         switch (MT) {
-            case 1: e = launch_attn<128, 1, 4, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream); break;
-            case 2: e = launch_attn<128, 2, 2, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream); break;
-            case 3: e = launch_attn<128, 3, 2, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream); break;
-            case 4: e = launch_attn<128, 4, 2, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream); break;
+            case 1: e = launch_attn<128, 1, 4, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream, pl.cs); break;
+            case 2: e = launch_attn<128, 2, 2, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream, pl.cs); break;
+            case 3: e = launch_attn<128, 3, 2, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream, pl.cs); break;
+            case 4: e = launch_attn<128, 4, 2, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream, pl.cs); break;
             default: *why = "(Hq/Hkv) * gamma must be <= 64"; return SDKV_ERR_UNSUPPORTED;
         }
     } else {
         switch (MT) {
-            case 1: e = launch_attn<64, 1, 4, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream); break;
-            case 2: e = launch_attn<64, 2, 2, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream); break;
-            case 3: e = launch_attn<64, 3, 2, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream); break;
-            case 4: e = launch_attn<64, 4, 2, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream); break;
+            case 1: e = launch_attn<64, 1, 4, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream, pl.cs); break;
+            case 2: e = launch_attn<64, 2, 2, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream, pl.cs); break;
+            case 3: e = launch_attn<64, 3, 2, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream, pl.cs); break;
+            case 4: e = launch_attn<64, 4, 2, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream, pl.cs); break;
             default: *why = "(Hq/Hkv) * gamma must be <= 64"; return SDKV_ERR_UNSUPPORTED;
         }
     }
@@ -765,6 +912,8 @@ int launch_sparse_decode(const AttnLaunch& a, int num_sms, const char** why) {
     p.BH = BH;
     p.grid_target = sparse_grid_target(num_sms);
     p.min_chunk = kSparseTK;
+    p.cs = 1;
+    p.ncl = 1;
     const int max_chunks = p.grid_target + BH;
     WsLayout L = attn_ws_layout(a.ws, BH, p.R, a.d, max_chunks);
     if (a.ws_bytes < L.bytes) {
@@ -845,8 +994,7 @@ int dense_verify_noalloc(const AttnLaunch& a_in, const CUtensorMap* tmk, const C
     }
     // The array keeps the previous call's contents: the status word and the
     // per-head counters must start at zero.
-    e = cudaMemsetAsync(ptr, 0, kWsHeader + align256(sizeof(int) * static_cast<size_t>(a_in.B) * a_in.Hkv),
-                        a_in.stream);
+    e = cudaMemsetAsync(ptr, 0, kWsHeader + align256(attn_ticket_bytes(a_in.B * a_in.Hkv)), a_in.stream);
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);
         return SDKV_ERR_CUDA;
