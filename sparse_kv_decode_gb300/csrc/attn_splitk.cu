@@ -144,10 +144,12 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
             s_work[5] = bh * p.nsplit;
         }
     } else {
-        // Chunk plan, identical in every CTA: chunk length Cl = max(min_chunk,
-        // ceil(total / grid_target) rounded up to 16); head i owns
-        // max(1, ceil(k_i / Cl)) consecutive chunk ids.
-        // the first tile of heads is loaded together with the total (one round trip)
+        // Chunk plan, identical in every CTA.  Chunk length cl = max(min_chunk,
+        // ceil(total / (grid_target - cs * BH)) rounded up to 16).  Without
+        // clusters head i owns max(1, ceil(k_i / cl)) consecutive chunk ids of
+        // length cl; with clusters of cs CTAs it owns cs * ceil(k_i / (cs * cl))
+        // chunks (a whole number of clusters) of balanced length; trailing ones
+        // may be empty.  Either way the chunk count stays within the grid.
         int start = 0, kh = 0;
         if (tid < p.BH) {
             start = p.offsets[tid];
@@ -159,13 +161,15 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
         }
         __syncthreads();
         const int total = max(s_tot, 0);
-        int cl = (total + p.grid_target - 1) / p.grid_target;
+        const int cs = p.cs;
+        const int slots = max(1, p.grid_target - (cs > 1 ? cs * p.BH : 0));
+        int cl = (total + slots - 1) / slots;
         cl = max(p.min_chunk, (cl + 15) & ~15);
         const int c = blockIdx.x;
         int running = 0;
         for (int base = 0; base < p.BH; base += C::NT) {
             const int i = base + tid;
-            int nch = 0;
+            int nch = 0, chl = cl;
             if (base > 0 && i < p.BH) {
                 start = p.offsets[i];
                 kh = p.offsets[i + 1] - start;
@@ -175,16 +179,22 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
                     flag_status(p.status, SDKV_DEV_BAD_LIST);
                     kh = 0;
                 }
-                nch = max(1, (kh + cl - 1) / cl);
+                if (cs > 1) {
+                    nch = cs * max(1, (kh + cs * cl - 1) / (cs * cl));
+                    chl = (((kh + nch - 1) / nch) + 15) & ~15;
+                } else {
+                    nch = max(1, (kh + cl - 1) / cl);
+                }
             }
             int tile_total;
             const int excl = block_excl_scan<C::NT>(nch, s_scan, tile_total);
             const int first = running + excl;
             if (i < p.BH && c >= first && c < first + nch) {
                 const int j = c - first;
+                const int l0 = min(start + j * chl, start + kh);
                 s_work[0] = i;
-                s_work[1] = start + j * cl;
-                s_work[2] = min(start + (j + 1) * cl, start + kh);
+                s_work[1] = l0;
+                s_work[2] = max(l0, min(start + (j + 1) * chl, start + kh));
                 s_work[3] = c;
                 s_work[4] = nch;
                 s_work[5] = first;
@@ -290,7 +300,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
                 }
             }
         }
-        if (!SPARSE && p.cs > 1) {   // the two cluster barriers of the consumers' epilogue
+        if (p.cs > 1) {   // the two cluster barriers of the consumers' epilogue
             cluster_sync_all();
             cluster_sync_all();
         }
@@ -433,7 +443,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
                 mbar_wait(bar_full + 8 * s, (last_t / STAGES) & 1);
             }
         }
-        if (!SPARSE && p.cs > 1) {
+        if (p.cs > 1) {
             cluster_sync_all();
             cluster_sync_all();
         }
@@ -491,7 +501,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
             }
             const int g = row / p.gamma, tt = row - (row / p.gamma) * p.gamma;
             const size_t orow = (static_cast<size_t>(b) * p.Hq + h * p.G + g) * p.gamma + tt;
-            if (!SPARSE && p.cs > 1) {
+            if (p.cs > 1) {
                 // shown to the cluster: in place of group 0's parked row (read above by this thread only)
                 *reinterpret_cast<float4*>(mrg + row * C::MPITCH + d0) = a4;
                 if (d0 == 0) *reinterpret_cast<float2*>(smem + C::OFF_XML + row * 8) = make_float2(M, L);
@@ -510,7 +520,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
             }
         }
     }
-    if constexpr (!SPARSE) {
+    {
         if (p.cs > 1) {
             // ---------------------------------------------- merge the cluster's splits through DSMEM
             // CTA `rank` of the cluster reduces head dims [rank*D/cs, (rank+1)*D/cs) of
@@ -521,8 +531,8 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
             const int CS = p.cs;
             const uint32_t rank = cluster_ctarank();
             const int sl4 = D / CS / 4;                      // float4 per row in this slice
-            const int sp = blockIdx.x - (blockIdx.x / p.nsplit) * p.nsplit;
-            const int gcl = bh * p.ncl + sp / CS;            // global cluster index
+            const int gcl = cidx / CS;                       // global cluster index (partial slot)
+            const int gcl0 = c0 / CS, ncl_h = nch / CS;      // the head's clusters
             const uint32_t xml_s = sbase + C::OFF_XML, mrg_s = sbase + C::OFF_K;
             for (int e = tid; e < p.R * sl4; e += C::NCT) {
                 const int row = e / sl4;
@@ -555,7 +565,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
                 }
                 const int g = row / p.gamma, tt = row - (row / p.gamma) * p.gamma;
                 const size_t orow = (static_cast<size_t>(b) * p.Hq + h * p.G + g) * p.gamma + tt;
-                if (p.ncl == 1) {
+                if (ncl_h == 1) {
                     const float il = L > 0.f ? 1.f / L : 0.f;
                     uint2 packed;
                     packed.x = pack_bf16(a4.x * il, a4.y * il);
@@ -571,23 +581,23 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
             }
             __threadfence();
             cluster_sync_all();   // peers may leave only after everyone has read their rows
-            if (p.ncl == 1) return;
+            if (ncl_h == 1) return;
             named_bar_sync(1, C::NCT);
             if (tid == 0) {
                 const int old = atomicAdd(p.tickets + bh * 8 + rank, 1);
-                s_last = (old == p.ncl - 1);
+                s_last = (old == ncl_h - 1);
             }
             named_bar_sync(1, C::NCT);
             if (!s_last) return;
             __threadfence();
-            // last cluster of the head for this slice: merge the ncl cluster partials
+            // last cluster of the head for this slice: merge the head's cluster partials
             for (int e = tid; e < p.R * sl4; e += C::NCT) {
                 const int row = e / sl4;
                 const int d0 = static_cast<int>(rank) * (D / CS) + 4 * (e - row * sl4);
                 float mm = -INFINITY, ll = 0.f;
                 float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int cl = 0; cl < p.ncl; ++cl) {
-                    const size_t gi = static_cast<size_t>(bh) * p.ncl + cl;
+                for (int cl = 0; cl < ncl_h; ++cl) {
+                    const size_t gi = static_cast<size_t>(gcl0) + cl;
                     const float2 v2 = __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((gi * CS + rank) * p.R + row) * 2));
                     const float4 o4 = __ldcg(reinterpret_cast<const float4*>(p.part_o + (gi * p.R + row) * D + d0));
                     if (v2.x == -INFINITY) continue;
@@ -785,7 +795,16 @@ DensePlan dense_plan(int BH, int n_total, int num_sms) {
     return pl;
 }
 
-int sparse_grid_target(int num_sms) { return 2 * std::max(num_sms, 1); }
+int sparse_grid_target(int num_sms) { return ((2 * std::max(num_sms, 1)) / kMaxCluster) * kMaxCluster; }
+
+// Clusters for the gathered decode only when every head can own whole clusters
+// and still leave the grid half free for long lists.
+int sparse_cluster(int BH, int grid_target) {
+    for (int cs = kMaxCluster; cs > 1; cs /= 2)
+        if (2 * cs * BH <= grid_target) return cs;
+    return 1;
+}
+int sparse_max_chunks(int BH, int grid_target, int cs) { return cs > 1 ? grid_target : grid_target + BH; }
 
 template <int D, int MT, int KW, int TK, int STAGES, bool SPARSE>
 cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv, int grid,
@@ -912,9 +931,9 @@ int launch_sparse_decode(const AttnLaunch& a, int num_sms, const char** why) {
     p.BH = BH;
     p.grid_target = sparse_grid_target(num_sms);
     p.min_chunk = kSparseTK;
-    p.cs = 1;
+    p.cs = sparse_cluster(BH, p.grid_target);
     p.ncl = 1;
-    const int max_chunks = p.grid_target + BH;
+    const int max_chunks = sparse_max_chunks(BH, p.grid_target, p.cs);
     WsLayout L = attn_ws_layout(a.ws, BH, p.R, a.d, max_chunks);
     if (a.ws_bytes < L.bytes) {
         *why = "workspace smaller than sdkv_workspace_size(SDKV_OP_SPARSE_DECODE, ...)";
@@ -930,14 +949,14 @@ int launch_sparse_decode(const AttnLaunch& a, int num_sms, const char** why) {
     cudaError_t e = cudaErrorInvalidValue;
     if (a.d == 128) {
         switch (MT) {
-            case 1: e = launch_attn<128, 1, 4, kSparseTK, kSparseStages, true>(p, dummy, dummy, max_chunks, a.stream); break;
-            case 2: e = launch_attn<128, 2, 2, kSparseTK, kSparseStages, true>(p, dummy, dummy, max_chunks, a.stream); break;
+            case 1: e = launch_attn<128, 1, 4, kSparseTK, kSparseStages, true>(p, dummy, dummy, max_chunks, a.stream, p.cs); break;
+            case 2: e = launch_attn<128, 2, 2, kSparseTK, kSparseStages, true>(p, dummy, dummy, max_chunks, a.stream, p.cs); break;
             default: *why = "Hq/Hkv must be <= 32"; return SDKV_ERR_UNSUPPORTED;
         }
     } else {
         switch (MT) {
-            case 1: e = launch_attn<64, 1, 4, kSparseTK, kSparseStages, true>(p, dummy, dummy, max_chunks, a.stream); break;
-            case 2: e = launch_attn<64, 2, 2, kSparseTK, kSparseStages, true>(p, dummy, dummy, max_chunks, a.stream); break;
+            case 1: e = launch_attn<64, 1, 4, kSparseTK, kSparseStages, true>(p, dummy, dummy, max_chunks, a.stream, p.cs); break;
+            case 2: e = launch_attn<64, 2, 2, kSparseTK, kSparseStages, true>(p, dummy, dummy, max_chunks, a.stream, p.cs); break;
             default: *why = "Hq/Hkv must be <= 32"; return SDKV_ERR_UNSUPPORTED;
         }
     }
