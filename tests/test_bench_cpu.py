@@ -1,0 +1,85 @@
+"""CPU checks of the measurement side: the byte account of the workloads, the
+reference arm's JSON line, and the multi-rank helpers of bench.py (max over
+ranks, barrier) on world_size 2 with the gloo backend."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+import workloads
+from sparse_kv_decode_gb300 import byte_account as ba
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_algorithmic_bytes_of_the_llama_32k_layer():
+    w = workloads.WORKLOADS[2]
+    dense = ba.dense_verify_bytes(w.batch, w.hq, w.hkv, w.d, w.n - 1, 1)
+    sparse = ba.sparse_decode_bytes(w.batch, w.hq, w.d, w.batch * w.hkv * w.keep[0])
+    assert dense == 8 * 32768 * 512 + 32 * 512              # full K/V + q in / o out
+    assert round(dense / 1e6, 1) == 134.2
+    assert round(sparse / 1e6, 1) == 40.6                    # 8 x 9830 rows x (512 B + int32 index)
+    # the byte bound of 30% selection over dense (ByteCross ideal speedup, attention only)
+    assert 3.2 < dense / sparse < 3.4
+
+
+def test_keep_lengths_of_the_workloads():
+    assert workloads.WORKLOADS[2].keep == (9830,)
+    assert workloads.WORKLOADS[4].keep == (13107, 39321, 65536)
+    w3 = workloads.WORKLOADS[3]
+    assert w3.frames * w3.frame_tokens + w3.text_tokens == w3.n == 12800
+
+
+def test_reference_arm_prints_one_json_line():
+    env = dict(os.environ, PYTHONPATH=ROOT)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                        "tiny", "--steps", "1", "--warmup", "0"], capture_output=True, text=True, env=env,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference"
+    assert rec["unit"] == "us/step" and rec["value"] > 0
+    assert rec["e2e"]["h2d_bytes_per_step"] == 0
+    assert rec["cpu_baseline"]["kind"] == "oracle"
+    assert rec["warmup"] >= 3
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    w, r, _ = bench.dist_init()
+    bench.barrier(w)
+    m = bench.max_over_ranks(10.0 + 5.0 * r, w)
+    q.put((r, w, m))
+    torch.distributed.destroy_process_group()
+
+
+def test_bench_max_over_ranks_gloo_two_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(2))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res == [(0, 2, 15.0), (1, 2, 15.0)]
