@@ -5,9 +5,10 @@
 // must be normalised over ALL its visible keys before rows are summed, so the
 // keys are read twice:
 //   pass 1: per row, the running max m and sum l of 2^(x - m) over the keys
-//           (x = scale * log2(e) * q.k); partial (m, l) per key split, merged by
-//           the last split CTA of the row block (atomic ticket) into (M, 1/L);
-//   pass 2: per key, sum over rows of 2^(x - M) / L.
+//           (x = scale * log2(e) * q.k), one partial (m, l) per key split;
+//   pass 2: merges the split partials of its rows into (M, L) in its prologue
+//           (overlapping its first tile), then per key sums 2^(x - M - log2 L)
+//           over the rows.
 //
 // Both passes run the 128-row x 128-key x d contraction on the 5th-generation
 // tensor cores (tcgen05.mma, bf16 in, fp32 accumulators in tensor memory):
@@ -34,10 +35,8 @@ struct ScoreParams {
     float scale_log2, inv_w;
     float* scores;
     int* status;
-    int* tick1;       // [BH][n_mg]
     int* tick2;       // [BH][nsplit]
-    float* st_part;   // [BH][nsplit][R][2]
-    float* st_final;  // [BH][R][2]  (M, 1/L)
+    float* st_part;   // [BH][nsplit][R][2]  pass-1 (m, l) per key split
     float* sc_part;   // [n_mg][BH][n]
 };
 
@@ -55,9 +54,8 @@ struct ScoreCfg {
     static constexpr int HALF_B = TK * 128;       // one 64-wide K-block of a 128-row operand
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = Q_B;
-    static constexpr int OFF_CB = OFF_K + STAGES * TILE_B;     // pass 2: -M per row
-    static constexpr int OFF_CI = OFF_CB + ROWS * 4;           // pass 2: 1/L per row
-    static constexpr int OFF_LIM = OFF_CI + ROWS * 4;          // last visible key per row
+    static constexpr int OFF_CB = OFF_K + STAGES * TILE_B;     // pass 2: -(M + log2 L) per row
+    static constexpr int OFF_LIM = OFF_CB + ROWS * 4;          // last visible key per row
     static constexpr int OFF_RED = OFF_LIM + ROWS * 4;         // [2][TK] half sums / [ROWS][2] stats
     static constexpr int OFF_BAR = OFF_RED + 2 * TK * 4;
     static constexpr int NBAR = 2 * STAGES + 1 + 2 + 2;
@@ -187,19 +185,56 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
         const int half = ew >> 2;           // accumulator columns half*64 .. +63
         const int tl = 32 * quad + lane;    // accumulator lane of this thread
         float* cb = reinterpret_cast<float*>(smem + C::OFF_CB);
-        float* ci = reinterpret_cast<float*>(smem + C::OFF_CI);
         int* lim = reinterpret_cast<int*>(smem + C::OFF_LIM);
         float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
         const int et = ew * 32 + lane;      // 0 .. NET-1
         if (et < C::ROWS) {
             const int r = row_base + et;
             lim[et] = (r < p.R) ? p.q_pos0 + r % p.W : -1;
-            if (PASS2) {
-                float2 st = make_float2(INFINITY, 0.f);   // rows past R: -M = -inf, 1/L = 0
-                if (r < p.R)
-                    st = __ldcg(reinterpret_cast<const float2*>(p.st_final + (static_cast<size_t>(bh) * p.R + r) * 2));
-                cb[et] = -st.x;
-                ci[et] = st.y;
+        }
+        if constexpr (PASS2) {
+            // Row statistics over the key splits of pass 1: thread et merges splits
+            // s = et/128, et/128 + 2, ... of row et%128 (up to 16 loads in flight),
+            // the two halves meet in shared memory.  The exponent bias of a row is
+            // -(M + log2 L), so a key's probability is 2^(c*q.k + bias).
+            const int rr = et & (C::ROWS - 1), s0 = et >> 7;
+            const int r = row_base + rr;
+            float mm = -INFINITY, ll = 0.f;
+            if (r < p.R) {
+                const float* base = p.st_part + (static_cast<size_t>(bh) * p.nsplit * p.R + r) * 2;
+                const size_t stride = static_cast<size_t>(p.R) * 2;
+                for (int sb = s0; sb < p.nsplit; sb += 32) {
+                    float2 v2[16];
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        const int sidx = sb + 2 * u;
+                        v2[u] = sidx < p.nsplit ? __ldcg(reinterpret_cast<const float2*>(base + sidx * stride))
+                                                : make_float2(-INFINITY, 0.f);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        if (v2[u].x == -INFINITY) continue;
+                        if (v2[u].x > mm) {
+                            ll = ll * fast_exp2(mm - v2[u].x) + v2[u].y;
+                            mm = v2[u].x;
+                        } else {
+                            ll += v2[u].y * fast_exp2(v2[u].x - mm);
+                        }
+                    }
+                }
+            }
+            if (s0 == 1) {
+                red[2 * rr] = mm;
+                red[2 * rr + 1] = ll;
+            }
+            named_bar_sync(1, C::NET);
+            if (s0 == 0) {
+                const float m2 = red[2 * rr], l2 = red[2 * rr + 1];
+                const float M = fmaxf(mm, m2);
+                float L = 0.f;
+                if (M != -INFINITY)
+                    L = (mm == -INFINITY ? 0.f : ll * fast_exp2(mm - M)) + (m2 == -INFINITY ? 0.f : l2 * fast_exp2(m2 - M));
+                cb[rr] = (r < p.R && L > 0.f) ? -(M + fast_log2(L)) : -INFINITY;   // rows past R add nothing
             }
         }
         named_bar_sync(1, C::NET);
@@ -262,11 +297,10 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
 #pragma unroll
                     for (int i = 0; i < 64; i += 4) {
                         const float4 b4 = *reinterpret_cast<const float4*>(cb + half * 64 + i);
-                        const float4 c4 = *reinterpret_cast<const float4*>(ci + half * 64 + i);
-                        float e0 = fast_exp2(fmaf(__uint_as_float(v[i + 0]), c, b4.x)) * c4.x;
-                        float e1 = fast_exp2(fmaf(__uint_as_float(v[i + 1]), c, b4.y)) * c4.y;
-                        float e2 = fast_exp2(fmaf(__uint_as_float(v[i + 2]), c, b4.z)) * c4.z;
-                        float e3 = fast_exp2(fmaf(__uint_as_float(v[i + 3]), c, b4.w)) * c4.w;
+                        float e0 = fast_exp2(fmaf(__uint_as_float(v[i + 0]), c, b4.x));
+                        float e1 = fast_exp2(fmaf(__uint_as_float(v[i + 1]), c, b4.y));
+                        float e2 = fast_exp2(fmaf(__uint_as_float(v[i + 2]), c, b4.z));
+                        float e3 = fast_exp2(fmaf(__uint_as_float(v[i + 3]), c, b4.w));
                         if (!all_rows) {
                             const int4 l4 = *reinterpret_cast<const int4*>(lim + half * 64 + i);
                             e0 = key <= l4.x ? e0 : 0.f;
@@ -315,36 +349,6 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
                         *reinterpret_cast<float2*>(p.st_part + ((static_cast<size_t>(bh) * p.nsplit + sp) * p.R + r) * 2) =
                             make_float2(M, L);
                 }
-                __threadfence();
-                named_bar_sync(1, C::NET);
-                if (et == 0) {
-                    const int old = atomicAdd(p.tick1 + bh * p.n_mg + mg, 1);
-                    s_last = (old == p.nsplit - 1);
-                }
-                named_bar_sync(1, C::NET);
-                if (s_last) {
-                    __threadfence();
-                    const int r = row_base + et;   // one thread per row
-                    if (et < C::ROWS && r < p.R) {
-                        const float* base = p.st_part + (static_cast<size_t>(bh) * p.nsplit * p.R + r) * 2;
-                        const size_t stride = static_cast<size_t>(p.R) * 2;
-                        float mm = -INFINITY, ll = 0.f;
-#pragma unroll 4
-                        for (int s = 0; s < p.nsplit; ++s) {
-                            const float2 v2 = __ldcg(reinterpret_cast<const float2*>(base + s * stride));
-                            if (v2.x == -INFINITY) continue;
-                            if (v2.x > mm) {
-                                ll = ll * fast_exp2(mm - v2.x) + v2.y;
-                                mm = v2.x;
-                            } else {
-                                ll += v2.y * fast_exp2(v2.x - mm);
-                            }
-                        }
-                        *reinterpret_cast<float2*>(p.st_final + (static_cast<size_t>(bh) * p.R + r) * 2) =
-                            make_float2(mm, ll > 0.f ? 1.f / ll : 0.f);
-                    }
-                    if (et == 0) atomicExch(p.tick1 + bh * p.n_mg + mg, 0);
-                }
             } else if (p.n_mg > 1) {
                 __threadfence();
                 named_bar_sync(1, C::NET);
@@ -390,7 +394,7 @@ namespace {
 
 struct ScorePlan {
     int n_mg, nsplit, chunk;
-    size_t off_t1, off_t2, off_sp, off_sf, off_sc, bytes;
+    size_t off_t2, off_sp, off_sc, bytes;
 };
 
 ScorePlan score_plan(int B, int Hq, int Hkv, int n, int W, int num_sms) {
@@ -407,15 +411,11 @@ ScorePlan score_plan(int B, int Hq, int Hkv, int n, int W, int num_sms) {
     pl.nsplit = (n + chunk - 1) / chunk;
     pl.chunk = chunk;
     size_t off = kWsHeader;
-    pl.off_t1 = off;
-    off += sizeof(int) * static_cast<size_t>(BH) * pl.n_mg;
     pl.off_t2 = off;
     off += sizeof(int) * static_cast<size_t>(BH) * pl.nsplit;
     off = align256(off);
     pl.off_sp = off;
     off = align256(off + sizeof(float) * 2 * static_cast<size_t>(BH) * pl.nsplit * R);
-    pl.off_sf = off;
-    off = align256(off + sizeof(float) * 2 * static_cast<size_t>(BH) * R);
     pl.off_sc = off;
     if (pl.n_mg > 1) off = align256(off + sizeof(float) * static_cast<size_t>(pl.n_mg) * BH * n);
     pl.bytes = off;
@@ -481,10 +481,8 @@ int launch_score(const ScoreLaunch& a, const CUtensorMap* tmk, const CUtensorMap
     p.inv_w = 1.0f / static_cast<float>(a.W);
     p.scores = a.scores;
     p.status = reinterpret_cast<int*>(ws);
-    p.tick1 = reinterpret_cast<int*>(ws + pl.off_t1);
     p.tick2 = reinterpret_cast<int*>(ws + pl.off_t2);
     p.st_part = reinterpret_cast<float*>(ws + pl.off_sp);
-    p.st_final = reinterpret_cast<float*>(ws + pl.off_sf);
     p.sc_part = reinterpret_cast<float*>(ws + pl.off_sc);
     const int grid = p.BH * pl.n_mg * pl.nsplit;
     cudaError_t e;
