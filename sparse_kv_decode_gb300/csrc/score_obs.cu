@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
         mbar_init(bar_q, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_tfull + 8 * i, 1);
-            mbar_init(bar_tempty + 8 * i, C::NEPI);
+            mbar_init(bar_tempty + 8 * i, C::NEPI / 2);   // one epilogue group per buffer
         }
         fence_mbar_init();
         s_abort = 0;
@@ -244,83 +244,92 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
         float m_run = -INFINITY, l_run = 0.f;
         bool aborted = false;
 
-        for (int t = 0; t < ntiles; ++t) {
+        // Epilogue group `half` (warps 2-5 or 6-9) takes the tiles of its parity,
+        // i.e. always accumulator buffer `half`, all 128 columns; the two groups
+        // never meet inside the loop.  Columns are read 64 at a time; the buffer
+        // is handed back to the MMA issuer as soon as the second half is loaded.
+        for (int t = half; t < ntiles; t += 2) {
             const int buf = t & 1;
-            const bool bad = !mbar_wait(bar_tfull + 8 * buf, (t >> 1) & 1);
-            if (bad) aborted = true;
-            uint32_t v[64];
-            if (!bad) {
-                tc_fence_after();
-                const uint32_t ta = tmem + (static_cast<uint32_t>(32 * quad) << 16) + buf * C::TK + half * 64;
-                tmem_ld32(ta, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-                tmem_ld32(ta + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-                tmem_wait_ld();
-                tc_fence_before();
+            if (!mbar_wait(bar_tfull + 8 * buf, (t >> 1) & 1)) {
+                aborted = true;
+                break;
             }
-            __syncwarp();
-            if (lane == 0 && !bad) mbar_arrive(bar_tempty + 8 * buf);
+            tc_fence_after();
+            const uint32_t ta = tmem + (static_cast<uint32_t>(32 * quad) << 16) + buf * C::TK;
             const int key0 = lo + t * C::TK;
-            if constexpr (!PASS2) {
-                if (bad) break;
-                if (my_lim >= 0) {
-                    // columns are keys key0 + half*64 + i
-                    const int kfirst = key0 + half * 64;
-                    const bool full = (kfirst + 63 < hi) && (kfirst + 63 <= my_lim);
-                    float mx = -INFINITY;
-                    if (full) {
+            float acc = 0.f;   // pass 2: this key's sum over the rows
 #pragma unroll
-                        for (int i = 0; i < 64; ++i) mx = fmaxf(mx, __uint_as_float(v[i]));
-                    } else {
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t v[64];
+                tmem_ld32(ta + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+                tmem_ld32(ta + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+                tmem_wait_ld();
+                if (hh == 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_tempty + 8 * buf);
+                }
+                if constexpr (!PASS2) {
+                    // row tl, columns = keys key0 + hh*64 + i
+                    if (my_lim >= 0) {
+                        const int kfirst = key0 + hh * 64;
+                        const bool full = (kfirst + 63 < hi) && (kfirst + 63 <= my_lim);
+                        float mx = -INFINITY;
+                        if (full) {
 #pragma unroll
-                        for (int i = 0; i < 64; ++i) {
-                            const int key = kfirst + i;
-                            const float x = (key < hi && key <= my_lim) ? __uint_as_float(v[i]) : -INFINITY;
-                            v[i] = __float_as_uint(x);
-                            mx = fmaxf(mx, x);
+                            for (int i = 0; i < 64; ++i) mx = fmaxf(mx, __uint_as_float(v[i]));
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 64; ++i) {
+                                const int key = kfirst + i;
+                                const float x = (key < hi && key <= my_lim) ? __uint_as_float(v[i]) : -INFINITY;
+                                v[i] = __float_as_uint(x);
+                                mx = fmaxf(mx, x);
+                            }
+                        }
+                        if (mx != -INFINITY) {
+                            const float mnew = fmaxf(m_run, mx * c);
+                            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                            for (int i = 0; i < 64; ++i) s4[i & 3] += fast_exp2(fmaf(__uint_as_float(v[i]), c, -mnew));
+                            l_run = l_run * fast_exp2(m_run - mnew) + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+                            m_run = mnew;
                         }
                     }
-                    if (mx != -INFINITY) {
-                        const float mnew = fmaxf(m_run, mx * c);
-                        float acc = 0.f;
-#pragma unroll
-                        for (int i = 0; i < 64; ++i) acc += fast_exp2(fmaf(__uint_as_float(v[i]), c, -mnew));
-                        l_run = l_run * fast_exp2(m_run - mnew) + acc;
-                        m_run = mnew;
-                    }
-                }
-            } else {
-                // lane tl is key key0 + tl; columns are window rows half*64 + i
-                const int key = key0 + tl;
-                float acc = 0.f;
-                if (!bad) {
+                } else {
+                    // lane tl is key key0 + tl; columns are window rows hh*64 + i
+                    const int key = key0 + tl;
                     const bool all_rows = key0 + C::TK - 1 <= p.q_pos0;
+                    float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int i = 0; i < 64; i += 4) {
-                        const float4 b4 = *reinterpret_cast<const float4*>(cb + half * 64 + i);
+                        const float4 b4 = *reinterpret_cast<const float4*>(cb + hh * 64 + i);
                         float e0 = fast_exp2(fmaf(__uint_as_float(v[i + 0]), c, b4.x));
                         float e1 = fast_exp2(fmaf(__uint_as_float(v[i + 1]), c, b4.y));
                         float e2 = fast_exp2(fmaf(__uint_as_float(v[i + 2]), c, b4.z));
                         float e3 = fast_exp2(fmaf(__uint_as_float(v[i + 3]), c, b4.w));
                         if (!all_rows) {
-                            const int4 l4 = *reinterpret_cast<const int4*>(lim + half * 64 + i);
+                            const int4 l4 = *reinterpret_cast<const int4*>(lim + hh * 64 + i);
                             e0 = key <= l4.x ? e0 : 0.f;
                             e1 = key <= l4.y ? e1 : 0.f;
                             e2 = key <= l4.z ? e2 : 0.f;
                             e3 = key <= l4.w ? e3 : 0.f;
                         }
-                        acc += (e0 + e1) + (e2 + e3);
+                        s4[0] += e0;
+                        s4[1] += e1;
+                        s4[2] += e2;
+                        s4[3] += e3;
                     }
+                    acc += (s4[0] + s4[1]) + (s4[2] + s4[3]);
                 }
-                float* rb = red + buf * C::TK;
-                if (half == 1) rb[tl] = acc;
-                // one barrier per tile; it also stops every epilogue warp if any timed out
-                if (named_bar_or(1, C::NET, bad)) break;
-                if (half == 0 && key < hi) {
-                    const float v2 = acc + rb[tl];
+            }
+            if constexpr (PASS2) {
+                const int key = key0 + tl;
+                if (key < hi) {
                     if (p.n_mg == 1)
-                        p.scores[static_cast<size_t>(bh) * p.n + key] = v2 * p.inv_w;
+                        p.scores[static_cast<size_t>(bh) * p.n + key] = acc * p.inv_w;
                     else
-                        p.sc_part[(static_cast<size_t>(mg) * p.BH + bh) * p.n + key] = v2;
+                        p.sc_part[(static_cast<size_t>(mg) * p.BH + bh) * p.n + key] = acc;
                 }
             }
         }
