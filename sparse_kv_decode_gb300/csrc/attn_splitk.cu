@@ -68,8 +68,10 @@ struct AttnCfg {
     static constexpr int OFF_V = STAGES * TILE_B;
     static constexpr int OFF_Q = 2 * STAGES * TILE_B;
     static constexpr int OFF_ML = OFF_Q + ROWS * QPITCH;          // [KW][ROWS] (m, l)
-    static constexpr int OFF_XML = OFF_ML + KW * ROWS * 2 * 4;    // [ROWS] (m, l) shown to the cluster
-    static constexpr int OFF_BAR = OFF_XML + ROWS * 2 * 4;
+    // cluster merge: what the peers push to this CTA (its slice of the head dims)
+    static constexpr int OFF_RCV = OFF_ML + KW * ROWS * 2 * 4;    // [src][R][D/cs] fp32
+    static constexpr int OFF_RML = OFF_RCV + ROWS * D * 4;           // [src][R] (m, l)
+    static constexpr int OFF_BAR = OFF_RML + 8 * ROWS * 2 * 4;
     static constexpr int SMEM = OFF_BAR + 2 * STAGES * 8;
     static constexpr int SMEM_ALLOC = SMEM + 1024;
     static_assert((TILE_B % 1024) == 0, "swizzled stages need 1024-byte alignment");
@@ -300,10 +302,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
                 }
             }
         }
-        if (p.cs > 1) {   // the two cluster barriers of the consumers' epilogue
-            cluster_sync_all();
-            cluster_sync_all();
-        }
+        if (p.cs > 1) cluster_sync_all();   // the consumers' cluster barrier
         return;
     }
 
@@ -443,10 +442,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
                 mbar_wait(bar_full + 8 * s, (last_t / STAGES) & 1);
             }
         }
-        if (p.cs > 1) {
-            cluster_sync_all();
-            cluster_sync_all();
-        }
+        if (p.cs > 1) cluster_sync_all();
         return;
     }
 
@@ -502,9 +498,16 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
             const int g = row / p.gamma, tt = row - (row / p.gamma) * p.gamma;
             const size_t orow = (static_cast<size_t>(b) * p.Hq + h * p.G + g) * p.gamma + tt;
             if (p.cs > 1) {
-                // shown to the cluster: in place of group 0's parked row (read above by this thread only)
-                *reinterpret_cast<float4*>(mrg + row * C::MPITCH + d0) = a4;
-                if (d0 == 0) *reinterpret_cast<float2*>(smem + C::OFF_XML + row * 8) = make_float2(M, L);
+                // push to the cluster CTA that owns these dims (its receive buffer is
+                // not used by the main loop, so early pushes are safe); (M, L) to all
+                const int SL = D / p.cs;
+                const uint32_t me = cluster_ctarank();
+                const int owner = d0 / SL;
+                st_dsmem_f4(dsmem_addr(sbase + C::OFF_RCV + ((me * p.R + row) * SL + (d0 - owner * SL)) * 4, owner),
+                            a4);
+                if (d0 == 0)
+                    for (int r = 0; r < p.cs; ++r)
+                        st_dsmem_f2(dsmem_addr(sbase + C::OFF_RML + (me * p.R + row) * 8, r), make_float2(M, L));
             } else if (nch == 1) {
                 const float il = L > 0.f ? 1.f / L : 0.f;
                 uint2 packed;
@@ -522,42 +525,35 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
     }
     {
         if (p.cs > 1) {
-            // ---------------------------------------------- merge the cluster's splits through DSMEM
-            // CTA `rank` of the cluster reduces head dims [rank*D/cs, (rank+1)*D/cs) of
-            // every row over the cs splits of the cluster, reading the peers' rows
-            // from their shared memory; one partial per cluster (or the output, when
-            // one cluster covers the head) goes to global memory.
+            // ---------------------------------------------- merge the cluster's splits
+            // CTA `rank` of the cluster owns head dims [rank*D/cs, (rank+1)*D/cs); every
+            // CTA has pushed its rows' slices and (M, L) into the owners' shared
+            // memory, so after one cluster barrier the merge reads local memory only.
+            // One partial per cluster (or the output, when one cluster covers the
+            // head) goes to global memory.
             cluster_sync_all();
             const int CS = p.cs;
+            const int SL = D / CS;
             const uint32_t rank = cluster_ctarank();
-            const int sl4 = D / CS / 4;                      // float4 per row in this slice
+            const int sl4 = SL / 4;                          // float4 per row in this slice
             const int gcl = cidx / CS;                       // global cluster index (partial slot)
             const int gcl0 = c0 / CS, ncl_h = nch / CS;      // the head's clusters
-            const uint32_t xml_s = sbase + C::OFF_XML, mrg_s = sbase + C::OFF_K;
+            const float* rcv = reinterpret_cast<const float*>(smem + C::OFF_RCV);
+            const float2* rml = reinterpret_cast<const float2*>(smem + C::OFF_RML);
             for (int e = tid; e < p.R * sl4; e += C::NCT) {
                 const int row = e / sl4;
-                const int d0 = static_cast<int>(rank) * (D / CS) + 4 * (e - row * sl4);
-                float mc[8], lc[8];
+                const int dd = 4 * (e - row * sl4);
+                const int d0 = static_cast<int>(rank) * SL + dd;
                 float M = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    mc[c] = -INFINITY;
-                    lc[c] = 0.f;
-                    if (c < CS) {
-                        const float2 v = ld_dsmem_f2(dsmem_addr(xml_s + row * 8, c));
-                        mc[c] = v.x;
-                        lc[c] = v.y;
-                        M = fmaxf(M, v.x);
-                    }
-                }
+                for (int c = 0; c < CS; ++c) M = fmaxf(M, rml[c * p.R + row].x);
                 float L = 0.f;
                 float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    if (c >= CS || mc[c] == -INFINITY) continue;
-                    const float w = fast_exp2(mc[c] - M);
-                    L += w * lc[c];
-                    const float4 v4 = ld_dsmem_f4(dsmem_addr(mrg_s + (row * C::MPITCH + d0) * 4, c));
+                for (int c = 0; c < CS; ++c) {
+                    const float2 ml2 = rml[c * p.R + row];
+                    if (ml2.x == -INFINITY) continue;
+                    const float w = fast_exp2(ml2.x - M);
+                    L += w * ml2.y;
+                    const float4 v4 = *reinterpret_cast<const float4*>(rcv + (c * p.R + row) * SL + dd);
                     a4.x += w * v4.x;
                     a4.y += w * v4.y;
                     a4.z += w * v4.z;
@@ -574,13 +570,12 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
                     if (d0 == 0 && p.lse) p.lse[orow] = L > 0.f ? (M + fast_log2(L)) * kLn2 : -INFINITY;
                 } else {
                     *reinterpret_cast<float4*>(p.part_o + (static_cast<size_t>(gcl) * p.R + row) * D + d0) = a4;
-                    if (e - row * sl4 == 0)   // this rank's copy of the cluster's (M, L)
+                    if (dd == 0)   // this rank's copy of the cluster's (M, L)
                         *reinterpret_cast<float2*>(
                             p.part_ml + ((static_cast<size_t>(gcl) * CS + rank) * p.R + row) * 2) = make_float2(M, L);
                 }
             }
             __threadfence();
-            cluster_sync_all();   // peers may leave only after everyone has read their rows
             if (ncl_h == 1) return;
             named_bar_sync(1, C::NCT);
             if (tid == 0) {
@@ -596,20 +591,32 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
                 const int d0 = static_cast<int>(rank) * (D / CS) + 4 * (e - row * sl4);
                 float mm = -INFINITY, ll = 0.f;
                 float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int cl = 0; cl < ncl_h; ++cl) {
-                    const size_t gi = static_cast<size_t>(gcl0) + cl;
-                    const float2 v2 = __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((gi * CS + rank) * p.R + row) * 2));
-                    const float4 o4 = __ldcg(reinterpret_cast<const float4*>(p.part_o + (gi * p.R + row) * D + d0));
-                    if (v2.x == -INFINITY) continue;
-                    const float mnew = fmaxf(mm, v2.x);
-                    const float fa = (mm == -INFINITY) ? 0.f : fast_exp2(mm - mnew);
-                    const float fb = fast_exp2(v2.x - mnew);
-                    ll = ll * fa + v2.y * fb;
-                    a4.x = a4.x * fa + o4.x * fb;
-                    a4.y = a4.y * fa + o4.y * fb;
-                    a4.z = a4.z * fa + o4.z * fb;
-                    a4.w = a4.w * fa + o4.w * fb;
-                    mm = mnew;
+                for (int cb = 0; cb < ncl_h; cb += 8) {
+                    float2 v2[8];
+                    float4 o4[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {   // all loads of the batch in flight together
+                        const size_t gi = static_cast<size_t>(gcl0) + cb + u;
+                        v2[u] = make_float2(-INFINITY, 0.f);
+                        o4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (cb + u < ncl_h) {
+                            v2[u] = __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((gi * CS + rank) * p.R + row) * 2));
+                            o4[u] = __ldcg(reinterpret_cast<const float4*>(p.part_o + (gi * p.R + row) * D + d0));
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        if (v2[u].x == -INFINITY) continue;
+                        const float mnew = fmaxf(mm, v2[u].x);
+                        const float fa = (mm == -INFINITY) ? 0.f : fast_exp2(mm - mnew);
+                        const float fb = fast_exp2(v2[u].x - mnew);
+                        ll = ll * fa + v2[u].y * fb;
+                        a4.x = a4.x * fa + o4[u].x * fb;
+                        a4.y = a4.y * fa + o4[u].y * fb;
+                        a4.z = a4.z * fa + o4[u].z * fb;
+                        a4.w = a4.w * fa + o4[u].w * fb;
+                        mm = mnew;
+                    }
                 }
                 const int g = row / p.gamma, tt = row - (row / p.gamma) * p.gamma;
                 const size_t orow = (static_cast<size_t>(b) * p.Hq + h * p.G + g) * p.gamma + tt;
