@@ -410,11 +410,14 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
                     l_r[i] += x[nt][2 * i] + x[nt][2 * i + 1];
                 }
             }
-            uint32_t pa[4];
-            pa[0] = pack_bf16(x[0][0], x[0][1]);
-            pa[1] = pack_bf16(x[0][2], x[0][3]);
-            pa[2] = pack_bf16(x[1][0], x[1][1]);
-            pa[3] = pack_bf16(x[1][2], x[1][3]);
+            // P as two bf16 terms, p = hi + lo (about 16 significant bits): the
+            // weights of the PV product then match the fp32 sum l closely even
+            // when a few keys carry the whole softmax
+            uint32_t pa[4], pl[4];
+            split_bf16(x[0][0], x[0][1], pa[0], pl[0]);
+            split_bf16(x[0][2], x[0][3], pa[1], pl[1]);
+            split_bf16(x[1][0], x[1][1], pa[2], pl[2]);
+            split_bf16(x[1][2], x[1][3], pa[3], pl[3]);
 #pragma unroll
             for (int jj = 0; jj < D / 16; ++jj) {
                 uint32_t vb[4];
@@ -422,6 +425,8 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
                 ldsm_x4_t(vb, tile_addr<D, TK, SPARSE>(vst, row, 2 * jj + (lane >> 4)));
                 mma_bf16_16816(o_acc[2 * jj], pa, vb[0], vb[1]);
                 mma_bf16_16816(o_acc[2 * jj + 1], pa, vb[2], vb[3]);
+                mma_bf16_16816(o_acc[2 * jj], pl, vb[0], vb[1]);
+                mma_bf16_16816(o_acc[2 * jj + 1], pl, vb[2], vb[3]);
             }
         }
         __syncwarp();
@@ -575,16 +580,16 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
                             p.part_ml + ((static_cast<size_t>(gcl) * CS + rank) * p.R + row) * 2) = make_float2(M, L);
                 }
             }
-            __threadfence();
             if (ncl_h == 1) return;
             named_bar_sync(1, C::NCT);
             if (tid == 0) {
+                fence_acq_rel_gpu();                       // release this CTA's slice of the partial
                 const int old = atomicAdd(p.tickets + bh * 8 + rank, 1);
+                fence_acq_rel_gpu();                       // acquire the other clusters' (if last)
                 s_last = (old == ncl_h - 1);
             }
             named_bar_sync(1, C::NCT);
             if (!s_last) return;
-            __threadfence();
             // last cluster of the head for this slice: merge the head's cluster partials
             for (int e = tid; e < p.R * sl4; e += C::NCT) {
                 const int row = e / sl4;
@@ -634,15 +639,15 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
     if (nch == 1) return;
 
     // -------------------------------------------------- last CTA of the head merges the partials
-    __threadfence();
     named_bar_sync(1, C::NCT);
     if (tid == 0) {
+        fence_acq_rel_gpu();                               // release this CTA's partial
         const int old = atomicAdd(p.tickets + bh, 1);
+        fence_acq_rel_gpu();                               // acquire the others' (if last)
         s_last = (old == nch - 1);
     }
     named_bar_sync(1, C::NCT);
     if (!s_last) return;
-    __threadfence();
 
     // Partials are merged in batches of splits that fit in the (now idle) stage
     // buffers.  Per batch, one round trip: the batch's o blocks and (m, l) pairs are

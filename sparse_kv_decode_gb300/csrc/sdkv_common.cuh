@@ -81,6 +81,16 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// (a, b) as a bf16 pair hi and the bf16 pair of what rounding left over, lo:
+// a = hi.x + lo.x, b = hi.y + lo.y to about 16 significant bits
+__device__ __forceinline__ void split_bf16(float a, float b, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -151,6 +161,14 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
+// Same copy with a source size of zero: nothing is read, the 16 bytes are zeros.
+__device__ __forceinline__ void cp_async_16_zero(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, 0;" ::"r"(dst), "l"(src) : "memory");
+}
+// GPU-scope acquire-release fence: with a CTA barrier before it, it publishes the
+// CTA's earlier global writes ahead of a following relaxed atomic (release side),
+// and after an atomic it orders the later reads behind it (acquire side).
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 // The mbarrier receives one arrival once every cp.async this thread issued so
 // far has landed (the arrival is counted in the barrier's expected count).
 __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {

@@ -125,6 +125,65 @@ def test_sparse_decode_matches_oracle(B, Hq, Hkv, d, n, lens):
     _status_ok(ws)
 
 
+def test_sparse_many_short_lists():
+    # 20,480 (sequence, KV head) lists of 0..2 entries: the CTA ranges cross more
+    # than a hundred heads each (offsets read on the fly), and the range plan
+    # reads the offsets in several rounds
+    g = torch.Generator().manual_seed(21)
+    B, Hq, Hkv, d, n = 80, 256, 256, 64, 16
+    k = _rand((B, Hkv, n, d), g)
+    v = _rand((B, Hkv, n, d), g, 0.5)   # |o| < 4: a bf16 output then rounds by less than 1e-2
+    q = _rand((B, Hq, d), g)
+    rng = np.random.default_rng(21)
+    lens = rng.integers(0, 3, size=B * Hkv).tolist()
+    offs_d, offs = csr(lens, DEV)
+    _, idx = workloads.random_lists(B, Hkv, n, lens, seed=21)
+    ws = sk.new_workspace(sk.workspace_size(sk.OP_SPARSE_DECODE, B, Hq, Hkv, d, 0, 0), DEV)
+    o, lse = sk.sparse_decode_attn(q.to(DEV), k.to(DEV), v.to(DEV), offs_d, idx.to(DEV), scale_of(d), ws=ws)
+    o_ref, l_ref = oracle.sparse_decode(q, k, v, offs, idx.numpy())
+    assert_attn_close(o, o_ref, "sparse short lists")
+    assert_lse_close(lse, l_ref, "sparse short lists")
+    _status_ok(ws)
+
+
+def test_sparse_ragged_mha_lists_cross_ranges():
+    # SparseMM-like: one query row per KV head, lengths from 0 to the whole cache,
+    # so CTA ranges start and end inside lists and span several lists
+    g = torch.Generator().manual_seed(22)
+    B, Hq, Hkv, d, n = 2, 32, 32, 128, 2048
+    k = _rand((B, Hkv, n, d), g)
+    v = _rand((B, Hkv, n, d), g)
+    q = _rand((B, Hq, d), g, 1.5)
+    rng = np.random.default_rng(22)
+    lens = rng.integers(0, n + 1, size=B * Hkv).tolist()
+    lens[3] = 0
+    lens[4] = n
+    offs_d, offs = csr(lens, DEV)
+    _, idx = workloads.random_lists(B, Hkv, n, lens, seed=22)
+    ws = sk.new_workspace(sk.workspace_size(sk.OP_SPARSE_DECODE, B, Hq, Hkv, d, 0, 0), DEV)
+    for _ in range(2):   # the per-head tickets are back at zero after a call
+        o, lse = sk.sparse_decode_attn(q.to(DEV), k.to(DEV), v.to(DEV), offs_d, idx.to(DEV), scale_of(d), ws=ws)
+        o_ref, l_ref = oracle.sparse_decode(q, k, v, offs, idx.numpy())
+        assert_attn_close(o, o_ref, "sparse ragged mha")
+        assert_lse_close(lse, l_ref, "sparse ragged mha")
+    _status_ok(ws)
+
+
+def test_dense_many_heads_per_range():
+    # 256 KV heads of 302 rows: CTA ranges hold parts of two or three heads
+    g = torch.Generator().manual_seed(23)
+    B, Hq, Hkv, d, n_prefix, gamma = 4, 64, 64, 128, 300, 2
+    k = _rand((B, Hkv, n_prefix + gamma, d), g)
+    v = _rand((B, Hkv, n_prefix + gamma, d), g)
+    q = _rand((B, Hq, gamma, d), g, 1.5)
+    ws = sk.new_workspace(sk.workspace_size(sk.OP_DENSE_VERIFY, B, Hq, Hkv, d, n_prefix + gamma, gamma), DEV)
+    o, lse = sk.dense_verify_attn(q.to(DEV), k.to(DEV), v.to(DEV), n_prefix, scale_of(d), ws=ws)
+    o_ref, l_ref = oracle.dense_verify(q, k, v, n_prefix)
+    assert_attn_close(o, o_ref, "dense many heads")
+    assert_lse_close(lse, l_ref, "dense many heads")
+    _status_ok(ws)
+
+
 def test_sparse_keep_all_equals_dense_on_gpu():
     g = torch.Generator().manual_seed(3)
     B, Hq, Hkv, d, n = 1, 32, 8, 128, 5000
