@@ -261,9 +261,7 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 uint32_t v[64];
-                tmem_ld32(ta + hh * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-                tmem_ld32(ta + hh * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-                tmem_wait_ld();
+                tmem_ld64_sync(ta + hh * 64, v);
                 if (hh == 1) {
                     tc_fence_before();
                     __syncwarp();
