@@ -19,6 +19,14 @@ Every function here restates, in numpy float64, what the pages define:
                     one query over the selected keys only.
   dense_verify      StD section 3.1: gamma drafted positions verified in one
                     pass over the full cache, causal among the drafts.
+  window_lists      StD baselines ("Streaming") / ByteCross "The Attention
+                    Baseline": attention sinks plus the recent window.
+  compact_kv,       ByteCross "Speedup Across Context": selected entries
+  sparse_decode_    gathered into a contiguous buffer read by every later step.
+  compact
+  specvlm_*         SpecVLM post, "The SpecVLM Method": top-P retention of the
+                    verifier's attention mass, then uniform subsampling.
+  append_drafts     StD 3.1: the draft steps' lists grow by the drafted tokens.
 
 Pins (tests/test_oracle_pins.py) tie each function to closed forms,
 invariants, brute force and printed values; none is "parity unpinned".
@@ -32,4 +40,11 @@ from .sdkv_oracle import (  # noqa: F401
     sparse_decode,
     dense_verify,
     to_f64,
+    window_lists,
+    compact_kv,
+    sparse_decode_compact,
+    specvlm_importance,
+    specvlm_select,
+    append_drafts,
+    MASS_FRAC_BITS,
 )

@@ -271,3 +271,144 @@ def dense_verify(q, k, v, n_prefix: int, scale: float | None = None):
                 o[b, hq, t], lse[b, hq, t] = _attend(q[b, hq, t], k[b, h, : last + 1],
                                                      v[b, h, : last + 1], scale)
     return o, lse
+
+
+# ---------------------------------------------------------------------------
+# Next rows beyond the hot path
+# ---------------------------------------------------------------------------
+
+# f2  StreamingLLM-style lists: attention sinks plus the recent window, no
+#     scoring (StD, Baselines: the "Streaming" draft model; ByteCross, "The
+#     Attention Baseline": a sink-plus-recent window timed against dense).
+
+def window_lists(B: int, Hkv: int, n: int, n_sink: int, n_recent: int):
+    """Every (b, h) keeps the first n_sink and the last n_recent of its n cache
+    rows, ascending and without repeats (all n rows when they overlap).
+    Returns CSR (offsets int64 [B*Hkv+1], indices int32)."""
+    keep = sorted(set(range(0, min(n_sink, n))) | set(range(max(n - n_recent, 0), n)))
+    BH = B * Hkv
+    offsets = np.arange(BH + 1, dtype=np.int64) * len(keep)
+    indices = np.tile(np.asarray(keep, dtype=np.int32), BH)
+    return offsets, indices
+
+
+# f1  contiguous compaction of the selected rows (ByteCross, "Speedup Across
+#     Context": the selected entries are gathered into a contiguous buffer
+#     that every later step reads in one kernel call).
+
+def compact_kv(k, v, offsets, indices):
+    """Row offsets[i] - offsets[0] + j of the output is row indices[offsets[i] + j]
+    of KV head (b, h) = divmod(i, Hkv) of the cache: each head's selected rows in
+    list order, the heads one after another.  Returns (k_c, v_c), [total][d]."""
+    k = to_f64(k)
+    v = to_f64(v)
+    offsets = np.asarray(offsets, dtype=np.int64)
+    indices = np.asarray(indices, dtype=np.int64)
+    B, Hkv, _, d = k.shape
+    total = int(offsets[-1] - offsets[0])
+    k_c = np.zeros((total, d))
+    v_c = np.zeros((total, d))
+    for i in range(B * Hkv):
+        b, h = divmod(i, Hkv)
+        sel = indices[offsets[i]: offsets[i + 1]]
+        a = int(offsets[i] - offsets[0])
+        k_c[a: a + len(sel)] = k[b, h, sel]
+        v_c[a: a + len(sel)] = v[b, h, sel]
+    return k_c, v_c
+
+
+def sparse_decode_compact(q, k_c, v_c, offsets, Hkv: int, scale: float | None = None):
+    """Decode over compacted rows: query head hq of sequence b attends the rows
+    [offsets[i] - offsets[0], offsets[i+1] - offsets[0]) of k_c / v_c, with
+    i = b * Hkv + hq // G.  Same definition as sparse_decode, other addressing."""
+    q = to_f64(q)
+    k_c = to_f64(k_c)
+    v_c = to_f64(v_c)
+    offsets = np.asarray(offsets, dtype=np.int64)
+    B, Hq, d = q.shape
+    G = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = np.zeros((B, Hq, d))
+    lse = np.zeros((B, Hq))
+    for b in range(B):
+        for hq in range(Hq):
+            i = b * Hkv + hq // G
+            a, z = int(offsets[i] - offsets[0]), int(offsets[i + 1] - offsets[0])
+            o[b, hq], lse[b, hq] = _attend(q[b, hq], k_c[a:z], v_c[a:z], scale)
+    return o, lse
+
+
+# f3  SpecVLM selection (SpecVLM post, "The SpecVLM Method": Stage I
+#     verifier-guided top-P retention, Stage II spatially uniform reduction).
+
+MASS_FRAC_BITS = 32   # masses are compared as exact sums of multiples of 2^-32
+
+
+def specvlm_importance(scores):
+    """a_j = the mean over all attention maps (layers x heads) of their score
+    for token j.  scores: [units][n] -> [n] (float64)."""
+    s = to_f64(scores)
+    return s.reshape(-1, s.shape[-1]).mean(axis=0)
+
+
+def specvlm_select(a, v_lo: int, v_hi: int, lam_r: float, r: float, keep_lo: int, keep_hi: int) -> np.ndarray:
+    """Draft-side token list for the video tokens V = [v_lo, v_hi) and the
+    always-kept range [keep_lo, keep_hi) (the text tokens), ascending.
+
+    Stage I: order V by a_j descending (equal a_j: lower index first) and keep
+    the shortest prefix V_R whose mass reaches lam_r times the mass of V.
+    Stage II: walk the other tokens of V in index order at the interval
+    I = (|V| - |V_R|) / ((1 - r) |V|) and keep the ones at positions
+    floor(k I), k = 0, 1, ...  The list is V_R u V_U u [keep_lo, keep_hi).
+
+    Readings: a_j are the fp32 scores the caller passes; each mass is a_j
+    rounded to the nearest multiple of 2^-32 (exact integer sums, so the
+    crossing is decided exactly); the target lam_r * S and I are float64.
+    """
+    a = np.asarray(a, dtype=np.float64)
+    V = np.arange(v_lo, v_hi)
+    nV = len(V)
+    if nV == 0:
+        return np.arange(keep_lo, keep_hi, dtype=np.int32)
+    av = a[V]
+    fx = [int(np.rint(x * 2.0 ** MASS_FRAC_BITS)) for x in av]          # exact Python ints
+    order = sorted(range(nV), key=lambda j: (-av[j], j))
+    S = sum(fx)
+    target = lam_r * float(S)
+    acc, c = 0, 0
+    while c < nV and float(acc) < target:
+        acc += fx[order[c]]
+        c += 1
+    retained = set(int(V[j]) for j in order[:c])
+    left = [int(x) for x in V if int(x) not in retained]
+    I = float(nV - c) / ((1.0 - r) * float(nV))
+    sampled = set()
+    k = 0
+    while True:
+        pos = math.floor(k * I) if I > 0 else len(left)
+        if pos >= len(left):
+            break
+        sampled.add(left[pos])
+        k += 1
+    out = sorted(retained | sampled | set(range(keep_lo, keep_hi)))
+    return np.asarray(out, dtype=np.int32)
+
+
+# f4  StD draft lists (StD, 3.1 Decoding Procedures / 3.2): draft step t sees
+#     the base selection plus the t + 1 drafted positions appended so far.
+
+def append_drafts(base_offsets, base_indices, n_pos: int, n_new: int):
+    """Each (b, h) list of the base CSR followed by n_pos, ..., n_pos + n_new - 1.
+    Returns the new CSR (offsets int64, indices int32)."""
+    bo = np.asarray(base_offsets, dtype=np.int64)
+    bi = np.asarray(base_indices, dtype=np.int64)
+    BH = len(bo) - 1
+    offs = [0]
+    parts = []
+    for i in range(BH):
+        parts.append(bi[bo[i]: bo[i + 1]])
+        parts.append(np.arange(n_pos, n_pos + n_new))
+        offs.append(offs[-1] + int(bo[i + 1] - bo[i]) + n_new)
+    idx = np.concatenate(parts) if parts else np.zeros(0)
+    return np.asarray(offs, dtype=np.int64), idx.astype(np.int32)
