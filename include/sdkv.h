@@ -77,6 +77,8 @@ extern "C" {
 #define SDKV_OP_SELECT            2
 #define SDKV_OP_SPARSE_DECODE     3
 #define SDKV_OP_DENSE_VERIFY      4
+#define SDKV_OP_COMPACT           5
+#define SDKV_OP_SPECVLM           6
 
 /*
  * Per-head cache budgets.  [SparseMM] methodology: with N heads, total budget
@@ -109,6 +111,9 @@ int sdkv_head_budgets(const float* s, int32_t n_heads, int64_t total_B, int32_t 
  *   op = SDKV_OP_SELECT:        (B, 0, Hkv, 0, n, 0)
  *   op = SDKV_OP_SPARSE_DECODE: (B, Hq, Hkv, d, 0, 0)
  *   op = SDKV_OP_DENSE_VERIFY:  (B, Hq, Hkv, d, n, gamma)   n = n_prefix + gamma
+ *   op = SDKV_OP_COMPACT:       (any)                       status word only
+ *   op = SDKV_OP_SPECVLM:       (B, 0, 0, 0, nV, 0)         nV = v_hi - v_lo
+ * sdkv_sparse_decode_compact uses the SDKV_OP_SPARSE_DECODE size.
  * Queries the current device's SM count.  Returns 0 for an invalid request.
  */
 size_t sdkv_workspace_size(int32_t op, int32_t B, int32_t Hq, int32_t Hkv, int32_t d,
@@ -249,6 +254,104 @@ const char* sdkv_last_error(void);
 
 /* Library ABI version (major * 100 + minor). */
 int32_t sdkv_version(void);
+
+/* ---------------------------------------------------------------------------
+ * Around the hot path: list builders, compaction, SpecVLM selection.
+ * ------------------------------------------------------------------------- */
+
+/*
+ * Sink-plus-recent lists, no scoring.  [StD] baselines ("Streaming": a draft
+ * model with streaming attention); [ByteCross] "The Attention Baseline" (a
+ * sink-plus-recent window timed against dense decoding).  Every (b, h) keeps
+ * rows [0, min(n_sink, n)) and [max(n - n_recent, min(n_sink, n)), n), so each
+ * list has k = min(n, n_sink + n_recent) entries, ascending.
+ *   offsets  device int32[B*Hkv + 1] (written: i * k)
+ *   indices  device int32[B*Hkv*k]   (written)
+ * Asynchronous on `stream`; no workspace.  Feed the lists to
+ * sdkv_sparse_decode_attn unchanged.
+ */
+int sdkv_window_lists(int32_t B, int32_t Hkv, int32_t n, int32_t n_sink, int32_t n_recent,
+                      int32_t* offsets, int32_t* indices, void* stream);
+
+/*
+ * Draft-step lists.  [StD] 3.1: the sparse model proposes gamma tokens one at a
+ * time; draft step t attends the base selection plus the t + 1 positions
+ * drafted so far, whose KV rows it has just appended to the cache.  Each list
+ * of the base CSR followed by n_pos, n_pos + 1, ..., n_pos + n_new - 1:
+ *   offsets[i] = (base_offsets[i] - base_offsets[0]) + i * n_new
+ *   base_*   device CSR of BH lists (every base entry below n_pos keeps the
+ *            new lists ascending)
+ *   offsets  device int32[BH + 1], indices device int32[total + BH * n_new]
+ *            (written; must not alias the base arrays)
+ * Asynchronous on `stream`; no workspace.
+ */
+int sdkv_append_drafts(const int32_t* base_offsets, const int32_t* base_indices, int32_t BH,
+                       int32_t n_pos, int32_t n_new, int32_t* offsets, int32_t* indices,
+                       void* stream);
+
+/*
+ * Contiguous compaction of the selected rows.  [ByteCross] "Speedup Across
+ * Context": after selection the kept entries are gathered into a contiguous
+ * buffer that every later step reads in one kernel call.  Row
+ * offsets[i] - offsets[0] + j of k_out / v_out is row indices[offsets[i] + j]
+ * of KV head (b, h) = (i / Hkv, i % Hkv) of the caches.
+ *   k, v, kv_strides, n_cap, offsets, indices  as for sdkv_sparse_decode_attn
+ *            (entries outside [0, n_cap) set SDKV_DEV_BAD_INDEX and copy row 0)
+ *   rows_cap rows k_out and v_out hold; list rows past it are skipped and set
+ *            SDKV_DEV_BAD_LIST
+ *   k_out, v_out  device bf16 [rows_cap][d] (written), 16-byte aligned
+ *   ws       workspace of at least sdkv_workspace_size(SDKV_OP_COMPACT, ...)
+ * Asynchronous on `stream`.  Reads and writes 4*d bytes per listed row.
+ */
+int sdkv_compact_kv(const void* k, const void* v, const int64_t kv_strides[3], int32_t n_cap,
+                    const int32_t* offsets, const int32_t* indices, int32_t B, int32_t Hkv,
+                    int32_t d, int64_t rows_cap, void* k_out, void* v_out, void* ws,
+                    size_t ws_bytes, void* stream);
+
+/*
+ * Sparse decode over compacted rows: the attention of sdkv_sparse_decode_attn,
+ * where the rows of list i are the contiguous rows [offsets[i] - offsets[0],
+ * offsets[i+1] - offsets[0]) of k_c / v_c (as written by sdkv_compact_kv).
+ * Streamed with tensor copies, no index reads.
+ *   rows_cap rows of k_c / v_c (the tensor maps' extent; rows past it read 0)
+ *   other arguments as for sdkv_sparse_decode_attn; workspace of at least
+ *   sdkv_workspace_size(SDKV_OP_SPARSE_DECODE, ...)
+ */
+int sdkv_sparse_decode_compact(const void* q, const void* k_c, const void* v_c, int64_t rows_cap,
+                               const int32_t* offsets, int32_t B, int32_t Hq, int32_t Hkv,
+                               int32_t d, float scale, void* o, float* lse, void* ws,
+                               size_t ws_bytes, void* stream);
+
+/*
+ * SpecVLM token selection.  [SpecVLM] "The SpecVLM Method": the importance of
+ * token j is the mean of the verifier's attention maps (all layers and heads)
+ *     a_j = (1/units) sum_u scores[b][u][j]        (fp32, units in order)
+ * Stage I keeps the shortest prefix V_R of the video tokens V = [v_lo, v_hi),
+ * ordered by a_j descending (equal a_j: lower j first), whose mass reaches
+ * lam_r times the mass of V (top-P).  Stage II walks the other video tokens in
+ * index order at the interval I = (|V| - |V_R|) / ((1 - r)|V|) and keeps the
+ * ones at positions floor(k I), k = 0, 1, ...  The list is V_R u V_U plus the
+ * always-kept range [keep_lo, keep_hi) (e.g. the text tokens), ascending.
+ * Exact decisions: every mass is a_j rounded to the nearest multiple of 2^-32
+ * and summed as an integer; lam_r * S, I and k * I are float64.
+ *   scores     device float [B][units][n], finite and >= 0 (others count as
+ *              0 and set SDKV_DEV_BAD_LIST)
+ *   lam_r      in [0, 1];  r (pruning ratio) in [0, 1)
+ *   keep range disjoint from V
+ *   importance device float [B][n] (written)
+ *   indices    device int32 [B][(v_hi - v_lo) + (keep_hi - keep_lo)] (written;
+ *              the first counts[b] entries of row b are the list)
+ *   counts     device int32 [B] (written)
+ *   ws         workspace of at least sdkv_workspace_size(SDKV_OP_SPECVLM, B, 0,
+ *              0, 0, v_hi - v_lo, 0)
+ * Asynchronous on `stream`.  One CTA per sequence; up to 16384 video tokens
+ * sort in shared memory, more in the workspace (at most 2^20).
+ */
+int sdkv_specvlm_select(const float* scores, int32_t B, int32_t units, int32_t n,
+                        int32_t v_lo, int32_t v_hi, double lam_r, double r,
+                        int32_t keep_lo, int32_t keep_hi, float* importance,
+                        int32_t* indices, int32_t* counts, void* ws, size_t ws_bytes,
+                        void* stream);
 
 #ifdef __cplusplus
 }

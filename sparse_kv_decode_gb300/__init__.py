@@ -5,7 +5,9 @@ of include/sdkv.h); this package is its thin Python binding plus the byte
 account used to report achieved bandwidth.
 """
 from ._lib import (  # noqa: F401
+    OP_COMPACT,
     OP_DENSE_VERIFY,
+    OP_SPECVLM,
     OP_SCORE,
     OP_SELECT,
     OP_SPARSE_DECODE,
@@ -20,4 +22,9 @@ from ._lib import (  # noqa: F401
     version,
     workspace_size,
     workspace_status,
+    window_lists,
+    append_drafts,
+    compact_kv,
+    sparse_decode_compact,
+    specvlm_select,
 )

@@ -32,6 +32,8 @@ OP_SCORE = 1
 OP_SELECT = 2
 OP_SPARSE_DECODE = 3
 OP_DENSE_VERIFY = 4
+OP_COMPACT = 5
+OP_SPECVLM = 6
 
 _c_i32 = ctypes.c_int32
 _c_i64 = ctypes.c_int64
@@ -83,6 +85,19 @@ def lib() -> ctypes.CDLL:
     L.sdkv_dense_verify_attn_noalloc.restype = ctypes.c_int
     L.sdkv_workspace_status.argtypes = [_c_vp, ctypes.POINTER(_c_i32), _c_vp]
     L.sdkv_workspace_status.restype = ctypes.c_int
+    L.sdkv_window_lists.argtypes = [_c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_vp, _c_vp, _c_vp]
+    L.sdkv_window_lists.restype = ctypes.c_int
+    L.sdkv_append_drafts.argtypes = [_c_vp, _c_vp, _c_i32, _c_i32, _c_i32, _c_vp, _c_vp, _c_vp]
+    L.sdkv_append_drafts.restype = ctypes.c_int
+    L.sdkv_compact_kv.argtypes = [_c_vp, _c_vp, _I64x3, _c_i32, _c_vp, _c_vp, _c_i32, _c_i32, _c_i32, _c_i64,
+                                  _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]
+    L.sdkv_compact_kv.restype = ctypes.c_int
+    L.sdkv_sparse_decode_compact.argtypes = [_c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_i32, _c_i32, _c_i32, _c_i32,
+                                             _c_f, _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]
+    L.sdkv_sparse_decode_compact.restype = ctypes.c_int
+    L.sdkv_specvlm_select.argtypes = [_c_vp, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, ctypes.c_double,
+                                      ctypes.c_double, _c_i32, _c_i32, _c_vp, _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]
+    L.sdkv_specvlm_select.restype = ctypes.c_int
     _lib = L
     return L
 
@@ -254,3 +269,106 @@ def dense_verify_attn_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                                                 Hkv, d, n_prefix, gamma, scale, o.data_ptr(), _ptr(lse),
                                                 _stream(q)))
     return o, lse
+
+
+# --------------------------------------------------------------------------- around the hot path
+
+def window_lists(B: int, Hkv: int, n: int, n_sink: int, n_recent: int, device,
+                 offsets: torch.Tensor | None = None, indices: torch.Tensor | None = None):
+    """sdkv_window_lists: sink-plus-recent lists, k = min(n, n_sink + n_recent) per head."""
+    k = min(n, n_sink + n_recent)
+    if offsets is None:
+        offsets = torch.empty(B * Hkv + 1, dtype=torch.int32, device=device)
+    if indices is None:
+        indices = torch.empty(max(B * Hkv * k, 1), dtype=torch.int32, device=device)
+    _need(offsets, "offsets", torch.int32)
+    _need(indices, "indices", torch.int32)
+    _check(lib().sdkv_window_lists(B, Hkv, n, n_sink, n_recent, offsets.data_ptr(), indices.data_ptr(),
+                                   _stream(offsets)))
+    return offsets, indices
+
+
+def append_drafts(base_offsets: torch.Tensor, base_indices: torch.Tensor, total: int, n_pos: int, n_new: int,
+                  offsets: torch.Tensor | None = None, indices: torch.Tensor | None = None):
+    """sdkv_append_drafts: every base list followed by n_pos .. n_pos + n_new - 1.
+    `total` = base_offsets[-1] - base_offsets[0] (host value, sizes the output)."""
+    _need(base_offsets, "base_offsets", torch.int32)
+    _need(base_indices, "base_indices", torch.int32)
+    BH = base_offsets.numel() - 1
+    if offsets is None:
+        offsets = torch.empty(BH + 1, dtype=torch.int32, device=base_offsets.device)
+    if indices is None:
+        indices = torch.empty(max(total + BH * n_new, 1), dtype=torch.int32, device=base_offsets.device)
+    _check(lib().sdkv_append_drafts(base_offsets.data_ptr(), base_indices.data_ptr(), BH, n_pos, n_new,
+                                    offsets.data_ptr(), indices.data_ptr(), _stream(base_offsets)))
+    return offsets, indices
+
+
+def compact_kv(k: torch.Tensor, v: torch.Tensor, offsets: torch.Tensor, indices: torch.Tensor, total: int,
+               k_out: torch.Tensor | None = None, v_out: torch.Tensor | None = None,
+               ws: torch.Tensor | None = None):
+    """sdkv_compact_kv: the listed rows of every head into contiguous [total][d] buffers."""
+    for t, nm in ((k, "k"), (v, "v")):
+        _need(t, nm, torch.bfloat16)
+    _need(offsets, "offsets", torch.int32)
+    _need(indices, "indices", torch.int32)
+    if k.stride() != v.stride() or k.shape != v.shape:
+        raise ValueError("K and V must share shape and strides")
+    B, Hkv, n_cap, d = k.shape
+    if k_out is None:
+        k_out = torch.empty((max(total, 1), d), dtype=torch.bfloat16, device=k.device)
+    if v_out is None:
+        v_out = torch.empty((max(total, 1), d), dtype=torch.bfloat16, device=k.device)
+    if ws is None:
+        ws = new_workspace(workspace_size(OP_COMPACT, B, 0, Hkv, d, 0, 0), k.device)
+    _check(lib().sdkv_compact_kv(k.data_ptr(), v.data_ptr(), _kv_strides(k), n_cap, offsets.data_ptr(),
+                                 indices.data_ptr(), B, Hkv, d, k_out.shape[0], k_out.data_ptr(), v_out.data_ptr(),
+                                 ws.data_ptr(), ws.numel(), _stream(k)))
+    return k_out, v_out
+
+
+def sparse_decode_compact(q: torch.Tensor, k_c: torch.Tensor, v_c: torch.Tensor, offsets: torch.Tensor,
+                          Hkv: int, scale: float, o: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                          ws: torch.Tensor | None = None, want_lse: bool = True):
+    """sdkv_sparse_decode_compact: decode over rows compacted by compact_kv."""
+    for t, nm in ((q, "q"), (k_c, "k_c"), (v_c, "v_c")):
+        _need(t, nm, torch.bfloat16)
+    _need(offsets, "offsets", torch.int32)
+    if not (q.is_contiguous() and k_c.is_contiguous() and v_c.is_contiguous()):
+        raise ValueError("q, k_c and v_c must be contiguous")
+    B, Hq, d = q.shape
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = new_workspace(workspace_size(OP_SPARSE_DECODE, B, Hq, Hkv, d, 0, 0), q.device)
+    _check(lib().sdkv_sparse_decode_compact(q.data_ptr(), k_c.data_ptr(), v_c.data_ptr(), k_c.shape[0],
+                                            offsets.data_ptr(), B, Hq, Hkv, d, scale, o.data_ptr(), _ptr(lse),
+                                            ws.data_ptr(), ws.numel(), _stream(q)))
+    return o, lse
+
+
+def specvlm_select(scores: torch.Tensor, v_lo: int, v_hi: int, lam_r: float, r: float, keep_lo: int,
+                   keep_hi: int, importance: torch.Tensor | None = None, indices: torch.Tensor | None = None,
+                   counts: torch.Tensor | None = None, ws: torch.Tensor | None = None):
+    """sdkv_specvlm_select: scores [B][units][n] fp32 -> (importance [B][n],
+    indices [B][cap], counts [B]); row b's list is indices[b, :counts[b]]."""
+    _need(scores, "scores", torch.float32)
+    if not scores.is_contiguous():
+        raise ValueError("scores must be contiguous [B][units][n]")
+    B, units, n = scores.shape
+    cap = (v_hi - v_lo) + (keep_hi - keep_lo)
+    dev = scores.device
+    if importance is None:
+        importance = torch.empty((B, n), dtype=torch.float32, device=dev)
+    if indices is None:
+        indices = torch.empty((B, max(cap, 1)), dtype=torch.int32, device=dev)
+    if counts is None:
+        counts = torch.empty(B, dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = new_workspace(workspace_size(OP_SPECVLM, B, 0, 0, 0, v_hi - v_lo, 0), dev)
+    _check(lib().sdkv_specvlm_select(scores.data_ptr(), B, units, n, v_lo, v_hi, lam_r, r, keep_lo, keep_hi,
+                                     importance.data_ptr(), indices.data_ptr(), counts.data_ptr(), ws.data_ptr(),
+                                     ws.numel(), _stream(scores)))
+    return importance, indices, counts

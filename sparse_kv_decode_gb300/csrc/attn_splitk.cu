@@ -48,17 +48,21 @@ struct AttnParams {
     float* part_ml;
 };
 
-template <int D, int MT, int KW, int TK, int STAGES, bool SPARSE>
+// Kinds of rows a launch streams: the whole cache (dense verify), rows gathered
+// through the index lists, or the lists' rows compacted into contiguous buffers.
+constexpr int kDense = 0, kGather = 1, kContig = 2;
+
+template <int D, int MT, int KW, int TK, int STAGES, int KIND>
 struct AttnCfg {
     static constexpr int NCW = MT * KW;          // consumer warps: row tiles x key groups
     static constexpr int NCT = NCW * 32;
-    static constexpr int NPW = SPARSE ? 2 : 1;   // producer warps (gathering rows needs more issuers)
+    static constexpr int NPW = (KIND == kGather) ? 2 : 1;   // producer warps (gathering rows needs more issuers)
     static constexpr int NT = NCT + NPW * 32;
     static constexpr int KPW = TK / KW;          // keys per consumer warp per stage
     static_assert(KPW % 16 == 0, "keys per warp must be a multiple of 16");
     static_assert(D % (4 * KW) == 0, "each key group reduces a slice of the head dims");
     static_assert(D == 64 || D == 128, "head dim");
-    static_assert(!SPARSE || TK == 32 * NPW, "one list entry per producer lane per tile");
+    static_assert(KIND != kGather || TK == 32 * NPW, "one list entry per producer lane per tile");
     static constexpr int ROWB = 2 * D;
     static constexpr int TILE_B = TK * ROWB;
     static constexpr int QPITCH = 2 * D + 16;
@@ -113,11 +117,12 @@ __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int row, int chunk)
     return sw128_addr<TK>(base, row, chunk);
 }
 
-template <int D, int MT, int KW, int TK, int STAGES, bool SPARSE>
-__global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
+template <int D, int MT, int KW, int TK, int STAGES, int KIND>
+__global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, KIND>::NT)
     attn_splitk_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv) {
-    using C = AttnCfg<D, MT, KW, TK, STAGES, SPARSE>;
+    using C = AttnCfg<D, MT, KW, TK, STAGES, KIND>;
+    constexpr bool SPARSE = (KIND != kDense);    // list-driven chunk plan, no causal limits
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem =
         reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -130,6 +135,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
     __shared__ int s_work[6];
     __shared__ int s_scan[C::NT / 32];
     __shared__ int s_tot;
+    __shared__ int s_off0;           // offsets[0]: row 0 of the compacted buffers
     __shared__ int s_abort;
     __shared__ int s_last;
 
@@ -158,7 +164,8 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
             kh = p.offsets[tid + 1] - start;
         }
         if (tid == 0) {
-            s_tot = p.offsets[p.BH] - p.offsets[0];
+            s_off0 = p.offsets[0];
+            s_tot = p.offsets[p.BH] - s_off0;
             s_work[0] = -1;
         }
         __syncthreads();
@@ -209,7 +216,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
     if (tid == 0) {
 #pragma unroll
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar_full + 8 * s, SPARSE ? C::NPW * 32 : 1);
+            mbar_init(bar_full + 8 * s, KIND == kGather ? C::NPW * 32 : 1);
             mbar_init(bar_empty + 8 * s, C::NCW);
         }
         fence_mbar_init();
@@ -228,7 +235,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
 
     // ------------------------------------------------------------------ producer
     if (warp >= C::NCW) {
-        if constexpr (SPARSE) {
+        if constexpr (KIND == kGather) {
             // Gather: the NPW producer warps own 32 tile rows each; lane j of a warp
             // holds the list entry of its warp's row j (loaded one tile ahead), and
             // CPR lanes copy one row as CPR 16-byte chunks per instruction.
@@ -279,9 +286,12 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
             }
             cp_async_wait_all();
         } else {
+            // TMA producer: dense tiles of the cache (4-D map: dims, row, head,
+            // sequence) or tiles of the compacted rows (2-D map: dims, row)
             if (lane == 0) {
                 prefetch_tmap(&tmk);
                 prefetch_tmap(&tmv);
+                const int crow0 = (KIND == kContig) ? lo - s_off0 : 0;   // compacted buffers: the chunk's first row
                 for (int t = 0; t < ntiles; ++t) {
                     const int s = t % STAGES;
                     const uint32_t ph = (t / STAGES) & 1;
@@ -294,10 +304,15 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, SPARSE>::NT)
                     const int row0 = lo + t * TK;
 #pragma unroll
                     for (int half = 0; half < D / 64; ++half) {
-                        tma_load_4d(sbase + C::OFF_K + s * C::TILE_B + half * TK * 128, &tmk, half * 64, row0,
-                                    h, b, bar_full + 8 * s);
-                        tma_load_4d(sbase + C::OFF_V + s * C::TILE_B + half * TK * 128, &tmv, half * 64, row0,
-                                    h, b, bar_full + 8 * s);
+                        const uint32_t kdst = sbase + C::OFF_K + s * C::TILE_B + half * TK * 128;
+                        const uint32_t vdst = sbase + C::OFF_V + s * C::TILE_B + half * TK * 128;
+                        if constexpr (KIND == kContig) {
+                            tma_load_2d(kdst, &tmk, half * 64, crow0 + t * TK, bar_full + 8 * s);
+                            tma_load_2d(vdst, &tmv, half * 64, crow0 + t * TK, bar_full + 8 * s);
+                        } else {
+                            tma_load_4d(kdst, &tmk, half * 64, row0, h, b, bar_full + 8 * s);
+                            tma_load_4d(vdst, &tmv, half * 64, row0, h, b, bar_full + 8 * s);
+                        }
                     }
                 }
             }
@@ -818,11 +833,11 @@ int sparse_cluster(int BH, int grid_target) {
 }
 int sparse_max_chunks(int BH, int grid_target, int cs) { return cs > 1 ? grid_target : grid_target + BH; }
 
-template <int D, int MT, int KW, int TK, int STAGES, bool SPARSE>
+template <int D, int MT, int KW, int TK, int STAGES, int KIND>
 cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv, int grid,
                         cudaStream_t st, int cluster = 1) {
-    using C = AttnCfg<D, MT, KW, TK, STAGES, SPARSE>;
-    auto kern = attn_splitk_kernel<D, MT, KW, TK, STAGES, SPARSE>;
+    using C = AttnCfg<D, MT, KW, TK, STAGES, KIND>;
+    auto kern = attn_splitk_kernel<D, MT, KW, TK, STAGES, KIND>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -912,18 +927,18 @@ int launch_dense_verify(const AttnLaunch& a, const CUtensorMap* tmk, const CUten
     cudaError_t e = cudaErrorInvalidValue;
     if (a.d == 128) {
         switch (MT) {
-            case 1: e = launch_attn<128, 1, 4, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream, pl.cs); break;
-            case 2: e = launch_attn<128, 2, 2, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream, pl.cs); break;
-            case 3: e = launch_attn<128, 3, 2, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream, pl.cs); break;
-            case 4: e = launch_attn<128, 4, 2, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream, pl.cs); break;
+            case 1: e = launch_attn<128, 1, 4, kDenseTK, kDenseStages, kDense>(p, *tmk, *tmv, grid, a.stream, pl.cs); break;
+            case 2: e = launch_attn<128, 2, 2, kDenseTK, kDenseStages, kDense>(p, *tmk, *tmv, grid, a.stream, pl.cs); break;
+            case 3: e = launch_attn<128, 3, 2, kDenseTK, kDenseStages, kDense>(p, *tmk, *tmv, grid, a.stream, pl.cs); break;
+            case 4: e = launch_attn<128, 4, 2, kDenseTK, kDenseStages, kDense>(p, *tmk, *tmv, grid, a.stream, pl.cs); break;
             default: *why = "(Hq/Hkv) * gamma must be <= 64"; return SDKV_ERR_UNSUPPORTED;
         }
     } else {
         switch (MT) {
-            case 1: e = launch_attn<64, 1, 4, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream, pl.cs); break;
-            case 2: e = launch_attn<64, 2, 2, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream, pl.cs); break;
-            case 3: e = launch_attn<64, 3, 2, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream, pl.cs); break;
-            case 4: e = launch_attn<64, 4, 2, kDenseTK, kDenseStages, false>(p, *tmk, *tmv, grid, a.stream, pl.cs); break;
+            case 1: e = launch_attn<64, 1, 4, kDenseTK, kDenseStages, kDense>(p, *tmk, *tmv, grid, a.stream, pl.cs); break;
+            case 2: e = launch_attn<64, 2, 2, kDenseTK, kDenseStages, kDense>(p, *tmk, *tmv, grid, a.stream, pl.cs); break;
+            case 3: e = launch_attn<64, 3, 2, kDenseTK, kDenseStages, kDense>(p, *tmk, *tmv, grid, a.stream, pl.cs); break;
+            case 4: e = launch_attn<64, 4, 2, kDenseTK, kDenseStages, kDense>(p, *tmk, *tmv, grid, a.stream, pl.cs); break;
             default: *why = "(Hq/Hkv) * gamma must be <= 64"; return SDKV_ERR_UNSUPPORTED;
         }
     }
@@ -934,7 +949,13 @@ int launch_dense_verify(const AttnLaunch& a, const CUtensorMap* tmk, const CUten
     return SDKV_OK;
 }
 
-int launch_sparse_decode(const AttnLaunch& a, int num_sms, const char** why) {
+namespace {
+
+// Sparse decode over index lists (KIND = kGather: rows gathered from the caches)
+// or over the lists' rows compacted into contiguous buffers (KIND = kContig).
+template <int KIND>
+int launch_list_decode(const AttnLaunch& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int num_sms,
+                       const char** why) {
     AttnParams p = make_params(a);
     const int BH = a.B * a.Hkv;
     p.offsets = a.offsets;
@@ -955,20 +976,18 @@ int launch_sparse_decode(const AttnLaunch& a, int num_sms, const char** why) {
     p.tickets = L.tickets;
     p.part_o = L.part_o;
     p.part_ml = L.part_ml;
-    CUtensorMap dummy;
-    memset(&dummy, 0, sizeof(dummy));
     const int MT = (p.R + 15) / 16;
     cudaError_t e = cudaErrorInvalidValue;
     if (a.d == 128) {
         switch (MT) {
-            case 1: e = launch_attn<128, 1, 4, kSparseTK, kSparseStages, true>(p, dummy, dummy, max_chunks, a.stream, p.cs); break;
-            case 2: e = launch_attn<128, 2, 2, kSparseTK, kSparseStages, true>(p, dummy, dummy, max_chunks, a.stream, p.cs); break;
+            case 1: e = launch_attn<128, 1, 4, kSparseTK, kSparseStages, KIND>(p, tmk, tmv, max_chunks, a.stream, p.cs); break;
+            case 2: e = launch_attn<128, 2, 2, kSparseTK, kSparseStages, KIND>(p, tmk, tmv, max_chunks, a.stream, p.cs); break;
             default: *why = "Hq/Hkv must be <= 32"; return SDKV_ERR_UNSUPPORTED;
         }
     } else {
         switch (MT) {
-            case 1: e = launch_attn<64, 1, 4, kSparseTK, kSparseStages, true>(p, dummy, dummy, max_chunks, a.stream, p.cs); break;
-            case 2: e = launch_attn<64, 2, 2, kSparseTK, kSparseStages, true>(p, dummy, dummy, max_chunks, a.stream, p.cs); break;
+            case 1: e = launch_attn<64, 1, 4, kSparseTK, kSparseStages, KIND>(p, tmk, tmv, max_chunks, a.stream, p.cs); break;
+            case 2: e = launch_attn<64, 2, 2, kSparseTK, kSparseStages, KIND>(p, tmk, tmv, max_chunks, a.stream, p.cs); break;
             default: *why = "Hq/Hkv must be <= 32"; return SDKV_ERR_UNSUPPORTED;
         }
     }
@@ -977,6 +996,19 @@ int launch_sparse_decode(const AttnLaunch& a, int num_sms, const char** why) {
         return SDKV_ERR_CUDA;
     }
     return SDKV_OK;
+}
+
+}  // namespace
+
+int launch_sparse_decode(const AttnLaunch& a, int num_sms, const char** why) {
+    CUtensorMap dummy;
+    memset(&dummy, 0, sizeof(dummy));
+    return launch_list_decode<kGather>(a, dummy, dummy, num_sms, why);
+}
+
+int launch_sparse_decode_compact(const AttnLaunch& a, const CUtensorMap* tmk, const CUtensorMap* tmv, int num_sms,
+                                 const char** why) {
+    return launch_list_decode<kContig>(a, *tmk, *tmv, num_sms, why);
 }
 
 // -------------------------------------------------------------------------------------

@@ -229,6 +229,11 @@ size_t sdkv_workspace_size(int32_t op, int32_t B, int32_t Hq, int32_t Hkv, int32
         case SDKV_OP_DENSE_VERIFY:
             if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv || n <= 0 || gamma_or_W <= 0 || n < gamma_or_W) return 0;
             return dense_ws_bytes(B, Hq, Hkv, d, n, gamma_or_W, dev.num_sms);
+        case SDKV_OP_COMPACT:
+            return SDKV_WS_HEADER_BYTES;
+        case SDKV_OP_SPECVLM:
+            if (B <= 0 || n < 0 || n > (1 << 20)) return 0;
+            return specvlm_ws_bytes(B, n);
         default:
             return 0;
     }
@@ -422,6 +427,127 @@ int sdkv_workspace_status(void* ws, int32_t* status, void* stream) {
     if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, sizeof(int32_t), st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return fail(SDKV_ERR_CUDA, cudaGetErrorString(e));
+    g_last_error.clear();
+    return SDKV_OK;
+}
+
+
+// ----------------------------------------------------------------------------------------
+// next rows
+// ----------------------------------------------------------------------------------------
+int sdkv_window_lists(int32_t B, int32_t Hkv, int32_t n, int32_t n_sink, int32_t n_recent, int32_t* offsets,
+                      int32_t* indices, void* stream) {
+    if (!offsets || !indices) return fail(SDKV_ERR_INVALID_ARG, "null pointer");
+    if (B <= 0 || Hkv <= 0 || n < 0 || n_sink < 0 || n_recent < 0)
+        return fail(SDKV_ERR_INVALID_ARG, "need B, Hkv > 0 and n, n_sink, n_recent >= 0");
+    const int64_t k = std::min<int64_t>(n, static_cast<int64_t>(n_sink) + n_recent);
+    if (static_cast<int64_t>(B) * Hkv * k > 0x7fffffff) return fail(SDKV_ERR_INVALID_ARG, "lists too long");
+    const char* why = "";
+    const int rc = launch_window_lists(B, Hkv, n, n_sink, n_recent, offsets, indices,
+                                       static_cast<cudaStream_t>(stream), &why);
+    if (rc) return fail(rc, why);
+    g_last_error.clear();
+    return SDKV_OK;
+}
+
+int sdkv_append_drafts(const int32_t* base_offsets, const int32_t* base_indices, int32_t BH, int32_t n_pos,
+                       int32_t n_new, int32_t* offsets, int32_t* indices, void* stream) {
+    if (!base_offsets || !base_indices || !offsets || !indices) return fail(SDKV_ERR_INVALID_ARG, "null pointer");
+    if (BH <= 0 || n_pos < 0 || n_new < 0) return fail(SDKV_ERR_INVALID_ARG, "need BH > 0 and n_pos, n_new >= 0");
+    if (offsets == base_offsets || indices == base_indices)
+        return fail(SDKV_ERR_INVALID_ARG, "output lists must not alias the base lists");
+    const char* why = "";
+    const int rc = launch_append_drafts(base_offsets, base_indices, BH, n_pos, n_new, offsets, indices,
+                                        static_cast<cudaStream_t>(stream), &why);
+    if (rc) return fail(rc, why);
+    g_last_error.clear();
+    return SDKV_OK;
+}
+
+int sdkv_compact_kv(const void* k, const void* v, const int64_t kv_strides[3], int32_t n_cap,
+                    const int32_t* offsets, const int32_t* indices, int32_t B, int32_t Hkv, int32_t d,
+                    int64_t rows_cap, void* k_out, void* v_out, void* ws, size_t ws_bytes, void* stream) {
+    if (B <= 0 || Hkv <= 0) return fail(SDKV_ERR_INVALID_ARG, "B and Hkv must be positive");
+    if (d != 64 && d != 128) return fail(SDKV_ERR_UNSUPPORTED, "head dim must be 64 or 128");
+    if (!offsets || !indices || !k_out || !v_out) return fail(SDKV_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(k_out) || !aligned16(v_out)) return fail(SDKV_ERR_INVALID_ARG, "k_out/v_out not 16-byte aligned");
+    int rc = check_kv(k, v, kv_strides, d);
+    if (rc) return rc;
+    if (n_cap <= 0 || rows_cap < 0) return fail(SDKV_ERR_INVALID_ARG, "need n_cap > 0 and rows_cap >= 0");
+    if ((rc = check_ws(ws, ws_bytes, SDKV_WS_HEADER_BYTES))) return rc;
+    CompactLaunch a{k, v, kv_strides[0], kv_strides[1], kv_strides[2], n_cap, B, Hkv, d, offsets, indices,
+                    rows_cap, k_out, v_out, ws, static_cast<cudaStream_t>(stream)};
+    const char* why = "";
+    rc = launch_compact_kv(a, &why);
+    if (rc) return fail(rc, why);
+    g_last_error.clear();
+    return SDKV_OK;
+}
+
+int sdkv_sparse_decode_compact(const void* q, const void* k_c, const void* v_c, int64_t rows_cap,
+                               const int32_t* offsets, int32_t B, int32_t Hq, int32_t Hkv, int32_t d, float scale,
+                               void* o, float* lse, void* ws, size_t ws_bytes, void* stream) {
+    int rc = check_heads(B, Hq, Hkv, d);
+    if (rc) return rc;
+    if (!q || !o || !offsets || !k_c || !v_c) return fail(SDKV_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(q) || !aligned16(o) || !aligned16(k_c) || !aligned16(v_c))
+        return fail(SDKV_ERR_INVALID_ARG, "q/o/k_c/v_c not 16-byte aligned");
+    if (rows_cap <= 0 || rows_cap > 0x7fffffff) return fail(SDKV_ERR_INVALID_ARG, "rows_cap must be in [1, 2^31)");
+    if (Hq / Hkv > 32) return fail(SDKV_ERR_UNSUPPORTED, "Hq/Hkv must be <= 32");
+    if (static_cast<int64_t>(B) * Hkv > 65536) return fail(SDKV_ERR_UNSUPPORTED, "B*Hkv must be <= 65536");
+    if (!std::isfinite(scale)) return fail(SDKV_ERR_INVALID_ARG, "scale must be finite");
+    const DeviceInfo dev = current_device();
+    if (dev.num_sms <= 0) return fail(SDKV_ERR_CUDA, "no CUDA device");
+    if ((rc = check_ws(ws, ws_bytes, sparse_ws_bytes(B, Hq, Hkv, d, dev.num_sms)))) return rc;
+    CUtensorMap tmk, tmv;
+    if ((rc = encode_rows_tmap(&tmk, k_c, rows_cap, d, 64))) return rc;
+    if ((rc = encode_rows_tmap(&tmv, v_c, rows_cap, d, 64))) return rc;
+    AttnLaunch a{};
+    a.q = q;
+    a.k = k_c;
+    a.v = v_c;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.d = d;
+    a.gamma = 1;
+    a.o = o;
+    a.lse = lse;
+    a.scale = scale;
+    a.offsets = offsets;
+    a.indices = nullptr;
+    a.n_cap = static_cast<int>(rows_cap);
+    a.ws = ws;
+    a.ws_bytes = ws_bytes;
+    a.stream = static_cast<cudaStream_t>(stream);
+    const char* why = "";
+    rc = launch_sparse_decode_compact(a, &tmk, &tmv, dev.num_sms, &why);
+    if (rc) return fail(rc, why);
+    g_last_error.clear();
+    return SDKV_OK;
+}
+
+int sdkv_specvlm_select(const float* scores, int32_t B, int32_t units, int32_t n, int32_t v_lo, int32_t v_hi,
+                        double lam_r, double r, int32_t keep_lo, int32_t keep_hi, float* importance,
+                        int32_t* indices, int32_t* counts, void* ws, size_t ws_bytes, void* stream) {
+    if (!scores || !importance || !indices || !counts) return fail(SDKV_ERR_INVALID_ARG, "null pointer");
+    if (B <= 0 || units <= 0 || n <= 0) return fail(SDKV_ERR_INVALID_ARG, "B, units, n must be positive");
+    if (!(0 <= v_lo && v_lo <= v_hi && v_hi <= n)) return fail(SDKV_ERR_INVALID_ARG, "need 0 <= v_lo <= v_hi <= n");
+    if (!(0 <= keep_lo && keep_lo <= keep_hi && keep_hi <= n))
+        return fail(SDKV_ERR_INVALID_ARG, "need 0 <= keep_lo <= keep_hi <= n");
+    if (keep_lo < keep_hi && v_lo < v_hi && !(keep_hi <= v_lo || keep_lo >= v_hi))
+        return fail(SDKV_ERR_INVALID_ARG, "the kept range must not overlap the video tokens");
+    if (!(lam_r >= 0.0 && lam_r <= 1.0)) return fail(SDKV_ERR_INVALID_ARG, "lam_r must be in [0, 1]");
+    if (!(r >= 0.0 && r < 1.0)) return fail(SDKV_ERR_INVALID_ARG, "r must be in [0, 1)");
+    if (v_hi - v_lo > (1 << 20)) return fail(SDKV_ERR_UNSUPPORTED, "at most 2^20 video tokens");
+    if (static_cast<int64_t>(B) * units * n > (int64_t(1) << 40)) return fail(SDKV_ERR_INVALID_ARG, "scores too large");
+    int rc = check_ws(ws, ws_bytes, specvlm_ws_bytes(B, v_hi - v_lo));
+    if (rc) return rc;
+    SpecLaunch a{scores, B, units, n, v_lo, v_hi, keep_lo, keep_hi, lam_r, r, importance, indices, counts, ws,
+                 static_cast<cudaStream_t>(stream)};
+    const char* why = "";
+    rc = launch_specvlm(a, &why);
+    if (rc) return fail(rc, why);
     g_last_error.clear();
     return SDKV_OK;
 }

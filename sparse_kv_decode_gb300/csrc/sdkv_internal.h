@@ -45,6 +45,9 @@ size_t sparse_ws_bytes(int B, int Hq, int Hkv, int d, int num_sms);
 int launch_dense_verify(const AttnLaunch& a, const CUtensorMap* tmk, const CUtensorMap* tmv,
                         int num_sms, const char** why);
 int launch_sparse_decode(const AttnLaunch& a, int num_sms, const char** why);
+// decode over the lists' rows compacted into contiguous [rows][d] buffers (2-D tensor maps)
+int launch_sparse_decode_compact(const AttnLaunch& a, const CUtensorMap* tmk, const CUtensorMap* tmv, int num_sms,
+                                 const char** why);
 // dense verify with its scratch in the library's fixed device array (no allocation)
 int dense_verify_noalloc(const AttnLaunch& a, const CUtensorMap* tmk, const CUtensorMap* tmv, int num_sms,
                          const char** why);
@@ -76,5 +79,37 @@ struct SelectLaunch {
 };
 size_t select_ws_bytes(int B, int Hkv, int n);
 int launch_select(const SelectLaunch& a, const char** why);
+
+// ---- next rows (next_rows.cu) ------------------------------------------------------
+int launch_window_lists(int B, int Hkv, int n, int n_sink, int n_recent, int* offsets, int* indices,
+                        cudaStream_t st, const char** why);
+int launch_append_drafts(const int* base_offsets, const int* base_indices, int BH, int n_pos, int n_new,
+                         int* offsets, int* indices, cudaStream_t st, const char** why);
+struct CompactLaunch {
+    const void* k;
+    const void* v;
+    int64_t sb, sh, sn;
+    int n_cap, B, Hkv, d;
+    const int32_t* offsets;
+    const int32_t* indices;
+    long long rows_cap;
+    void* k_out;
+    void* v_out;
+    void* ws;
+    cudaStream_t stream;
+};
+int launch_compact_kv(const CompactLaunch& a, const char** why);
+struct SpecLaunch {
+    const float* scores;
+    int B, units, n, v_lo, v_hi, keep_lo, keep_hi;
+    double lam_r, r;
+    float* importance;
+    int32_t* indices;
+    int32_t* counts;
+    void* ws;
+    cudaStream_t stream;
+};
+size_t specvlm_ws_bytes(int B, int nV);
+int launch_specvlm(const SpecLaunch& a, const char** why);
 
 }  // namespace sdkv
