@@ -56,6 +56,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (small profiling cases only; reported in config)")
+    ap.add_argument("--no-next", action="store_true", help="skip the timings of the next rows (f1..f4)")
     return ap.parse_args()
 
 
@@ -423,6 +424,127 @@ def run_e2e(path, K, world):
             "steps": K}
 
 
+def time_graph_us(fn, reps: int = 10, flush: torch.Tensor | None = None) -> float:
+    """Median device time (µs) of one CUDA-graph replay of `fn`'s launches,
+    with an L2 flush (a write larger than L2) before every replay."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    ts = []
+    for r in range(reps + 3):
+        if flush is not None:
+            flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        if r >= 3:
+            ts.append(a.elapsed_time(b) * 1e3)
+    return float(np.median(ts))
+
+
+def next_rows_timings(path, hbm_peak, dev):
+    """Timings of the rows beyond the hot path (each a separate measurement,
+    outside the step):
+      f1  compaction of the selected rows (once per selection) and the decode
+          over the compacted rows, on this workload's lists, every layer;
+      f2  decode over sink + recent lists (4 + 64), every layer;
+      f3  SpecVLM selection for one request of the video workload (28 layers x
+          4 KV heads of window scores over 12,800 tokens, 12,544 of them video);
+      f4  one StD round of the video workload per layer: 5 draft steps (list
+          append on the device + sparse decode over the 1,024 kept + drafted
+          rows) and the verify of the 5 drafts, in one graph."""
+    sk = path.sk
+    L, B, Hq, Hkv, d, n = path.L, path.B, path.Hq, path.Hkv, path.d, path.n
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    out = {}
+    # f1
+    kc, vc = [], []
+    for l, lay in enumerate(path.layers):
+        tot = path.totals[l]
+        kc.append(torch.empty((max(tot, 1), d), dtype=torch.bfloat16, device=dev))
+        vc.append(torch.empty((max(tot, 1), d), dtype=torch.bfloat16, device=dev))
+    ws_c = sk.new_workspace(sk.workspace_size(sk.OP_COMPACT, B, 0, Hkv, d, 0, 0), dev)
+
+    def compact():
+        for l, lay in enumerate(path.layers):
+            sk.compact_kv(lay["k"], lay["v"], path.offs_dev[l], path.idx[l], path.totals[l], k_out=kc[l],
+                          v_out=vc[l], ws=ws_c)
+
+    def contig():
+        for l, lay in enumerate(path.layers):
+            sk.sparse_decode_compact(lay["q"], kc[l], vc[l], path.offs_dev[l], Hkv, path.scale, o=path.o_sp[l],
+                                     lse=path.l_sp[l], ws=path.ws_sp)
+    t_comp = time_graph_us(compact, flush=flush) / L
+    t_contig = time_graph_us(contig, flush=flush) / L
+    mean_total = float(np.mean(path.totals))
+    b_comp = 2 * mean_total * 4 * d                                  # read and write K and V rows
+    b_contig = mean_total * 4 * d + B * Hq * 4 * d                   # K/V rows + q in / o out
+    out["f1_compaction"] = {"us_per_layer": t_comp, "alg_bytes_per_layer": b_comp,
+                            "gbs": b_comp / t_comp / 1e3, "frac_of_measured_hbm": b_comp / t_comp / 1e3 / hbm_peak}
+    out["f1_contiguous_decode"] = {"us_per_layer": t_contig, "alg_bytes_per_layer": b_contig,
+                                   "gbs": b_contig / t_contig / 1e3,
+                                   "frac_of_measured_hbm": b_contig / t_contig / 1e3 / hbm_peak}
+    assert sk.workspace_status(ws_c) == 0 and sk.workspace_status(path.ws_sp) == 0
+    del kc, vc
+    # f2
+    w_offs, w_idx = sk.window_lists(B, Hkv, n, 4, 64, dev)
+
+    def window():
+        for l, lay in enumerate(path.layers):
+            sk.sparse_decode_attn(lay["q"], lay["k"], lay["v"], w_offs, w_idx, path.scale, o=path.o_sp[l],
+                                  lse=path.l_sp[l], ws=path.ws_sp)
+    t_win = time_graph_us(window, flush=flush) / L
+    b_win = B * Hkv * 68 * (4 * d + 4) + B * Hq * 4 * d
+    out["f2_window_decode"] = {"us_per_layer": t_win, "alg_bytes_per_layer": b_win, "lists": "4 sinks + 64 recent"}
+    # f3 and f4 on the video workload
+    vw = workloads.by_name("video")
+    g = torch.Generator(device=dev).manual_seed(7)
+    units = vw.layers * vw.hkv
+    scores = torch.rand((1, units, vw.n), generator=g, device=dev) ** 4
+    v_hi = vw.frames * vw.frame_tokens
+    ws_s = sk.new_workspace(sk.workspace_size(sk.OP_SPECVLM, 1, 0, 0, 0, v_hi, 0), dev)
+    imp = torch.empty((1, vw.n), dtype=torch.float32, device=dev)
+    sidx = torch.empty((1, vw.n), dtype=torch.int32, device=dev)
+    cnt = torch.empty(1, dtype=torch.int32, device=dev)
+
+    def spec():
+        sk.specvlm_select(scores, 0, v_hi, 0.5, 0.9, v_hi, vw.n, importance=imp, indices=sidx, counts=cnt, ws=ws_s)
+    t_spec = time_graph_us(spec, flush=flush)
+    out["f3_specvlm_select"] = {"us_per_request": t_spec, "units": units, "tokens": vw.n, "video_tokens": v_hi,
+                                "lam_r": 0.5, "r": 0.9, "kept": int(cnt.item())}
+    gam = vw.gamma
+    lay = workloads.make_layer(vw, 0, device=dev, n=vw.n + gam)
+    vs = 1.0 / math.sqrt(vw.d)
+    BHv = vw.batch * vw.hkv
+    kh = vw.text_tokens + 768
+    base_o = torch.arange(BHv + 1, dtype=torch.int32, device=dev) * kh
+    sc = sk.score_obs_window(lay["q_obs"][:, :, : vw.text_tokens].contiguous(), lay["k"], vw.n, vw.q_pos0, vs)
+    base_i = sk.select_topk(sc, vw.n, vw.cand_lo, vw.cand_hi, vw.n_sink, vw.n_recent, base_o, BHv * kh)
+    d_offs = [torch.empty(BHv + 1, dtype=torch.int32, device=dev) for _ in range(gam)]
+    d_idx = [torch.empty(BHv * (kh + t + 1), dtype=torch.int32, device=dev) for t in range(gam)]
+    o_d = torch.empty((vw.batch, vw.hq, vw.d), dtype=torch.bfloat16, device=dev)
+    o_v = torch.empty((vw.batch, vw.hq, gam, vw.d), dtype=torch.bfloat16, device=dev)
+    ws_sp = sk.new_workspace(sk.workspace_size(sk.OP_SPARSE_DECODE, vw.batch, vw.hq, vw.hkv, vw.d, 0, 0), dev)
+    ws_de = sk.new_workspace(sk.workspace_size(sk.OP_DENSE_VERIFY, vw.batch, vw.hq, vw.hkv, vw.d, vw.n + gam, gam),
+                             dev)
+
+    def round_():
+        for t in range(gam):
+            sk.append_drafts(base_o, base_i, BHv * kh, vw.n, t + 1, offsets=d_offs[t], indices=d_idx[t])
+            sk.sparse_decode_attn(lay["q_ver"][:, :, t].contiguous(), lay["k"], lay["v"], d_offs[t], d_idx[t], vs,
+                                  o=o_d, ws=ws_sp, want_lse=False)
+        sk.dense_verify_attn(lay["q_ver"], lay["k"], lay["v"], vw.n, vs, o=o_v, ws=ws_de, want_lse=False)
+    t_round = time_graph_us(round_, flush=flush)
+    out["f4_std_round"] = {"us_per_layer": t_round, "us_per_step_all_layers": t_round * vw.layers, "gamma": gam,
+                           "kept_per_head": kh, "launches_per_layer": 2 * gam + 1}
+    return out
+
+
 def run_sdkv(args, world, rank, local):
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU for --impl sdkv")
@@ -521,6 +643,8 @@ def run_sdkv(args, world, rank, local):
     }
     if not args.no_e2e:
         line["e2e"] = run_e2e(path, min(K, 5), world)
+    if rank == 0 and not args.no_next:
+        line["next_rows"] = next_rows_timings(path, hbm_peak, dev)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, lambda l: path.layers[l], args.cpu_seconds)
     if rank == 0:
