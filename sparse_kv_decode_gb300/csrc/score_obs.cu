@@ -287,10 +287,17 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
                         }
                         if (mx != -INFINITY) {
                             const float mnew = fmaxf(m_run, mx * c);
-                            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+                            // four running sums (lanes i%4) in two paired registers
+                            const float2 c2 = make_float2(c, c), nm2 = make_float2(-mnew, -mnew);
+                            float2 s01 = make_float2(0.f, 0.f), s23 = s01;
 #pragma unroll
-                            for (int i = 0; i < 64; ++i) s4[i & 3] += fast_exp2(fmaf(__uint_as_float(v[i]), c, -mnew));
-                            l_run = l_run * fast_exp2(m_run - mnew) + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+                            for (int i = 0; i < 64; i += 4) {
+                                const float2 x01 = fma2(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), c2, nm2);
+                                const float2 x23 = fma2(make_float2(__uint_as_float(v[i + 2]), __uint_as_float(v[i + 3])), c2, nm2);
+                                s01 = add2(s01, make_float2(fast_exp2(x01.x), fast_exp2(x01.y)));
+                                s23 = add2(s23, make_float2(fast_exp2(x23.x), fast_exp2(x23.y)));
+                            }
+                            l_run = l_run * fast_exp2(m_run - mnew) + ((s01.x + s01.y) + (s23.x + s23.y));
                             m_run = mnew;
                         }
                     }
@@ -298,27 +305,38 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
                     // lane tl is key key0 + tl; columns are window rows hh*64 + i
                     const int key = key0 + tl;
                     const bool all_rows = key0 + C::TK - 1 <= p.q_pos0;
-                    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+                    const float2 c2 = make_float2(c, c);
+                    float2 s01 = make_float2(0.f, 0.f), s23 = s01;   // running sums of columns i%4
+                    if (all_rows) {
+                        // every window row sees every key of the tile: no mask
 #pragma unroll
-                    for (int i = 0; i < 64; i += 4) {
-                        const float4 b4 = *reinterpret_cast<const float4*>(cb + hh * 64 + i);
-                        float e0 = fast_exp2(fmaf(__uint_as_float(v[i + 0]), c, b4.x));
-                        float e1 = fast_exp2(fmaf(__uint_as_float(v[i + 1]), c, b4.y));
-                        float e2 = fast_exp2(fmaf(__uint_as_float(v[i + 2]), c, b4.z));
-                        float e3 = fast_exp2(fmaf(__uint_as_float(v[i + 3]), c, b4.w));
-                        if (!all_rows) {
-                            const int4 l4 = *reinterpret_cast<const int4*>(lim + hh * 64 + i);
-                            e0 = key <= l4.x ? e0 : 0.f;
-                            e1 = key <= l4.y ? e1 : 0.f;
-                            e2 = key <= l4.z ? e2 : 0.f;
-                            e3 = key <= l4.w ? e3 : 0.f;
+                        for (int i = 0; i < 64; i += 4) {
+                            const float4 b4 = *reinterpret_cast<const float4*>(cb + hh * 64 + i);
+                            const float2 x01 = fma2(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), c2,
+                                                    make_float2(b4.x, b4.y));
+                            const float2 x23 = fma2(make_float2(__uint_as_float(v[i + 2]), __uint_as_float(v[i + 3])), c2,
+                                                    make_float2(b4.z, b4.w));
+                            s01 = add2(s01, make_float2(fast_exp2(x01.x), fast_exp2(x01.y)));
+                            s23 = add2(s23, make_float2(fast_exp2(x23.x), fast_exp2(x23.y)));
                         }
-                        s4[0] += e0;
-                        s4[1] += e1;
-                        s4[2] += e2;
-                        s4[3] += e3;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 64; i += 4) {
+                            const float4 b4 = *reinterpret_cast<const float4*>(cb + hh * 64 + i);
+                            const int4 l4 = *reinterpret_cast<const int4*>(lim + hh * 64 + i);
+                            const float2 x01 = fma2(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), c2,
+                                                    make_float2(b4.x, b4.y));
+                            const float2 x23 = fma2(make_float2(__uint_as_float(v[i + 2]), __uint_as_float(v[i + 3])), c2,
+                                                    make_float2(b4.z, b4.w));
+                            const float e0 = key <= l4.x ? fast_exp2(x01.x) : 0.f;
+                            const float e1 = key <= l4.y ? fast_exp2(x01.y) : 0.f;
+                            const float e2 = key <= l4.z ? fast_exp2(x23.x) : 0.f;
+                            const float e3 = key <= l4.w ? fast_exp2(x23.y) : 0.f;
+                            s01 = add2(s01, make_float2(e0, e1));
+                            s23 = add2(s23, make_float2(e2, e3));
+                        }
                     }
-                    acc += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+                    acc += (s01.x + s01.y) + (s23.x + s23.y);
                 }
             }
             if constexpr (PASS2) {

@@ -5,14 +5,19 @@
 //      order-preserving uint32 key (larger score -> larger key) kept in shared
 //      memory;
 //   2. four 8-bit radix passes find the K-th largest key T and how many
-//      candidates equal to T are taken (need_eq): every CTA counts its keys
-//      (per-warp histograms, four lane-skewed copies so that scores crowding
-//      into a few exponent bins do not serialise the atomics), the eight CTA
-//      histograms are added through distributed shared memory, and every CTA
-//      derives the same digit;
-//   3. an ordered sweep writes, in ascending index order, every candidate > T
-//      and the first need_eq candidates == T (lower indices win ties), each CTA
-//      placing its segment after the counts of the lower-ranked CTAs.
+//      candidates equal to T are taken (need_eq).  In each pass every CTA
+//      counts the digit of its keys that match the prefix so far in one
+//      shared-memory histogram, stores that histogram into a slot of every CTA
+//      of the cluster, and after one cluster barrier every CTA adds the eight
+//      slots and derives the same digit;
+//   3. the kept histograms also give, for every CTA, how many of its keys are
+//      above T and equal to T, so each CTA knows where its segment of the list
+//      starts without another exchange; an ordered sweep then writes, in
+//      ascending index order, every candidate > T and the first need_eq
+//      candidates == T (lower indices win ties).
+// All cross-CTA traffic is stores into the peers' shared memory ahead of a
+// cluster barrier: after the last barrier no CTA touches another's memory, so
+// each leaves as soon as its own part of the list is written.
 // The result is exact: the same fp32 scores always give the same list.
 #include "sdkv_common.cuh"
 #include "sdkv_internal.h"
@@ -24,13 +29,12 @@ namespace {
 constexpr int kCS = 8;                          // CTAs per head (portable cluster size)
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kSkew = 4;                        // histogram copies per warp
+constexpr int kPasses = 4;                      // 8-bit digits of a 32-bit key
 constexpr int kSelKeysPerCta = 32 * 1024;       // shared-memory keys per CTA
-constexpr int kOffHist = kSelKeysPerCta * 4;
-constexpr int kOffCHist = kOffHist + kSelWarps * kSkew * 256 * 4;   // [2][256] this CTA's histogram
-constexpr int kOffTot = kOffCHist + 2 * 256 * 4;                      // [256] cluster histogram
-constexpr int kOffCnt = kOffTot + 256 * 4;                            // [2] this CTA's (gt, eq)
-constexpr int kSelSmem = kOffCnt + 16;
+constexpr int kOffHist = kSelKeysPerCta * 4;                          // [2][256] this CTA's histogram
+constexpr int kOffRecv = kOffHist + 2 * 256 * 4;                      // [pass][rank][256] every CTA's
+constexpr int kOffTot = kOffRecv + kPasses * kCS * 256 * 4;           // [256] cluster histogram
+constexpr int kSelSmem = kOffTot + 256 * 4;
 
 // Order-preserving image of an fp32 score: larger score -> larger key;
 // -0.0 equals +0.0; NaN maps to 0, below every number.
@@ -41,10 +45,32 @@ __device__ __forceinline__ uint32_t score_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+__device__ __forceinline__ void st_dsmem_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Split cluster barrier: arrive early, wait where it matters.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ unsigned warp_sum_u32(unsigned v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+
+__device__ __forceinline__ unsigned warp_excl_scan_u32(unsigned v, int lane) {
+    unsigned incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    return incl - v;
 }
 
 __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kSelThreads, 1)
@@ -52,13 +78,12 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kSelThreads, 1)
                        int n_recent, const int* __restrict__ offsets, int* __restrict__ indices, int* status) {
     extern __shared__ __align__(16) uint8_t smem[];
     uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
-    unsigned* wh = reinterpret_cast<unsigned*>(smem + kOffHist);     // [warp][copy][256]
-    unsigned* chist = reinterpret_cast<unsigned*>(smem + kOffCHist);
+    unsigned* hist = reinterpret_cast<unsigned*>(smem + kOffHist);   // [pass & 1][256]
+    unsigned* recv = reinterpret_cast<unsigned*>(smem + kOffRecv);   // [pass][rank][256]
     unsigned* tot = reinterpret_cast<unsigned*>(smem + kOffTot);
-    unsigned* cnt = reinterpret_cast<unsigned*>(smem + kOffCnt);
-    __shared__ unsigned s_digit, s_gt;
+    __shared__ unsigned s_digit[kPasses], s_gt;
+    __shared__ unsigned s_rgt[kSelWarps];   // warp w: keys of rank w/2 above the digits of passes 2(w%2), +1
     __shared__ unsigned s_wgt[kSelWarps], s_weq[kSelWarps], s_pos[kSelWarps], s_eqt[kSelWarps];
-    __shared__ unsigned s_cbase[2];   // (equal keys before this CTA, kept candidates before this CTA)
 
     const int bh = blockIdx.x / kCS;
     const int rank = static_cast<int>(cluster_ctarank());
@@ -66,10 +91,24 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kSelThreads, 1)
     griddep_wait();
     griddep_launch();
 
+    // this CTA's candidates; their first scores are requested before the list
+    // sizes so that the two reads overlap
+    const int ncand = cand_hi - cand_lo;
+    const int seg = ((ncand + kCS - 1) / kCS + 31) & ~31;
+    const int c0 = min(rank * seg, ncand), c1 = min(c0 + seg, ncand);
+    const int len = c1 - c0;
+    const float* sc = scores + static_cast<size_t>(bh) * n + cand_lo + c0;
+    constexpr int kInFlight = 16;
+    float v[kInFlight];
+#pragma unroll
+    for (int u = 0; u < kInFlight; ++u) {
+        const int i = tid + u * kSelThreads;
+        v[u] = (i < len) ? __ldg(sc + i) : 0.f;
+    }
+
     // every decision up to the sweep depends on the head only: uniform in the cluster
     const int start = offsets[bh];
     const int kh = offsets[bh + 1] - start;
-    const int ncand = cand_hi - cand_lo;
     const int K = kh - n_sink - n_recent;
     if (K < 0 || K > ncand) {
         if (rank == 0 && tid == 0) flag_status(status, SDKV_DEV_BAD_LIST);
@@ -81,56 +120,61 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kSelThreads, 1)
         for (int i = tid; i < n_recent; i += kSelThreads) out[n_sink + K + i] = n - n_recent + i;
     }
     if (K == 0) return;
-    const int seg = ((ncand + kCS - 1) / kCS + 31) & ~31;
-    const int c0 = min(rank * seg, ncand), c1 = min(c0 + seg, ncand);
-    const int len = c1 - c0;
     if (K == ncand) {
         for (int i = tid; i < len; i += kSelThreads) out[n_sink + c0 + i] = cand_lo + c0 + i;
         return;
     }
-    const float* sc = scores + static_cast<size_t>(bh) * n + cand_lo + c0;
-    for (int i0 = tid; i0 < len; i0 += 16 * kSelThreads) {   // 16 loads in flight per thread
-        float v[16];
+    // a peer's shared memory may be written only once that peer has started:
+    // arrive now, wait before the first store into a peer
+    cluster_arrive_relaxed();
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
+    for (int u = 0; u < kInFlight; ++u) {
+        const int i = tid + u * kSelThreads;
+        if (i < len) keys[i] = score_key(v[u]);
+    }
+    for (int i0 = tid + kInFlight * kSelThreads; i0 < len; i0 += kInFlight * kSelThreads) {
+#pragma unroll
+        for (int u = 0; u < kInFlight; ++u) {
             const int i = i0 + u * kSelThreads;
             v[u] = (i < len) ? __ldg(sc + i) : 0.f;
         }
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
+        for (int u = 0; u < kInFlight; ++u) {
             const int i = i0 + u * kSelThreads;
             if (i < len) keys[i] = score_key(v[u]);
         }
     }
+    hist[tid] = 0u;   // both parities (2 * 256 = kSelThreads entries)
+    __syncthreads();
 
     // ---- radix select of the K-th largest key, 8 bits per pass
     uint32_t prefix = 0, pmask = 0;
     unsigned krem = static_cast<unsigned>(K);
-    unsigned* myh = wh + warp * kSkew * 256 + (lane & (kSkew - 1)) * 256;
-    int pass = 0;
 #pragma unroll 1
-    for (int sh = 24; sh >= 0; sh -= 8, ++pass) {
-        for (int i = lane; i < kSkew * 256; i += 32) wh[warp * kSkew * 256 + i] = 0u;
-        __syncthreads();
+    for (int pass = 0; pass < kPasses; ++pass) {
+        const int sh = 24 - 8 * pass;
+        unsigned* h = hist + (pass & 1) * 256;
 #pragma unroll 4
         for (int i = tid; i < len; i += kSelThreads) {
             const uint32_t u = keys[i];
-            if ((u & pmask) == prefix) atomicAdd(&myh[(u >> sh) & 0xffu], 1u);
+            if ((u & pmask) == prefix) atomicAdd(&h[(u >> sh) & 0xffu], 1u);
         }
         __syncthreads();
-        unsigned* ch = chist + (pass & 1) * 256;   // alternating: peers read the previous one
+        if (pass == 0) cluster_wait();   // every CTA of the cluster is running
         if (tid < 256) {
-            unsigned c = 0;
-#pragma unroll 8
-            for (int w = 0; w < kSelWarps * kSkew; ++w) c += wh[w * 256 + tid];
-            ch[tid] = c;
+            // this CTA's histogram into slot [pass][rank] of every CTA of the cluster
+            const unsigned c = h[tid];
+            const uint32_t a = smem_u32(recv + (pass * kCS + rank) * 256 + tid);
+#pragma unroll
+            for (int r = 0; r < kCS; ++r) st_dsmem_u32(dsmem_addr(a, r), c);
+        } else {
+            hist[((pass + 1) & 1) * 256 + (tid - 256)] = 0u;   // the next pass's histogram
         }
-        cluster_sync_all();   // every CTA's histogram of this pass is complete
+        cluster_sync_all();   // every CTA's histogram of this pass has arrived everywhere
         if (tid < 256) {
-            const uint32_t a = smem_u32(ch + tid);
             unsigned c = 0;
 #pragma unroll
-            for (int r = 0; r < kCS; ++r) c += ld_dsmem_u32(dsmem_addr(a, r));
+            for (int r = 0; r < kCS; ++r) c += recv[(pass * kCS + r) * 256 + tid];
             tot[tid] = c;
         }
         __syncthreads();
@@ -142,96 +186,78 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kSelThreads, 1)
                 cnt8[j] = tot[255 - 8 * lane - j];
                 sum += cnt8[j];
             }
-            unsigned incl = sum;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            unsigned gt = incl - sum;   // keys with a larger digit than this lane's first
+            unsigned gt = warp_excl_scan_u32(sum, lane);   // keys with a larger digit than this lane's first
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 if (gt < krem && krem <= gt + cnt8[j]) {
-                    s_digit = 255 - 8 * lane - j;
+                    s_digit[pass] = 255 - 8 * lane - j;
                     s_gt = gt;
                 }
                 gt += cnt8[j];
             }
         }
         __syncthreads();
-        prefix |= s_digit << sh;
+        prefix |= s_digit[pass] << sh;
         pmask |= 0xffu << sh;
         krem -= s_gt;
     }
     const uint32_t T = prefix;
     const unsigned need_eq = krem;  // >= 1 candidates equal to T are taken in all
 
-    // ---- ordered sweep: warp w owns [w*wseg, (w+1)*wseg) of this CTA's segment
+    // ---- where each CTA's segment of the list starts.  A key is above T when,
+    // at the first pass where its digit differs from T's, the digit is larger:
+    // rank r holds sum over passes p of its slot-p counts of digits > digit_p.
+    {
+        const int r = warp >> 1, p0 = (warp & 1) * 2;
+        unsigned g = 0;
+#pragma unroll
+        for (int pp = p0; pp < p0 + 2; ++pp) {
+            const unsigned dig = s_digit[pp];
+            const unsigned* hr = recv + (pp * kCS + r) * 256;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const unsigned d = lane + 32 * j;   // consecutive lanes, consecutive banks
+                if (d > dig) g += hr[d];
+            }
+        }
+        g = warp_sum_u32(g);
+        if (lane == 0) s_rgt[warp] = g;
+    }
+    // ---- this CTA's keys above / equal to T, per warp: warp w owns [w*wseg, (w+1)*wseg)
     const int wseg = ((len + kSelWarps - 1) / kSelWarps + 31) & ~31;
     const int w0 = min(warp * wseg, len), w1 = min(w0 + wseg, len);
     unsigned ngt = 0, neq = 0;
-#pragma unroll 4
+#pragma unroll 8
     for (int i = w0 + lane; i < w1; i += 32) {
         const uint32_t u = keys[i];
         ngt += (u > T);
         neq += (u == T);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        ngt += __shfl_xor_sync(0xffffffffu, ngt, o);
-        neq += __shfl_xor_sync(0xffffffffu, neq, o);
-    }
+    ngt = warp_sum_u32(ngt);
+    neq = warp_sum_u32(neq);
     if (lane == 0) {
         s_wgt[warp] = ngt;
         s_weq[warp] = neq;
     }
     __syncthreads();
     if (tid == 0) {
-        unsigned g = 0, e = 0;
-        for (int w = 0; w < kSelWarps; ++w) {
-            g += s_wgt[w];
-            e += s_weq[w];
-        }
-        cnt[0] = g;
-        cnt[1] = e;
-    }
-    cluster_sync_all();   // every CTA's (gt, eq) is visible
-    if (tid == 0) {
-        // the CTAs of lower rank hold the earlier candidates
+        // the CTAs of lower rank hold the earlier candidates, then the warps of
+        // this CTA in order (a short serial walk: at most kCS + kSelWarps steps)
         unsigned eq_before = 0, kept_before = 0;
-        const uint32_t a = smem_u32(cnt);
         for (int r = 0; r < rank; ++r) {
-            const unsigned g = ld_dsmem_u32(dsmem_addr(a, r));
-            const unsigned e = ld_dsmem_u32(dsmem_addr(a + 4, r));
+            const unsigned g = s_rgt[2 * r] + s_rgt[2 * r + 1];
+            const unsigned e = recv[((kPasses - 1) * kCS + r) * 256 + s_digit[kPasses - 1]];
             const unsigned take = (need_eq > eq_before) ? min(e, need_eq - eq_before) : 0u;
             kept_before += g + take;
             eq_before += e;
         }
-        s_cbase[0] = eq_before;
-        s_cbase[1] = kept_before;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        const unsigned eqw = lane < kSelWarps ? s_weq[lane] : 0u;
-        const unsigned gtw = lane < kSelWarps ? s_wgt[lane] : 0u;
-        unsigned eq_incl = eqw;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const unsigned y = __shfl_up_sync(0xffffffffu, eq_incl, o);
-            if (lane >= o) eq_incl += y;
-        }
-        const unsigned eq_before = s_cbase[0] + eq_incl - eqw;
-        const unsigned eq_take = (need_eq > eq_before) ? min(eqw, need_eq - eq_before) : 0u;
-        const unsigned sel = gtw + eq_take;
-        unsigned sel_incl = sel;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const unsigned y = __shfl_up_sync(0xffffffffu, sel_incl, o);
-            if (lane >= o) sel_incl += y;
-        }
-        if (lane < kSelWarps) {
-            s_pos[lane] = s_cbase[1] + sel_incl - sel;
-            s_eqt[lane] = eq_take;
+        for (int w = 0; w < kSelWarps; ++w) {
+            const unsigned eqw = s_weq[w];
+            const unsigned eq_take = (need_eq > eq_before) ? min(eqw, need_eq - eq_before) : 0u;
+            s_pos[w] = kept_before;
+            s_eqt[w] = eq_take;
+            kept_before += s_wgt[w] + eq_take;
+            eq_before += eqw;
         }
     }
     __syncthreads();
@@ -239,6 +265,7 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kSelThreads, 1)
     const unsigned eq_take = s_eqt[warp];
     unsigned eq_seen = 0;
     const unsigned lt = (1u << lane) - 1u;
+#pragma unroll 8
     for (int i0 = w0; i0 < w1; i0 += 32) {
         const int i = i0 + lane;
         const bool inb = i < w1;
@@ -251,7 +278,6 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kSelThreads, 1)
         pos += __popc(tf);
         eq_seen += __popc(eqf);
     }
-    cluster_sync_all();   // peers may leave once everyone has read their counts
 }
 
 }  // namespace
