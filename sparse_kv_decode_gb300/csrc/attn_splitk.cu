@@ -51,6 +51,7 @@ struct AttnParams {
 // Kinds of rows a launch streams: the whole cache (dense verify), rows gathered
 // through the index lists, or the lists' rows compacted into contiguous buffers.
 constexpr int kDense = 0, kGather = 1, kContig = 2;
+constexpr int kMaxCluster = 8;     // portable cluster size
 
 template <int D, int MT, int KW, int TK, int STAGES, int KIND>
 struct AttnCfg {
@@ -525,9 +526,10 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, KIND>::NT)
                 const int owner = d0 / SL;
                 st_dsmem_f4(dsmem_addr(sbase + C::OFF_RCV + ((me * p.R + row) * SL + (d0 - owner * SL)) * 4, owner),
                             a4);
-                if (d0 == 0)
-                    for (int r = 0; r < p.cs; ++r)
-                        st_dsmem_f2(dsmem_addr(sbase + C::OFF_RML + (me * p.R + row) * 8, r), make_float2(M, L));
+                // every lane of the row holds the same (M, L): lane d0/4 sends it to
+                // rank d0/4 (D/4 >= cluster size, so one remote store at most per lane)
+                for (int r = d0 / 4; r < p.cs; r += D / 4)
+                    st_dsmem_f2(dsmem_addr(sbase + C::OFF_RML + (me * p.R + row) * 8, r), make_float2(M, L));
             } else if (nch == 1) {
                 const float il = L > 0.f ? 1.f / L : 0.f;
                 uint2 packed;
@@ -564,20 +566,32 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, KIND>::NT)
                 const int row = e / sl4;
                 const int dd = 4 * (e - row * sl4);
                 const int d0 = static_cast<int>(rank) * SL + dd;
+                // unrolled to the largest cluster so that all loads are in flight together
+                float2 ml2[kMaxCluster];
+                float4 v4[kMaxCluster];
+#pragma unroll
+                for (int c = 0; c < kMaxCluster; ++c) {
+                    ml2[c] = make_float2(-INFINITY, 0.f);
+                    v4[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (c < CS) {
+                        ml2[c] = rml[c * p.R + row];
+                        v4[c] = *reinterpret_cast<const float4*>(rcv + (c * p.R + row) * SL + dd);
+                    }
+                }
                 float M = -INFINITY;
-                for (int c = 0; c < CS; ++c) M = fmaxf(M, rml[c * p.R + row].x);
+#pragma unroll
+                for (int c = 0; c < kMaxCluster; ++c) M = fmaxf(M, ml2[c].x);
                 float L = 0.f;
                 float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int c = 0; c < CS; ++c) {
-                    const float2 ml2 = rml[c * p.R + row];
-                    if (ml2.x == -INFINITY) continue;
-                    const float w = fast_exp2(ml2.x - M);
-                    L += w * ml2.y;
-                    const float4 v4 = *reinterpret_cast<const float4*>(rcv + (c * p.R + row) * SL + dd);
-                    a4.x += w * v4.x;
-                    a4.y += w * v4.y;
-                    a4.z += w * v4.z;
-                    a4.w += w * v4.w;
+#pragma unroll
+                for (int c = 0; c < kMaxCluster; ++c) {
+                    if (ml2[c].x == -INFINITY) continue;
+                    const float w = fast_exp2(ml2[c].x - M);
+                    L += w * ml2[c].y;
+                    a4.x += w * v4[c].x;
+                    a4.y += w * v4[c].y;
+                    a4.z += w * v4[c].z;
+                    a4.w += w * v4[c].w;
                 }
                 const int g = row / p.gamma, tt = row - (row / p.gamma) * p.gamma;
                 const size_t orow = (static_cast<size_t>(b) * p.Hq + h * p.G + g) * p.gamma + tt;
@@ -761,7 +775,6 @@ constexpr int kDenseTK = 64;
 constexpr int kDenseStages = 3;
 constexpr int kSparseTK = 64;
 constexpr int kSparseStages = 3;
-constexpr int kMaxCluster = 8;     // portable cluster size
 
 // per-head counters: one per head-dim slice of a cluster merge (at most kMaxCluster)
 size_t attn_ticket_bytes(int BH) { return sizeof(int) * static_cast<size_t>(BH) * kMaxCluster; }
