@@ -334,8 +334,8 @@ int sdkv_sparse_decode_compact(const void* q, const void* k_c, const void* v_c, 
  * always-kept range [keep_lo, keep_hi) (e.g. the text tokens), ascending.
  * Exact decisions: every mass is a_j rounded to the nearest multiple of 2^-32
  * and summed as an integer; lam_r * S, I and k * I are float64.
- *   scores     device float [B][units][n], finite and >= 0 (others count as
- *              0 and set SDKV_DEV_BAD_LIST)
+ *   scores     device float [B][units][n]; importance values outside
+ *              [0, 2^31) and NaN count as 0 and set SDKV_DEV_BAD_LIST
  *   lam_r      in [0, 1];  r (pruning ratio) in [0, 1)
  *   keep range disjoint from V
  *   importance device float [B][n] (written)
@@ -344,8 +344,10 @@ int sdkv_sparse_decode_compact(const void* q, const void* k_c, const void* v_c, 
  *   counts     device int32 [B] (written)
  *   ws         workspace of at least sdkv_workspace_size(SDKV_OP_SPECVLM, B, 0,
  *              0, 0, v_hi - v_lo, 0)
- * Asynchronous on `stream`.  One CTA per sequence; up to 16384 video tokens
- * sort in shared memory, more in the workspace (at most 2^20).
+ * Asynchronous on `stream`.  One CTA per sequence; Stage I is a radix search
+ * for the crossing on the score bits (counts and masses per digit), Stage II
+ * enumerates floor(k I).  Up to 16384 video tokens keep their keys in shared
+ * memory, more in the workspace (at most 2^20).
  */
 int sdkv_specvlm_select(const float* scores, int32_t B, int32_t units, int32_t n,
                         int32_t v_lo, int32_t v_hi, double lam_r, double r,

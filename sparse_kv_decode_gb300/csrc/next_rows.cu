@@ -97,12 +97,22 @@ __global__ void importance_kernel(const float* __restrict__ scores, int units, i
     if (j >= n) return;
     const float* s = scores + static_cast<size_t>(b) * units * n + j;
     float acc = 0.f;
-    for (int u = 0; u < units; ++u) acc += s[static_cast<size_t>(u) * n];   // units in order
+    constexpr int kBatch = 32;   // loads in flight; the adds stay in unit order
+    for (int u0 = 0; u0 < units; u0 += kBatch) {
+        float x[kBatch];
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) x[q] = (u0 + q < units) ? __ldg(s + static_cast<size_t>(u0 + q) * n) : 0.f;
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q)
+            if (u0 + q < units) acc += x[q];
+    }
     importance[static_cast<size_t>(b) * n + j] = acc * inv_units;
 }
 
 constexpr int kSpecNT = 1024;
-constexpr int kSpecSmemKeys = 16384;   // sort in shared memory up to this many keys
+constexpr int kSpecSmemKeys = 16384;       // keys in shared memory up to this many video tokens
+constexpr int kSpecMaxTokens = 1 << 20;    // the sampled-rank bitmap lives in shared memory
+constexpr int kSpecSmemMax = 4 * ((1 << 20) / 32);
 
 struct SpecParams {
     const float* importance;
@@ -111,9 +121,8 @@ struct SpecParams {
     int* indices;
     int* counts;
     int* status;
-    unsigned long long* keys_ws;   // [B][N2] when the keys do not fit shared memory
-    unsigned char* flags_ws;       // [B][nV]
-    int N2;
+    uint32_t* keys_ws;   // [B][nV] when the keys do not fit shared memory
+    uint8_t* flags_ws;   // [B][nV] likewise
     bool keys_in_smem;
 };
 
@@ -144,132 +153,282 @@ __device__ long long cta_excl_scan(long long v, long long* s_w, long long* total
     return res;
 }
 
-// The mass of a score: the nearest multiple of 2^-32, as an integer.
-__device__ __forceinline__ long long mass_of_key(unsigned long long key) {
-    const uint32_t bits = ~static_cast<uint32_t>(key >> 32);
-    return __double2ll_rn(static_cast<double>(__uint_as_float(bits)) * 4294967296.0);
+// The mass of a score in [0, 2^31) from its fp32 bits: score * 2^32 rounded to
+// the nearest integer, ties to even.  The score is man * 2^(ex - 150) with a
+// 24-bit significand, so the scaled value man * 2^(ex - 118) is exact and the
+// rounding is decided on the bits shifted out.
+__device__ __forceinline__ long long mass_of_bits(uint32_t bits) {
+    const int ex = static_cast<int>(bits >> 23);
+    if (ex == 0) return 0;                                            // subnormal: far below 1/2
+    const unsigned long long man = (bits & 0x7fffffu) | 0x800000u;
+    const int sh = ex - 118;
+    if (sh >= 0) return static_cast<long long>(man << sh);
+    const int s = -sh;
+    if (s > 24) return 0;                                             // man < 2^24 <= 2^(s-1): below 1/2
+    const unsigned long long q = man >> s, rem = man & ((1ull << s) - 1ull), half = 1ull << (s - 1);
+    return static_cast<long long>(q + ((rem > half || (rem == half && (q & 1ull))) ? 1ull : 0ull));
 }
 
 __global__ void __launch_bounds__(kSpecNT, 1) specvlm_select_kernel(const __grid_constant__ SpecParams p) {
     extern __shared__ __align__(16) uint8_t dyn[];
     __shared__ long long s_w[kSpecNT / 32];
-    __shared__ int s_first;
-    const int b = blockIdx.x, tid = threadIdx.x;
-    const int nV = p.v_hi - p.v_lo, N2 = p.N2;
-    unsigned long long* keys = p.keys_in_smem ? reinterpret_cast<unsigned long long*>(dyn)
-                                              : p.keys_ws + static_cast<size_t>(b) * N2;
-    unsigned char* flag = p.flags_ws + static_cast<size_t>(b) * nV;
+    __shared__ unsigned s_cnt[256];
+    __shared__ unsigned s_mlo[256], s_mhi[256];   // per-digit mass: low word (wraps carried) and high word
+    __shared__ unsigned s_digit, s_cnt_above;
+    __shared__ long long s_above, s_j;
+    __shared__ double s_target, s_I;
+    __shared__ long long s_kcap;
+    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nV = p.v_hi - p.v_lo;
+    const int nW = (nV + 31) >> 5;
+    uint32_t* taken = reinterpret_cast<uint32_t*>(dyn);   // [nW] bitmap of the sampled leftover ranks
+    uint32_t* keys = p.keys_in_smem ? taken + nW : p.keys_ws + static_cast<size_t>(b) * nV;
+    uint8_t* fl = p.keys_in_smem ? reinterpret_cast<uint8_t*>(taken + nW + nV)
+                                 : p.flags_ws + static_cast<size_t>(b) * nV;   // 0, 1 = V_R, 2 = V_U
     const float* a = p.importance + static_cast<size_t>(b) * p.n + p.v_lo;
 
-    // keys: (~score bits, token) ascending = score descending, lower token first;
-    // NaN and negative scores count as zero mass; padding sorts last
-    for (int e = tid; e < N2; e += kSpecNT) {
-        unsigned long long key = ~0ull;
-        if (e < nV) {
-            float x = a[e];
-            if (!(x >= 0.f)) {
+    // keys = fp32 bits of the score shifted left by one (the sign bit is 0, so
+    // the first digit is the exponent): larger key, larger score.  Scores
+    // outside [0, 2^31) and NaN count as zero mass; -0 equals +0.
+    long long mloc = 0;
+    constexpr int kLoads = 8;   // loads in flight per thread
+    for (int e0 = tid; e0 < nV; e0 += kLoads * kSpecNT) {
+        float xs[kLoads];
+#pragma unroll
+        for (int q = 0; q < kLoads; ++q) {
+            const int e = e0 + q * kSpecNT;
+            xs[q] = e < nV ? a[e] : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < kLoads; ++q) {
+            const int e = e0 + q * kSpecNT;
+            if (e >= nV) break;
+            float x = xs[q];
+            if (!(x >= 0.f && x < 2147483648.f)) {
                 flag_status(p.status, SDKV_DEV_BAD_LIST);
                 x = 0.f;
             }
-            const uint32_t bits = __float_as_uint(x) & 0x7fffffffu;   // -0 -> +0
-            key = (static_cast<unsigned long long>(~bits) << 32) | static_cast<uint32_t>(e);
+            const uint32_t bits = __float_as_uint(x) & 0x7fffffffu;
+            keys[e] = bits << 1;
+            mloc += mass_of_bits(bits);
         }
-        keys[e] = key;
     }
-    for (int e = tid; e < nV; e += kSpecNT) flag[e] = 0;
+    for (int w = tid; w < nW; w += kSpecNT) taken[w] = 0u;
+    for (int i = tid; i < 256; i += kSpecNT) {
+        s_cnt[i] = 0u;
+        s_mlo[i] = 0u;
+        s_mhi[i] = 0u;
+    }
+    long long S = 0;
+    cta_excl_scan(mloc, s_w, &S);   // also orders the stores above before every later read
+    if (tid == 0) s_target = p.lam_r * static_cast<double>(S);
     __syncthreads();
-    // bitonic sort, ascending
-    for (int kk = 2; kk <= N2; kk <<= 1) {
-        for (int j = kk >> 1; j > 0; j >>= 1) {
-            for (int i = tid; i < N2; i += kSpecNT) {
-                const int ixj = i ^ j;
-                if (ixj > i) {
-                    const unsigned long long x = keys[i], y = keys[ixj];
-                    const bool up = (i & kk) == 0;
-                    if ((x > y) == up) {
-                        keys[i] = y;
-                        keys[ixj] = x;
-                    }
+    const double target = s_target;
+
+    // ---- Stage I.  In the order (score descending, lower token first) V_R ends
+    // at the first token where the running mass reaches the target.  Its key T
+    // is found 8 bits at a time: per digit of the keys that share the prefix so
+    // far, their count and mass; the digit whose range crosses the target is
+    // the next digit of T.  Then the keys above T are all in V_R, and of the
+    // keys equal to T (equal masses) the lowest j tokens complete it.
+    const bool stage1 = target > 0.0;
+    uint32_t T = 0u;
+    long long j = 0;
+    long long c = 0;   // |V_R|
+    if (stage1) {
+        uint32_t prefix = 0u, pmask = 0u;
+        long long above = 0;
+        unsigned cnt_above = 0u, cnt_T = 0u;
+#pragma unroll 1
+        for (int sh = 24; sh >= 0; sh -= 8) {
+            if (tid == 0) {   // overwritten by the crossing digit, which always exists
+                s_digit = 0u;
+                s_above = above;
+                s_cnt_above = cnt_above;
+            }
+            for (int e = tid; e < nV; e += kSpecNT) {
+                const uint32_t u = keys[e];
+                if ((u & pmask) == prefix) {
+                    const unsigned d = (u >> sh) & 0xffu;
+                    const unsigned long long m = static_cast<unsigned long long>(mass_of_bits(u >> 1));
+                    const unsigned lo = static_cast<unsigned>(m);
+                    unsigned hi = static_cast<unsigned>(m >> 32);
+                    atomicAdd(&s_cnt[d], 1u);
+                    const unsigned old = atomicAdd(&s_mlo[d], lo);
+                    if (old + lo < old) ++hi;   // this add wrapped the low word
+                    if (hi) atomicAdd(&s_mhi[d], hi);
                 }
             }
             __syncthreads();
+            if (warp == 0) {
+                // lane owns digits 255 - 8*lane .. 248 - 8*lane (descending)
+                long long m8[8], msum = 0;
+                unsigned c8[8], csum = 0;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int d = 255 - 8 * lane - q;
+                    m8[q] = static_cast<long long>((static_cast<unsigned long long>(s_mhi[d]) << 32) | s_mlo[d]);
+                    c8[q] = s_cnt[d];
+                    msum += m8[q];
+                    csum += c8[q];
+                }
+                long long mx = msum;
+                unsigned cx = csum;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const long long ym = __shfl_up_sync(0xffffffffu, mx, o);
+                    const unsigned yc = __shfl_up_sync(0xffffffffu, cx, o);
+                    if (lane >= o) {
+                        mx += ym;
+                        cx += yc;
+                    }
+                }
+                long long mb = above + mx - msum;
+                unsigned cb = cnt_above + cx - csum;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const long long mn = mb + m8[q];
+                    if (static_cast<double>(mb) < target && static_cast<double>(mn) >= target) {
+                        s_digit = 255 - 8 * lane - q;
+                        s_above = mb;
+                        s_cnt_above = cb;
+                    }
+                    mb = mn;
+                    cb += c8[q];
+                }
+            }
+            __syncthreads();
+            const unsigned d = s_digit & 0xffu;
+            above = s_above;
+            cnt_above = s_cnt_above;
+            cnt_T = s_cnt[d];
+            prefix |= d << sh;
+            pmask |= 0xffu << sh;
+            __syncthreads();   // every thread has read this pass's histogram
+            for (int i = tid; i < 256; i += kSpecNT) {
+                s_cnt[i] = 0u;
+                s_mlo[i] = 0u;
+                s_mhi[i] = 0u;
+            }
+            __syncthreads();
         }
+        T = prefix;
+        if (tid == 0) {
+            // the fewest keys equal to T (mass mT > 0 each) that reach the target
+            const long long mT = mass_of_bits(T >> 1);
+            long long jj = static_cast<long long>(cnt_T);
+            if (mT > 0) {
+                const double est = ceil((target - static_cast<double>(above)) / static_cast<double>(mT));
+                if (est < static_cast<double>(cnt_T)) jj = static_cast<long long>(est);
+            }
+            jj = max(1ll, min(jj, static_cast<long long>(cnt_T)));
+            while (jj > 1 && static_cast<double>(above + (jj - 1) * mT) >= target) --jj;
+            while (jj < static_cast<long long>(cnt_T) && static_cast<double>(above + jj * mT) < target) ++jj;
+            s_j = jj;
+        }
+        __syncthreads();
+        j = s_j;
+        c = static_cast<long long>(cnt_above) + j;
     }
-    // Stage I: prefix masses over the sorted order (each thread a contiguous block)
+
+    // ---- token order: each thread a contiguous block of V; fl[e] = 1 for V_R
     const int per = (nV + kSpecNT - 1) / kSpecNT;
     const int i0 = min(nV, tid * per), i1 = min(nV, i0 + per);
-    long long local = 0;
-    for (int i = i0; i < i1; ++i) local += mass_of_key(keys[i]);
-    long long S = 0;
-    const long long before = cta_excl_scan(local, s_w, &S);
-    const double target = p.lam_r * static_cast<double>(S);
-    if (tid == 0) s_first = nV;
-    __syncthreads();
+    const int j32 = static_cast<int>(j);
+    int eq_local = 0;
+    if (stage1)
+        for (int e = i0; e < i1; ++e) eq_local += (keys[e] == T) ? 1 : 0;
+    long long tot_eq = 0;
+    const int eq0 = static_cast<int>(cta_excl_scan(eq_local, s_w, &tot_eq));
+    int left_local = 0;
     {
-        long long acc = before;
-        for (int i = i0; i < i1; ++i) {
-            acc += mass_of_key(keys[i]);
-            if (static_cast<double>(acc) >= target) {
-                atomicMin(&s_first, i);
-                break;
+        int eqr = eq0;   // keys equal to T before this token
+        for (int e = i0; e < i1; ++e) {
+            const uint32_t u = keys[e];
+            bool in1 = false;
+            if (stage1 && u >= T) {
+                in1 = (u > T) || (eqr < j32);
+                eqr += (u == T) ? 1 : 0;
             }
+            fl[e] = in1 ? 1 : 0;
+            left_local += in1 ? 0 : 1;
         }
     }
-    __syncthreads();
-    const int c = (target <= 0.0) ? 0 : min(nV, s_first + 1);
-    for (int i = tid; i < c; i += kSpecNT) flag[static_cast<uint32_t>(keys[i])] = 1;
-    __syncthreads();
-    // Stage II: leftover ranks in token order, then the walk floor(k I) decided per token
-    long long nleft_local = 0;
-    for (int e = i0; e < i1; ++e) nleft_local += flag[e] ? 0 : 1;
     long long L = 0;
-    const long long rank0 = cta_excl_scan(nleft_local, s_w, &L);
-    const double I = static_cast<double>(nV - c) / ((1.0 - p.r) * static_cast<double>(nV));
-    long long rho = rank0;
-    long long keep_local = 0;
-    for (int e = i0; e < i1; ++e) {
-        if (!flag[e]) {
-            bool take = false;
-            if (I > 0.0) {
-                const double kc = floor(static_cast<double>(rho) / I);
-                for (double kk = fmax(kc - 1.0, 0.0); kk <= kc + 2.0 && !take; kk += 1.0)
-                    take = floor(kk * I) == static_cast<double>(rho);
-            }
-            if (take) flag[e] = 2;
-            ++rho;
+    const int rank0 = static_cast<int>(cta_excl_scan(left_local, s_w, &L));   // L = |V| - |V_R|
+
+    // ---- Stage II: the leftover ranks floor(k I) < L, k = 0, 1, ...  floor(k I)
+    // never decreases in k, and I >= 1/|V| when positive, so k <= |V| + 2 covers them
+    if (tid == 0) {
+        const double I0 = static_cast<double>(nV - c) / ((1.0 - p.r) * static_cast<double>(nV));
+        long long kcap = -1;
+        if (I0 > 0.0) {
+            const double kc = ceil(static_cast<double>(L) / I0) + 1.0;
+            kcap = kc < static_cast<double>(nV + 2) ? static_cast<long long>(kc) : nV + 2;
         }
-        keep_local += flag[e] ? 1 : 0;
+        s_I = I0;
+        s_kcap = kcap;
     }
     __syncthreads();
+    const double I = s_I;
+    {
+        const long long kcap = s_kcap;
+        for (long long k = tid; k <= kcap; k += kSpecNT) {
+            const double pos = floor(static_cast<double>(k) * I);
+            if (pos < static_cast<double>(L)) {
+                const int ip = static_cast<int>(pos);
+                atomicOr(&taken[ip >> 5], 1u << (ip & 31));
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- output: V_R u V_U ascending, with the always-kept range before or after V
+    int keep_local = 0;
+    {
+        int rr = rank0;   // leftover rank of the next leftover token
+        for (int e = i0; e < i1; ++e) {
+            if (!fl[e]) {
+                if ((taken[rr >> 5] >> (rr & 31)) & 1u) fl[e] = 2;
+                ++rr;
+            }
+            keep_local += fl[e] ? 1 : 0;
+        }
+    }
     long long nkeep = 0;
     const long long out0 = cta_excl_scan(keep_local, s_w, &nkeep);
-    // output: the kept tokens ascending, with the always-kept range before or after V
     const int nk = p.keep_hi - p.keep_lo;
     const bool keep_first = p.keep_hi <= p.v_lo;
     int* out = p.indices + static_cast<size_t>(b) * p.cap;
-    const long long vbase = keep_first ? nk : 0;
-    long long o = vbase + out0;
-    for (int e = i0; e < i1; ++e)
-        if (flag[e]) out[o++] = p.v_lo + e;
+    if (p.keys_in_smem) {
+        // the keys are no longer needed: stage V's part of the list there, then
+        // copy it out with consecutive threads on consecutive entries
+        __syncthreads();
+        int* stage = reinterpret_cast<int*>(keys);
+        int o = static_cast<int>(out0);
+        for (int e = i0; e < i1; ++e)
+            if (fl[e]) stage[o++] = p.v_lo + e;
+        __syncthreads();
+        int* dst = out + (keep_first ? nk : 0);
+        for (int i = tid; i < static_cast<int>(nkeep); i += kSpecNT) dst[i] = stage[i];
+    } else {
+        int o = (keep_first ? nk : 0) + static_cast<int>(out0);
+        for (int e = i0; e < i1; ++e)
+            if (fl[e]) out[o++] = p.v_lo + e;
+    }
     const long long kbase = keep_first ? 0 : nkeep;
     for (int e = tid; e < nk; e += kSpecNT) out[kbase + e] = p.keep_lo + e;
     if (tid == 0) p.counts[b] = static_cast<int>(nkeep + nk);
 }
 
 // ============================================================================ host
-namespace {
-int pow2_at_least(int x) {
-    int v = 1;
-    while (v < x) v <<= 1;
-    return v;
-}
-}  // namespace
 
 size_t specvlm_ws_bytes(int B, int nV) {
-    const int N2 = pow2_at_least(std::max(nV, 1));
     size_t bytes = kWsHeader;
-    if (N2 > kSpecSmemKeys) bytes += align256(sizeof(unsigned long long) * static_cast<size_t>(B) * N2);
-    bytes += align256(static_cast<size_t>(B) * std::max(nV, 1));
+    if (nV > kSpecSmemKeys) {
+        bytes += align256(sizeof(uint32_t) * static_cast<size_t>(B) * nV);   // keys
+        bytes += align256(static_cast<size_t>(B) * nV);                      // flags
+    }
     return bytes;
 }
 
@@ -328,7 +487,10 @@ int launch_compact_kv(const CompactLaunch& a, const char** why) {
 
 int launch_specvlm(const SpecLaunch& a, const char** why) {
     const int nV = a.v_hi - a.v_lo;
-    const int N2 = pow2_at_least(std::max(nV, 1));
+    if (nV > kSpecMaxTokens) {
+        *why = "more than 2^20 video tokens";
+        return SDKV_ERR_UNSUPPORTED;
+    }
     uint8_t* ws = static_cast<uint8_t*>(a.ws);
     SpecParams p{};
     p.importance = a.importance;
@@ -343,26 +505,23 @@ int launch_specvlm(const SpecLaunch& a, const char** why) {
     p.indices = a.indices;
     p.counts = a.counts;
     p.status = reinterpret_cast<int*>(ws);
-    p.N2 = N2;
-    p.keys_in_smem = N2 <= kSpecSmemKeys;
-    size_t off = kWsHeader;
+    p.keys_in_smem = nV <= kSpecSmemKeys;
     if (!p.keys_in_smem) {
-        p.keys_ws = reinterpret_cast<unsigned long long*>(ws + off);
-        off += align256(sizeof(unsigned long long) * static_cast<size_t>(a.B) * N2);
+        p.keys_ws = reinterpret_cast<uint32_t*>(ws + kWsHeader);
+        p.flags_ws = ws + kWsHeader + align256(sizeof(uint32_t) * static_cast<size_t>(a.B) * nV);
     }
-    p.flags_ws = ws + off;
     dim3 grid_imp((a.n + 255) / 256, a.B);
     importance_kernel<<<grid_imp, 256, 0, a.stream>>>(a.scores, a.units, a.n, 1.0f / static_cast<float>(a.units),
                                                       a.importance);
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess) {
-        const int smem = p.keys_in_smem ? N2 * 8 : 0;
+        const int nW = (nV + 31) / 32;
+        const int smem = 4 * nW + (p.keys_in_smem ? 5 * nV : 0);   // bitmap, then keys and flags
         static unsigned long long attr_set = 0;
         int dev = 0;
         e = cudaGetDevice(&dev);
         if (e == cudaSuccess && (dev >= 64 || !(attr_set & (1ull << dev)))) {
-            e = cudaFuncSetAttribute(specvlm_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kSpecSmemKeys * 8);
+            e = cudaFuncSetAttribute(specvlm_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSpecSmemMax);
             if (e == cudaSuccess && dev < 64) attr_set |= (1ull << dev);
         }
         if (e == cudaSuccess) {
