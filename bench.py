@@ -533,11 +533,13 @@ def next_rows_timings(path, hbm_peak, dev):
     ws_de = sk.new_workspace(sk.workspace_size(sk.OP_DENSE_VERIFY, vw.batch, vw.hq, vw.hkv, vw.d, vw.n + gam, gam),
                              dev)
 
+    q_step = [lay["q_ver"][:, :, t].contiguous() for t in range(gam)]   # each draft step's query
+
     def round_():
         for t in range(gam):
             sk.append_drafts(base_o, base_i, BHv * kh, vw.n, t + 1, offsets=d_offs[t], indices=d_idx[t])
-            sk.sparse_decode_attn(lay["q_ver"][:, :, t].contiguous(), lay["k"], lay["v"], d_offs[t], d_idx[t], vs,
-                                  o=o_d, ws=ws_sp, want_lse=False)
+            sk.sparse_decode_attn(q_step[t], lay["k"], lay["v"], d_offs[t], d_idx[t], vs, o=o_d, ws=ws_sp,
+                                  want_lse=False)
         sk.dense_verify_attn(lay["q_ver"], lay["k"], lay["v"], vw.n, vs, o=o_v, ws=ws_de, want_lse=False)
     t_round = time_graph_us(round_, flush=flush)
     out["f4_std_round"] = {"us_per_layer": t_round, "us_per_step_all_layers": t_round * vw.layers, "gamma": gam,

@@ -19,6 +19,8 @@ namespace sdkv {
 
 // ============================================================================ lists
 __global__ void window_lists_kernel(int BH, int n, int n_sink, int n_recent, int k, int* offsets, int* indices) {
+    griddep_wait();   // the lists may still be read by the previous kernel
+    griddep_launch();
     const long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int s1 = min(n_sink, n);
     const int w0 = max(n - n_recent, s1);
@@ -31,6 +33,8 @@ __global__ void window_lists_kernel(int BH, int n, int n_sink, int n_recent, int
 
 __global__ void append_drafts_kernel(const int* base_offsets, const int* base_indices, int BH, int n_pos, int n_new,
                                      int* offsets, int* indices) {
+    griddep_wait();   // the base lists come from, and the new ones may be read by, earlier kernels
+    griddep_launch();
     const int i = blockIdx.x;
     if (i >= BH) return;
     const int b0 = base_offsets[0];
@@ -438,8 +442,8 @@ int launch_window_lists(int B, int Hkv, int n, int n_sink, int n_recent, int* of
     const int k = std::min(n, n_sink + n_recent);
     const long long work = std::max<long long>(static_cast<long long>(BH) * k, BH + 1);
     const int grid = static_cast<int>((work + 255) / 256);
-    window_lists_kernel<<<grid, 256, 0, st>>>(BH, n, n_sink, n_recent, k, offsets, indices);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_pdl(window_lists_kernel, dim3(grid), dim3(256), 0, st, BH, n, n_sink, n_recent, k,
+                                     offsets, indices);
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);
         return SDKV_ERR_CUDA;
@@ -449,8 +453,8 @@ int launch_window_lists(int B, int Hkv, int n, int n_sink, int n_recent, int* of
 
 int launch_append_drafts(const int* base_offsets, const int* base_indices, int BH, int n_pos, int n_new,
                          int* offsets, int* indices, cudaStream_t st, const char** why) {
-    append_drafts_kernel<<<BH, 128, 0, st>>>(base_offsets, base_indices, BH, n_pos, n_new, offsets, indices);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_pdl(append_drafts_kernel, dim3(BH), dim3(128), 0, st, base_offsets, base_indices, BH,
+                                     n_pos, n_new, offsets, indices);
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);
         return SDKV_ERR_CUDA;
