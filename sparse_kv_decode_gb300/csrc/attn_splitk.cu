@@ -140,6 +140,23 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, KIND>::NT)
     __shared__ int s_abort;
     __shared__ int s_last;
 
+    if constexpr (!SPARSE) {
+        // dense: the work item is known from the grid alone, so the first stages'
+        // K and V tiles go to L2 while the previous kernel finishes
+        if (tid == 0) {
+            const int bh = blockIdx.x / p.nsplit, sp = blockIdx.x % p.nsplit;
+            const int b = bh / p.Hkv, h = bh - (bh / p.Hkv) * p.Hkv;
+            const int lo = sp * p.chunk, hi = min(lo + p.chunk, p.n_total);
+            prefetch_tmap(&tmk);
+            prefetch_tmap(&tmv);
+            for (int t = 0; t < STAGES && lo + t * TK < hi; ++t)
+#pragma unroll
+                for (int half = 0; half < D / 64; ++half) {
+                    tma_prefetch_4d(&tmk, half * 64, lo + t * TK, h, b);
+                    tma_prefetch_4d(&tmv, half * 64, lo + t * TK, h, b);
+                }
+        }
+    }
     griddep_wait();
 
     if constexpr (!SPARSE) {

@@ -96,6 +96,18 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
     const int ntiles = (hi - lo + C::TK - 1) / C::TK;
     const int row_base = mg * C::ROWS;   // first window row (of R = G * W) of this CTA
 
+    if (tid == 0) {
+        // the first stages' K tiles and this CTA's window rows into L2 while the
+        // previous kernel finishes
+        prefetch_tmap(&tmk);
+        prefetch_tmap(&tmq);
+        for (int t = 0; t < C::STAGES && t < ntiles; ++t)
+#pragma unroll
+            for (int hf = 0; hf < C::HALVES; ++hf) tma_prefetch_4d(&tmk, hf * 64, lo + t * C::TK, h, b);
+#pragma unroll
+        for (int hf = 0; hf < C::HALVES; ++hf)
+            tma_prefetch_2d(&tmq, hf * 64, (b * p.Hq + h * p.G) * p.W + row_base);
+    }
     griddep_wait();
     if (tid == 0) {
 #pragma unroll
