@@ -396,10 +396,48 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
                 named_bar_sync(1, C::NET);
                 if (s_last) {
                     __threadfence();
-                    for (int key = lo + et; key < hi; key += C::NET) {
+                    // each key's row-block partials added in row-block order; four keys
+                    // per step (16-byte loads where rows are aligned) and eight row
+                    // blocks' loads in flight
+                    const bool vec = (p.n % 4) == 0 && (reinterpret_cast<uintptr_t>(p.scores) & 15) == 0;
+                    const int k4 = vec ? (hi - lo) / 4 : 0;
+                    for (int q = et; q < k4; q += C::NET) {
+                        const int key = lo + 4 * q;
+                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int g0 = 0; g0 < p.n_mg; g0 += 8) {
+                            float4 v4[8];
+#pragma unroll
+                            for (int u = 0; u < 8; ++u)
+                                v4[u] = (g0 + u < p.n_mg)
+                                            ? __ldcg(reinterpret_cast<const float4*>(
+                                                  p.sc_part + (static_cast<size_t>(g0 + u) * p.BH + bh) * p.n + key))
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) {
+                                if (g0 + u < p.n_mg) {
+                                    acc.x += v4[u].x;
+                                    acc.y += v4[u].y;
+                                    acc.z += v4[u].z;
+                                    acc.w += v4[u].w;
+                                }
+                            }
+                        }
+                        *reinterpret_cast<float4*>(p.scores + static_cast<size_t>(bh) * p.n + key) =
+                            make_float4(acc.x * p.inv_w, acc.y * p.inv_w, acc.z * p.inv_w, acc.w * p.inv_w);
+                    }
+                    for (int key = lo + 4 * k4 + et; key < hi; key += C::NET) {
                         float v2 = 0.f;
-                        for (int g2 = 0; g2 < p.n_mg; ++g2)
-                            v2 += __ldcg(p.sc_part + (static_cast<size_t>(g2) * p.BH + bh) * p.n + key);
+                        for (int g0 = 0; g0 < p.n_mg; g0 += 8) {
+                            float v1[8];
+#pragma unroll
+                            for (int u = 0; u < 8; ++u)
+                                v1[u] = (g0 + u < p.n_mg)
+                                            ? __ldcg(p.sc_part + (static_cast<size_t>(g0 + u) * p.BH + bh) * p.n + key)
+                                            : 0.f;
+#pragma unroll
+                            for (int u = 0; u < 8; ++u)
+                                if (g0 + u < p.n_mg) v2 += v1[u];
+                        }
                         p.scores[static_cast<size_t>(bh) * p.n + key] = v2 * p.inv_w;
                     }
                     if (et == 0) atomicExch(p.tick2 + bh * p.nsplit + sp, 0);
@@ -441,7 +479,10 @@ ScorePlan score_plan(int B, int Hq, int Hkv, int n, int W, int num_sms) {
     constexpr int ROWS = 128, TK = 128;
     pl.n_mg = (R + ROWS - 1) / ROWS;
     const int target = std::max(num_sms, 1);   // one CTA per SM (tensor memory + 130 KB of stages)
-    int nsplit = std::max(1, (target + BH * pl.n_mg - 1) / (BH * pl.n_mg));
+    // splits per (sequence, KV head, row block): as many as fit one wave; a
+    // second wave would double the time for the few CTAs that spill into it
+    const int units = BH * pl.n_mg;
+    int nsplit = units >= target ? 1 : target / units;
     nsplit = std::min(nsplit, std::max(1, (n + TK - 1) / TK));
     int chunk = (n + nsplit - 1) / nsplit;
     chunk = ((chunk + TK - 1) / TK) * TK;

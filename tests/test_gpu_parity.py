@@ -222,6 +222,7 @@ def test_sparse_bad_index_is_flagged_not_faulted():
     (2, 8, 4, 128, 777, 16, 700),        # window not at the end: later keys unseen
     (1, 28, 4, 128, 1300, 40, 1260),     # group 7 x window 40 = 280 rows: three row blocks
     (1, 4, 1, 64, 200, 64, 136),         # 256 rows: two full row blocks
+    (1, 8, 2, 64, 1001, 48, 950),        # 192 rows: two row blocks, odd key count (unaligned rows)
 ])
 def test_score_matches_oracle(B, Hq, Hkv, d, n, W, q_pos0):
     g = torch.Generator().manual_seed(n + W)
