@@ -277,8 +277,10 @@ int sdkv_select_topk(const float* scores, int32_t B, int32_t Hkv, int32_t n, int
     if (static_cast<int64_t>(B) * Hkv > 0x7fffffff) return fail(SDKV_ERR_INVALID_ARG, "too many heads");
     int rc = check_ws(ws, ws_bytes, select_ws_bytes(B, Hkv, n));
     if (rc) return rc;
+    const DeviceInfo dev = current_device();
+    if (dev.num_sms <= 0) return fail(SDKV_ERR_CUDA, "no CUDA device");
     SelectLaunch a{scores, B, Hkv, n, cand_lo, cand_hi, n_sink, n_recent, offsets, indices, ws,
-                   static_cast<cudaStream_t>(stream)};
+                   static_cast<cudaStream_t>(stream), dev.num_sms};
     const char* why = "";
     rc = launch_select(a, &why);
     if (rc) return fail(rc, why);

@@ -76,6 +76,7 @@ struct SelectLaunch {
     int32_t* indices;
     void* ws;
     cudaStream_t stream;
+    int num_sms;
 };
 size_t select_ws_bytes(int B, int Hkv, int n);
 int launch_select(const SelectLaunch& a, const char** why);

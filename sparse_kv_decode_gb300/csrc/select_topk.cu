@@ -26,15 +26,18 @@ namespace sdkv {
 
 namespace {
 
-constexpr int kCS = 8;                          // CTAs per head (portable cluster size)
+constexpr int kMaxCS = 8;                       // CTAs per head at most (portable cluster size)
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kPasses = 4;                      // 8-bit digits of a 32-bit key
 constexpr int kSelKeysPerCta = 32 * 1024;       // shared-memory keys per CTA
-constexpr int kOffHist = kSelKeysPerCta * 4;                          // [2][256] this CTA's histogram
-constexpr int kOffRecv = kOffHist + 2 * 256 * 4;                      // [pass][rank][256] every CTA's
-constexpr int kOffTot = kOffRecv + kPasses * kCS * 256 * 4;           // [256] cluster histogram
-constexpr int kSelSmem = kOffTot + 256 * 4;
+template <int CS>
+struct SelCfg {
+    static constexpr int OFF_HIST = kSelKeysPerCta * 4;                 // [2][256] this CTA's histogram
+    static constexpr int OFF_RECV = OFF_HIST + 2 * 256 * 4;             // [pass][rank][256] every CTA's
+    static constexpr int OFF_TOT = OFF_RECV + kPasses * CS * 256 * 4;   // [256] cluster histogram
+    static constexpr int SMEM = OFF_TOT + 256 * 4;
+};
 
 // Order-preserving image of an fp32 score: larger score -> larger key;
 // -0.0 equals +0.0; NaN maps to 0, below every number.
@@ -73,19 +76,21 @@ __device__ __forceinline__ unsigned warp_excl_scan_u32(unsigned v, int lane) {
     return incl - v;
 }
 
-__global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kSelThreads, 1)
+template <int CS>
+__global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kSelThreads, 1)
     select_topk_kernel(const float* __restrict__ scores, int n, int cand_lo, int cand_hi, int n_sink,
                        int n_recent, const int* __restrict__ offsets, int* __restrict__ indices, int* status) {
     extern __shared__ __align__(16) uint8_t smem[];
     uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
-    unsigned* hist = reinterpret_cast<unsigned*>(smem + kOffHist);   // [pass & 1][256]
-    unsigned* recv = reinterpret_cast<unsigned*>(smem + kOffRecv);   // [pass][rank][256]
-    unsigned* tot = reinterpret_cast<unsigned*>(smem + kOffTot);
+    using C = SelCfg<CS>;
+    unsigned* hist = reinterpret_cast<unsigned*>(smem + C::OFF_HIST);   // [pass & 1][256]
+    unsigned* recv = reinterpret_cast<unsigned*>(smem + C::OFF_RECV);   // [pass][rank][256]
+    unsigned* tot = reinterpret_cast<unsigned*>(smem + C::OFF_TOT);
     __shared__ unsigned s_digit[kPasses], s_gt;
     __shared__ unsigned s_rgt[kSelWarps];   // warp w: keys of rank w/2 above the digits of passes 2(w%2), +1
     __shared__ unsigned s_wgt[kSelWarps], s_weq[kSelWarps], s_pos[kSelWarps], s_eqt[kSelWarps];
 
-    const int bh = blockIdx.x / kCS;
+    const int bh = blockIdx.x / CS;
     const int rank = static_cast<int>(cluster_ctarank());
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     griddep_wait();
@@ -94,7 +99,7 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kSelThreads, 1)
     // this CTA's candidates; their first scores are requested before the list
     // sizes so that the two reads overlap
     const int ncand = cand_hi - cand_lo;
-    const int seg = ((ncand + kCS - 1) / kCS + 31) & ~31;
+    const int seg = ((ncand + CS - 1) / CS + 31) & ~31;
     const int c0 = min(rank * seg, ncand), c1 = min(c0 + seg, ncand);
     const int len = c1 - c0;
     const float* sc = scores + static_cast<size_t>(bh) * n + cand_lo + c0;
@@ -126,7 +131,7 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kSelThreads, 1)
     }
     // a peer's shared memory may be written only once that peer has started:
     // arrive now, wait before the first store into a peer
-    cluster_arrive_relaxed();
+    if constexpr (CS > 1) cluster_arrive_relaxed();
 #pragma unroll
     for (int u = 0; u < kInFlight; ++u) {
         const int i = tid + u * kSelThreads;
@@ -160,21 +165,30 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kSelThreads, 1)
             if ((u & pmask) == prefix) atomicAdd(&h[(u >> sh) & 0xffu], 1u);
         }
         __syncthreads();
-        if (pass == 0) cluster_wait();   // every CTA of the cluster is running
+        if constexpr (CS > 1) {
+            if (pass == 0) cluster_wait();   // every CTA of the cluster is running
+        }
         if (tid < 256) {
             // this CTA's histogram into slot [pass][rank] of every CTA of the cluster
             const unsigned c = h[tid];
-            const uint32_t a = smem_u32(recv + (pass * kCS + rank) * 256 + tid);
+            if constexpr (CS > 1) {
+                const uint32_t a = smem_u32(recv + (pass * CS + rank) * 256 + tid);
 #pragma unroll
-            for (int r = 0; r < kCS; ++r) st_dsmem_u32(dsmem_addr(a, r), c);
+                for (int r = 0; r < CS; ++r) st_dsmem_u32(dsmem_addr(a, r), c);
+            } else {
+                recv[pass * 256 + tid] = c;
+            }
         } else {
             hist[((pass + 1) & 1) * 256 + (tid - 256)] = 0u;   // the next pass's histogram
         }
-        cluster_sync_all();   // every CTA's histogram of this pass has arrived everywhere
+        if constexpr (CS > 1)
+            cluster_sync_all();   // every CTA's histogram of this pass has arrived everywhere
+        else
+            __syncthreads();
         if (tid < 256) {
             unsigned c = 0;
 #pragma unroll
-            for (int r = 0; r < kCS; ++r) c += recv[(pass * kCS + r) * 256 + tid];
+            for (int r = 0; r < CS; ++r) c += recv[(pass * CS + r) * 256 + tid];
             tot[tid] = c;
         }
         __syncthreads();
@@ -212,8 +226,9 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kSelThreads, 1)
         unsigned g = 0;
 #pragma unroll
         for (int pp = p0; pp < p0 + 2; ++pp) {
+            if (r >= CS) break;
             const unsigned dig = s_digit[pp];
-            const unsigned* hr = recv + (pp * kCS + r) * 256;
+            const unsigned* hr = recv + (pp * CS + r) * 256;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const unsigned d = lane + 32 * j;   // consecutive lanes, consecutive banks
@@ -242,11 +257,11 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kSelThreads, 1)
     __syncthreads();
     if (tid == 0) {
         // the CTAs of lower rank hold the earlier candidates, then the warps of
-        // this CTA in order (a short serial walk: at most kCS + kSelWarps steps)
+        // this CTA in order (a short serial walk: at most CS + kSelWarps steps)
         unsigned eq_before = 0, kept_before = 0;
         for (int r = 0; r < rank; ++r) {
             const unsigned g = s_rgt[2 * r] + s_rgt[2 * r + 1];
-            const unsigned e = recv[((kPasses - 1) * kCS + r) * 256 + s_digit[kPasses - 1]];
+            const unsigned e = recv[((kPasses - 1) * CS + r) * 256 + s_digit[kPasses - 1]];
             const unsigned take = (need_eq > eq_before) ? min(e, need_eq - eq_before) : 0u;
             kept_before += g + take;
             eq_before += e;
@@ -289,34 +304,48 @@ size_t select_ws_bytes(int B, int Hkv, int n) {
     return kWsHeader;
 }
 
+namespace {
+
+// CTAs per head: 8 while every head's cluster fits the GPU at once; with more
+// heads, fewer per head (down to 1, one CTA and no cluster) so that all heads
+// run in about one wave, as long as a CTA's share fits its shared memory.
+int select_cluster_size(int BH, int ncand, int num_sms) {
+    int cs = kMaxCS;
+    while (cs > 1 && static_cast<long long>(BH) * cs > num_sms && (ncand + cs / 2 - 1) / (cs / 2) <= kSelKeysPerCta)
+        cs /= 2;
+    return cs;
+}
+
+template <int CS>
+cudaError_t launch_select_cs(const SelectLaunch& a) {
+    using C = SelCfg<CS>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    static unsigned long long attr_set = 0;   // one bit per device, per instantiation
+    if (e == cudaSuccess && (dev >= 64 || !(attr_set & (1ull << dev)))) {
+        e = cudaFuncSetAttribute(select_topk_kernel<CS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e == cudaSuccess && dev < 64) attr_set |= (1ull << dev);
+    }
+    if (e != cudaSuccess) return e;
+    return launch_pdl(select_topk_kernel<CS>, dim3(a.B * a.Hkv * CS), dim3(kSelThreads), C::SMEM, a.stream, a.scores,
+                      a.n, a.cand_lo, a.cand_hi, a.n_sink, a.n_recent, a.offsets, a.indices, static_cast<int*>(a.ws));
+}
+
+}  // namespace
+
 int launch_select(const SelectLaunch& a, const char** why) {
-    if (a.cand_hi - a.cand_lo > kCS * kSelKeysPerCta) {
+    const int ncand = a.cand_hi - a.cand_lo;
+    if (ncand > kMaxCS * kSelKeysPerCta) {
         *why = "more than 262144 candidates per head";
         return SDKV_ERR_UNSUPPORTED;
     }
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    static unsigned long long attr_set = 0;
-    if (e == cudaSuccess && (dev >= 64 || !(attr_set & (1ull << dev)))) {
-        e = cudaFuncSetAttribute(select_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelSmem);
-        if (e == cudaSuccess && dev < 64) attr_set |= (1ull << dev);
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (select_cluster_size(a.B * a.Hkv, ncand, std::max(a.num_sms, 1))) {
+        case 1: e = launch_select_cs<1>(a); break;
+        case 2: e = launch_select_cs<2>(a); break;
+        case 4: e = launch_select_cs<4>(a); break;
+        default: e = launch_select_cs<8>(a); break;
     }
-    if (e != cudaSuccess) {
-        *why = cudaGetErrorString(e);
-        return SDKV_ERR_CUDA;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.B * a.Hkv * kCS);
-    cfg.blockDim = dim3(kSelThreads);
-    cfg.dynamicSmemBytes = kSelSmem;
-    cfg.stream = a.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, select_topk_kernel, a.scores, a.n, a.cand_lo, a.cand_hi, a.n_sink, a.n_recent,
-                           a.offsets, a.indices, static_cast<int*>(a.ws));
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);
         return SDKV_ERR_CUDA;

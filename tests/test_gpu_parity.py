@@ -271,6 +271,23 @@ def test_select_exact_on_same_scores(n, cand_lo, cand_hi, n_sink, n_recent, K):
     assert np.array_equal(idx.cpu().numpy()[: len(want)], want)
 
 
+@pytest.mark.parametrize("B,Hkv", [(4, 8), (8, 8), (16, 8)])
+def test_select_many_heads(B, Hkv):
+    # 32, 64 and 128 heads: fewer CTAs per head (4, 2, 1) so that all heads run at once
+    rng = np.random.default_rng(B * Hkv)
+    n, cand_lo, n_recent = 3000, 4, 64
+    cand_hi = n - n_recent
+    sc = rng.lognormal(0, 2, (B, Hkv, n)).astype(np.float32)
+    sc[0, 0] = np.round(sc[0, 0] * 2) / 2            # ties
+    sc[1, 3, ::3] = 0.0
+    sc[B - 1, Hkv - 1, ::11] = np.nan
+    lens = [4 + int(k) + n_recent for k in rng.integers(0, cand_hi - cand_lo + 1, B * Hkv)]
+    offs_d, offs = csr(lens, DEV)
+    idx = sk.select_topk(torch.from_numpy(sc).to(DEV), n, cand_lo, cand_hi, 4, n_recent, offs_d, int(offs[-1]))
+    want = oracle.select_topk(sc, n, cand_lo, cand_hi, 4, n_recent, offs)
+    assert np.array_equal(idx.cpu().numpy(), want)
+
+
 def test_select_ragged_budgets_and_bad_list():
     rng = np.random.default_rng(1)
     B, Hkv, n = 1, 5, 4000
