@@ -554,8 +554,8 @@ def next_rows_timings(path, hbm_peak, dev):
     base_o = torch.arange(BHv + 1, dtype=torch.int32, device=dev) * kh
     sc = sk.score_obs_window(lay["q_obs"][:, :, : vw.text_tokens].contiguous(), lay["k"], vw.n, vw.q_pos0, vs)
     base_i = sk.select_topk(sc, vw.n, vw.cand_lo, vw.cand_hi, vw.n_sink, vw.n_recent, base_o, BHv * kh)
-    d_offs = [torch.empty(BHv + 1, dtype=torch.int32, device=dev) for _ in range(gam)]
-    d_idx = [torch.empty(BHv * (kh + t + 1), dtype=torch.int32, device=dev) for t in range(gam)]
+    d_offs = torch.empty((gam, BHv + 1), dtype=torch.int32, device=dev)
+    d_idx = torch.empty((gam, BHv * (kh + gam)), dtype=torch.int32, device=dev)
     o_d = torch.empty((vw.batch, vw.hq, vw.d), dtype=torch.bfloat16, device=dev)
     o_v = torch.empty((vw.batch, vw.hq, gam, vw.d), dtype=torch.bfloat16, device=dev)
     ws_sp = sk.new_workspace(sk.workspace_size(sk.OP_SPARSE_DECODE, vw.batch, vw.hq, vw.hkv, vw.d, 0, 0), dev)
@@ -565,14 +565,15 @@ def next_rows_timings(path, hbm_peak, dev):
     q_step = [lay["q_ver"][:, :, t].contiguous() for t in range(gam)]   # each draft step's query
 
     def round_():
+        # every draft step's list (base + the drafted positions so far) in one launch
+        sk.draft_lists(base_o, base_i, BHv * kh, vw.n, gam, offsets=d_offs, indices=d_idx)
         for t in range(gam):
-            sk.append_drafts(base_o, base_i, BHv * kh, vw.n, t + 1, offsets=d_offs[t], indices=d_idx[t])
             sk.sparse_decode_attn(q_step[t], lay["k"], lay["v"], d_offs[t], d_idx[t], vs, o=o_d, ws=ws_sp,
                                   want_lse=False)
         sk.dense_verify_attn(lay["q_ver"], lay["k"], lay["v"], vw.n, vs, o=o_v, ws=ws_de, want_lse=False)
     t_round = time_graph_us(round_, flush=flush)
     out["f4_std_round"] = {"us_per_layer": t_round, "us_per_step_all_layers": t_round * vw.layers, "gamma": gam,
-                           "kept_per_head": kh, "launches_per_layer": 2 * gam + 1}
+                           "kept_per_head": kh, "launches_per_layer": gam + 2}
     return out
 
 

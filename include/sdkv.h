@@ -290,6 +290,22 @@ int sdkv_append_drafts(const int32_t* base_offsets, const int32_t* base_indices,
                        void* stream);
 
 /*
+ * All draft-step lists of one StD round in one launch.  [StD] 3.1: draft step
+ * t = 0 .. gamma - 1 attends the base selection plus n_pos .. n_pos + t.  Set
+ * t is exactly what sdkv_append_drafts writes with n_new = t + 1:
+ *   offsets  device int32[gamma][BH + 1]; set t at offsets + t * (BH + 1)
+ *   indices  device int32[gamma][stride]; set t at indices + t * stride, with
+ *            stride >= (base_offsets[BH] - base_offsets[0]) + BH * gamma
+ *            (entries at or past stride are not written)
+ *   base_*   device CSR of BH lists, entries below n_pos; outputs must not
+ *            alias them
+ * Asynchronous on `stream`; no workspace.  One launch replaces gamma calls of
+ * sdkv_append_drafts.
+ */
+int sdkv_draft_lists(const int32_t* base_offsets, const int32_t* base_indices, int32_t BH, int32_t n_pos,
+                     int32_t gamma, int64_t stride, int32_t* offsets, int32_t* indices, void* stream);
+
+/*
  * Contiguous compaction of the selected rows.  [ByteCross] "Speedup Across
  * Context": after selection the kept entries are gathered into a contiguous
  * buffer that every later step reads in one kernel call.  Row

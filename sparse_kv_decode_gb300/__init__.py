@@ -24,6 +24,7 @@ from ._lib import (  # noqa: F401
     workspace_status,
     window_lists,
     append_drafts,
+    draft_lists,
     compact_kv,
     sparse_decode_compact,
     specvlm_select,

@@ -89,6 +89,8 @@ def lib() -> ctypes.CDLL:
     L.sdkv_window_lists.restype = ctypes.c_int
     L.sdkv_append_drafts.argtypes = [_c_vp, _c_vp, _c_i32, _c_i32, _c_i32, _c_vp, _c_vp, _c_vp]
     L.sdkv_append_drafts.restype = ctypes.c_int
+    L.sdkv_draft_lists.argtypes = [_c_vp, _c_vp, _c_i32, _c_i32, _c_i32, _c_i64, _c_vp, _c_vp, _c_vp]
+    L.sdkv_draft_lists.restype = ctypes.c_int
     L.sdkv_compact_kv.argtypes = [_c_vp, _c_vp, _I64x3, _c_i32, _c_vp, _c_vp, _c_i32, _c_i32, _c_i32, _c_i64,
                                   _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]
     L.sdkv_compact_kv.restype = ctypes.c_int
@@ -301,6 +303,28 @@ def append_drafts(base_offsets: torch.Tensor, base_indices: torch.Tensor, total:
         indices = torch.empty(max(total + BH * n_new, 1), dtype=torch.int32, device=base_offsets.device)
     _check(lib().sdkv_append_drafts(base_offsets.data_ptr(), base_indices.data_ptr(), BH, n_pos, n_new,
                                     offsets.data_ptr(), indices.data_ptr(), _stream(base_offsets)))
+    return offsets, indices
+
+
+def draft_lists(base_offsets: torch.Tensor, base_indices: torch.Tensor, total: int, n_pos: int, gamma: int,
+                offsets: torch.Tensor | None = None, indices: torch.Tensor | None = None):
+    """sdkv_draft_lists: the lists of draft steps 0 .. gamma-1 in one launch.
+    Returns offsets [gamma][BH + 1] and indices [gamma][stride] (set t = base
+    lists + n_pos .. n_pos + t); `total` = base_offsets[-1] - base_offsets[0]."""
+    _need(base_offsets, "base_offsets", torch.int32)
+    _need(base_indices, "base_indices", torch.int32)
+    BH = base_offsets.numel() - 1
+    stride = total + BH * gamma
+    if offsets is None:
+        offsets = torch.empty((gamma, BH + 1), dtype=torch.int32, device=base_offsets.device)
+    if indices is None:
+        indices = torch.empty((gamma, max(stride, 1)), dtype=torch.int32, device=base_offsets.device)
+    if offsets.shape != (gamma, BH + 1) or indices.dim() != 2 or indices.shape[0] != gamma:
+        raise ValueError("offsets must be [gamma][BH+1] and indices [gamma][stride]")
+    if indices.shape[1] < stride or not (offsets.is_contiguous() and indices.is_contiguous()):
+        raise ValueError("indices rows must hold total + BH * gamma entries, contiguous")
+    _check(lib().sdkv_draft_lists(base_offsets.data_ptr(), base_indices.data_ptr(), BH, n_pos, gamma,
+                                  indices.shape[1], offsets.data_ptr(), indices.data_ptr(), _stream(base_offsets)))
     return offsets, indices
 
 

@@ -48,6 +48,29 @@ __global__ void append_drafts_kernel(const int* base_offsets, const int* base_in
         indices[out0 + e] = (e < len) ? base_indices[st + e] : n_pos + (e - len);
 }
 
+// Every draft step's lists of one round: set t (grid y) is the base CSR with
+// n_pos .. n_pos + t appended to each list; entries at or past `stride` in a
+// set are not written.
+__global__ void draft_lists_kernel(const int* base_offsets, const int* base_indices, int BH, int n_pos,
+                                   long long stride, int* offsets, int* indices) {
+    griddep_wait();
+    griddep_launch();
+    const int i = blockIdx.x, t = blockIdx.y, n_new = t + 1;
+    const int b0 = base_offsets[0];
+    const int st = base_offsets[i], len = base_offsets[i + 1] - st;
+    const long long out0 = static_cast<long long>(st - b0) + static_cast<long long>(i) * n_new;
+    int* set_off = offsets + static_cast<size_t>(t) * (BH + 1);
+    int* set_idx = indices + static_cast<size_t>(t) * stride;
+    if (threadIdx.x == 0) {
+        set_off[i] = static_cast<int>(out0);
+        if (i == BH - 1) set_off[BH] = static_cast<int>(out0 + len + n_new);
+    }
+    for (int e = threadIdx.x; e < len + n_new; e += blockDim.x) {
+        const long long o = out0 + e;
+        if (o < stride) set_idx[o] = (e < len) ? base_indices[st + e] : n_pos + (e - len);
+    }
+}
+
 // ============================================================================ compaction
 // CTA c copies flat list positions [c*CH, (c+1)*CH): one warp per row, 16-byte
 // chunks, K chunks on the first D/8 lanes of a row group and V on the next.
@@ -455,6 +478,17 @@ int launch_append_drafts(const int* base_offsets, const int* base_indices, int B
                          int* offsets, int* indices, cudaStream_t st, const char** why) {
     const cudaError_t e = launch_pdl(append_drafts_kernel, dim3(BH), dim3(128), 0, st, base_offsets, base_indices, BH,
                                      n_pos, n_new, offsets, indices);
+    if (e != cudaSuccess) {
+        *why = cudaGetErrorString(e);
+        return SDKV_ERR_CUDA;
+    }
+    return SDKV_OK;
+}
+
+int launch_draft_lists(const int* base_offsets, const int* base_indices, int BH, int n_pos, int gamma,
+                       long long stride, int* offsets, int* indices, cudaStream_t st, const char** why) {
+    const cudaError_t e = launch_pdl(draft_lists_kernel, dim3(BH, gamma), dim3(128), 0, st, base_offsets, base_indices,
+                                     BH, n_pos, stride, offsets, indices);
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);
         return SDKV_ERR_CUDA;

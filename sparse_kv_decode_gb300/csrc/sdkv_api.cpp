@@ -466,6 +466,21 @@ int sdkv_append_drafts(const int32_t* base_offsets, const int32_t* base_indices,
     return SDKV_OK;
 }
 
+int sdkv_draft_lists(const int32_t* base_offsets, const int32_t* base_indices, int32_t BH, int32_t n_pos,
+                     int32_t gamma, int64_t stride, int32_t* offsets, int32_t* indices, void* stream) {
+    if (!base_offsets || !base_indices || !offsets || !indices) return fail(SDKV_ERR_INVALID_ARG, "null pointer");
+    if (BH <= 0 || n_pos < 0 || gamma <= 0 || gamma > 65535 || stride <= 0)
+        return fail(SDKV_ERR_INVALID_ARG, "need BH > 0, n_pos >= 0, 0 < gamma <= 65535, stride > 0");
+    if (offsets == base_offsets || indices == base_indices)
+        return fail(SDKV_ERR_INVALID_ARG, "output lists must not alias the base lists");
+    const char* why = "";
+    const int rc = launch_draft_lists(base_offsets, base_indices, BH, n_pos, gamma, stride, offsets, indices,
+                                      static_cast<cudaStream_t>(stream), &why);
+    if (rc) return fail(rc, why);
+    g_last_error.clear();
+    return SDKV_OK;
+}
+
 int sdkv_compact_kv(const void* k, const void* v, const int64_t kv_strides[3], int32_t n_cap,
                     const int32_t* offsets, const int32_t* indices, int32_t B, int32_t Hkv, int32_t d,
                     int64_t rows_cap, void* k_out, void* v_out, void* ws, size_t ws_bytes, void* stream) {

@@ -86,6 +86,8 @@ int launch_window_lists(int B, int Hkv, int n, int n_sink, int n_recent, int* of
                         cudaStream_t st, const char** why);
 int launch_append_drafts(const int* base_offsets, const int* base_indices, int BH, int n_pos, int n_new,
                          int* offsets, int* indices, cudaStream_t st, const char** why);
+int launch_draft_lists(const int* base_offsets, const int* base_indices, int BH, int n_pos, int gamma,
+                       long long stride, int* offsets, int* indices, cudaStream_t st, const char** why);
 struct CompactLaunch {
     const void* k;
     const void* v;

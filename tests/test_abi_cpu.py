@@ -31,7 +31,7 @@ def _declared():
 
 def test_exports_every_declared_symbol(L):
     names = _declared()
-    assert len(names) == 15, names
+    assert len(names) == 16, names
     for name in names:
         assert hasattr(L, name), name
     assert sk.version() == 100
@@ -113,6 +113,11 @@ def test_gpu_calls_reject_bad_arguments_without_launching(L):
     assert L.sdkv_select_topk(P, 1, 4, 100, 2, 99, 4, 8, P, P, P, 1 << 20, None) == _lib.SDKV_ERR_INVALID_ARG
     assert L.sdkv_select_topk(None, 1, 4, 100, 4, 90, 4, 8, P, P, P, 1 << 20, None) == _lib.SDKV_ERR_INVALID_ARG
     assert b"n_sink" in L.sdkv_last_error() or b"null" in L.sdkv_last_error()
+    # draft lists: zero gamma, outputs aliasing the base lists
+    assert L.sdkv_draft_lists(P, P, 4, 100, 0, 1000, ctypes.c_void_p(512), ctypes.c_void_p(768), None) == \
+        _lib.SDKV_ERR_INVALID_ARG
+    assert L.sdkv_draft_lists(P, ctypes.c_void_p(512), 4, 100, 2, 1000, P, ctypes.c_void_p(768), None) == \
+        _lib.SDKV_ERR_INVALID_ARG
 
 
 def test_product_path_fails_loudly_without_library(tmp_path, monkeypatch):

@@ -71,6 +71,21 @@ def test_append_drafts_exact():
         assert idx[: int(ro[-1])].cpu().numpy().tolist() == ri.tolist()
 
 
+def test_draft_lists_equal_appends():
+    rng = np.random.default_rng(35)
+    lens = [5, 0, 130, 1, 77, 1024]
+    base_o = np.concatenate([[3], 3 + np.cumsum(lens)]).astype(np.int32)
+    base_i = np.concatenate([rng.integers(0, 10000, 3)] +
+                            [np.sort(rng.choice(12000, L, replace=False)) for L in lens]).astype(np.int32)
+    bo, bi = torch.tensor(base_o, device=DEV), torch.tensor(base_i, device=DEV)
+    gamma = 5
+    offs, idx = sk.draft_lists(bo, bi, int(sum(lens)), 12000, gamma)
+    for t in range(gamma):
+        ro, ri = oracle.append_drafts(base_o, base_i, 12000, t + 1)
+        assert offs[t].cpu().numpy().tolist() == ro.tolist()
+        assert idx[t, : int(ro[-1])].cpu().numpy().tolist() == ri.tolist()
+
+
 # --------------------------------------------------------------------------- compaction + decode (f1)
 
 def _lists(B, Hkv, n, lens, seed, lead=0):
