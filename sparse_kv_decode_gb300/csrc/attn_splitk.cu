@@ -993,7 +993,7 @@ int launch_list_decode(const AttnLaunch& a, const CUtensorMap& tmk, const CUtens
     p.n_cap = a.n_cap;
     p.BH = BH;
     p.grid_target = sparse_grid_target(num_sms);
-    p.min_chunk = kSparseTK;
+    p.min_chunk = 4 * kSparseTK;   // short lists: one cluster per head, no cross-cluster merge
     p.cs = sparse_cluster(BH, p.grid_target);
     p.ncl = 1;
     const int max_chunks = sparse_max_chunks(BH, p.grid_target, p.cs);
