@@ -52,6 +52,8 @@ struct AttnParams {
 // through the index lists, or the lists' rows compacted into contiguous buffers.
 constexpr int kDense = 0, kGather = 1, kContig = 2;
 constexpr int kMaxCluster = 8;     // portable cluster size
+template <int D>
+constexpr int kLogD = (D == 128) ? 7 : 6;   // log2 of the head dim
 
 template <int D, int MT, int KW, int TK, int STAGES, int KIND>
 struct AttnCfg {
@@ -533,21 +535,23 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, KIND>::NT)
                 a4.z += v4.z;
                 a4.w += v4.w;
             }
-            const int g = row / p.gamma, tt = row - (row / p.gamma) * p.gamma;
-            const size_t orow = (static_cast<size_t>(b) * p.Hq + h * p.G + g) * p.gamma + tt;
             if (p.cs > 1) {
                 // push to the cluster CTA that owns these dims (its receive buffer is
-                // not used by the main loop, so early pushes are safe); (M, L) to all
-                const int SL = D / p.cs;
+                // not used by the main loop, so early pushes are safe); (M, L) to all.
+                // Cluster sizes are powers of two: slices by shifts.
+                const int lcs = __ffs(p.cs) - 1;
+                const int SL = D >> lcs;
                 const uint32_t me = cluster_ctarank();
-                const int owner = d0 / SL;
-                st_dsmem_f4(dsmem_addr(sbase + C::OFF_RCV + ((me * p.R + row) * SL + (d0 - owner * SL)) * 4, owner),
+                const int owner = d0 >> (kLogD<D> - lcs);
+                st_dsmem_f4(dsmem_addr(sbase + C::OFF_RCV + ((me * p.R + row) * SL + (d0 & (SL - 1))) * 4, owner),
                             a4);
                 // every lane of the row holds the same (M, L): lane d0/4 sends it to
                 // rank d0/4 (D/4 >= cluster size, so one remote store at most per lane)
                 for (int r = d0 / 4; r < p.cs; r += D / 4)
                     st_dsmem_f2(dsmem_addr(sbase + C::OFF_RML + (me * p.R + row) * 8, r), make_float2(M, L));
             } else if (nch == 1) {
+                const int g = row / p.gamma, tt = row - (row / p.gamma) * p.gamma;
+                const size_t orow = (static_cast<size_t>(b) * p.Hq + h * p.G + g) * p.gamma + tt;
                 const float il = L > 0.f ? 1.f / L : 0.f;
                 uint2 packed;
                 packed.x = pack_bf16(a4.x * il, a4.y * il);
@@ -572,16 +576,18 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, KIND>::NT)
             // head) goes to global memory.
             cluster_sync_all();
             const int CS = p.cs;
-            const int SL = D / CS;
+            const int lcs = __ffs(CS) - 1;                   // cluster sizes are powers of two
+            const int SL = D >> lcs;
             const uint32_t rank = cluster_ctarank();
-            const int sl4 = SL / 4;                          // float4 per row in this slice
-            const int gcl = cidx / CS;                       // global cluster index (partial slot)
-            const int gcl0 = c0 / CS, ncl_h = nch / CS;      // the head's clusters
+            const int lsl4 = kLogD<D> - lcs - 2;             // float4 per row in this slice: 1 << lsl4
+            const int sl4 = 1 << lsl4;
+            const int gcl = cidx >> lcs;                     // global cluster index (partial slot)
+            const int gcl0 = c0 >> lcs, ncl_h = nch >> lcs;  // the head's clusters
             const float* rcv = reinterpret_cast<const float*>(smem + C::OFF_RCV);
             const float2* rml = reinterpret_cast<const float2*>(smem + C::OFF_RML);
             for (int e = tid; e < p.R * sl4; e += C::NCT) {
-                const int row = e / sl4;
-                const int dd = 4 * (e - row * sl4);
+                const int row = e >> lsl4;
+                const int dd = 4 * (e & (sl4 - 1));
                 const int d0 = static_cast<int>(rank) * SL + dd;
                 // unrolled to the largest cluster so that all loads are in flight together
                 float2 ml2[kMaxCluster];
@@ -610,9 +616,9 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, KIND>::NT)
                     a4.z += w * v4[c].z;
                     a4.w += w * v4[c].w;
                 }
-                const int g = row / p.gamma, tt = row - (row / p.gamma) * p.gamma;
-                const size_t orow = (static_cast<size_t>(b) * p.Hq + h * p.G + g) * p.gamma + tt;
                 if (ncl_h == 1) {
+                    const int g = row / p.gamma, tt = row - (row / p.gamma) * p.gamma;
+                    const size_t orow = (static_cast<size_t>(b) * p.Hq + h * p.G + g) * p.gamma + tt;
                     const float il = L > 0.f ? 1.f / L : 0.f;
                     uint2 packed;
                     packed.x = pack_bf16(a4.x * il, a4.y * il);
@@ -638,8 +644,8 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, KIND>::NT)
             if (!s_last) return;
             // last cluster of the head for this slice: merge the head's cluster partials
             for (int e = tid; e < p.R * sl4; e += C::NCT) {
-                const int row = e / sl4;
-                const int d0 = static_cast<int>(rank) * (D / CS) + 4 * (e - row * sl4);
+                const int row = e >> lsl4;
+                const int d0 = static_cast<int>(rank) * SL + 4 * (e & (sl4 - 1));
                 float mm = -INFINITY, ll = 0.f;
                 float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
                 for (int cb = 0; cb < ncl_h; cb += 8) {
