@@ -180,14 +180,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
-// ---- bulk and tensor copies (global -> shared, completion on an mbarrier) -----
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
 
+// ---- tensor copies (global -> shared, completion on an mbarrier) ---------------
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
                                             int c3, uint32_t bar) {
     asm volatile(
@@ -201,19 +195,10 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-// Same copy with a source size of zero: nothing is read, the 16 bytes are zeros.
-__device__ __forceinline__ void cp_async_16_zero(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, 0;" ::"r"(dst), "l"(src) : "memory");
-}
 // GPU-scope acquire-release fence: with a CTA barrier before it, it publishes the
 // CTA's earlier global writes ahead of a following relaxed atomic (release side),
 // and after an atomic it orders the later reads behind it (acquire side).
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
-__device__ __forceinline__ int ld_acquire_gpu(const int* ptr) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
-    return v;
-}
 // The mbarrier receives one arrival once every cp.async this thread issued so
 // far has landed (the arrival is counted in the barrier's expected count).
 __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
@@ -333,19 +318,6 @@ __device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, uint32_t rank) {
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
     return r;
-}
-__device__ __forceinline__ float2 ld_dsmem_f2(uint32_t addr) {
-    float2 v;
-    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
-    return v;
-}
-__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
 }
 
 __device__ __forceinline__ void st_dsmem_f4(uint32_t addr, float4 v) {
