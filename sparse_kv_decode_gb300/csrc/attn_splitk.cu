@@ -159,6 +159,16 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, KIND>::NT)
                 }
         }
     }
+    if (tid == 0) {
+        // this CTA's own barriers: independent of the previous kernel
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, KIND == kGather ? C::NPW * 32 : 1);
+            mbar_init(bar_empty + 8 * s, C::NCW);
+        }
+        fence_mbar_init();
+        s_abort = 0;
+    }
     griddep_wait();
 
     if constexpr (!SPARSE) {
@@ -178,69 +188,114 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, KIND>::NT)
         // length cl; with clusters of cs CTAs it owns cs * ceil(k_i / (cs * cl))
         // chunks (a whole number of clusters) of balanced length; trailing ones
         // may be empty.  Either way the chunk count stays within the grid.
-        int start = 0, kh = 0;
-        if (tid < p.BH) {
-            start = p.offsets[tid];
-            kh = p.offsets[tid + 1] - start;
-        }
-        if (tid == 0) {
-            s_off0 = p.offsets[0];
-            s_tot = p.offsets[p.BH] - s_off0;
-            s_work[0] = -1;
-        }
-        __syncthreads();
-        const int total = max(s_tot, 0);
-        const int cs = p.cs;
-        const int slots = max(1, p.grid_target - (cs > 1 ? cs * p.BH : 0));
-        int cl = (total + slots - 1) / slots;
-        cl = max(p.min_chunk, (cl + 15) & ~15);
-        const int c = blockIdx.x;
-        int running = 0;
-        for (int base = 0; base < p.BH; base += C::NT) {
-            const int i = base + tid;
-            int nch = 0, chl = cl;
-            if (base > 0 && i < p.BH) {
-                start = p.offsets[i];
-                kh = p.offsets[i + 1] - start;
-            }
-            if (i < p.BH) {
-                if (kh < 0) {
-                    flag_status(p.status, SDKV_DEV_BAD_LIST);
-                    kh = 0;
+        if (p.BH <= 32) {
+            // one warp: each lane a head, the chunk ids by a shuffle scan
+            if (warp == 0) {
+                int start = 0, kh = 0;
+                if (lane < p.BH) {
+                    start = p.offsets[lane];
+                    kh = p.offsets[lane + 1] - start;
                 }
-                if (cs > 1) {
-                    nch = cs * max(1, (kh + cs * cl - 1) / (cs * cl));
-                    chl = (((kh + nch - 1) / nch) + 15) & ~15;
-                } else {
-                    nch = max(1, (kh + cl - 1) / cl);
+                const int off0 = __shfl_sync(0xffffffffu, start, 0);
+                const int total = max(__shfl_sync(0xffffffffu, start + kh, p.BH - 1) - off0, 0);
+                const int cs = p.cs;
+                const int slots = max(1, p.grid_target - (cs > 1 ? cs * p.BH : 0));
+                int cl = (total + slots - 1) / slots;
+                cl = max(p.min_chunk, (cl + 15) & ~15);
+                int nch = 0, chl = cl;
+                if (lane < p.BH) {
+                    if (kh < 0) {
+                        flag_status(p.status, SDKV_DEV_BAD_LIST);
+                        kh = 0;
+                    }
+                    if (cs > 1) {
+                        nch = cs * max(1, (kh + cs * cl - 1) / (cs * cl));
+                        chl = (((kh + nch - 1) / nch) + 15) & ~15;
+                    } else {
+                        nch = max(1, (kh + cl - 1) / cl);
+                    }
                 }
-            }
-            int tile_total;
-            const int excl = block_excl_scan<C::NT>(nch, s_scan, tile_total);
-            const int first = running + excl;
-            if (i < p.BH && c >= first && c < first + nch) {
-                const int j = c - first;
-                const int l0 = min(start + j * chl, start + kh);
-                s_work[0] = i;
-                s_work[1] = l0;
-                s_work[2] = max(l0, min(start + (j + 1) * chl, start + kh));
-                s_work[3] = c;
-                s_work[4] = nch;
-                s_work[5] = first;
-            }
-            running += tile_total;
-            __syncthreads();
-            if (s_work[0] >= 0 || running > c) break;
-        }
-    }
-    if (tid == 0) {
+                int incl = nch;
 #pragma unroll
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar_full + 8 * s, KIND == kGather ? C::NPW * 32 : 1);
-            mbar_init(bar_empty + 8 * s, C::NCW);
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const int first = incl - nch;
+                const int c = blockIdx.x;
+                const bool mine = lane < p.BH && c >= first && c < first + nch;
+                if (mine) {
+                    const int j = c - first;
+                    const int l0 = min(start + j * chl, start + kh);
+                    s_work[0] = lane;
+                    s_work[1] = l0;
+                    s_work[2] = max(l0, min(start + (j + 1) * chl, start + kh));
+                    s_work[3] = c;
+                    s_work[4] = nch;
+                    s_work[5] = first;
+                }
+                if (__ballot_sync(0xffffffffu, mine) == 0u && lane == 0) s_work[0] = -1;
+                if (lane == 0) {
+                    s_off0 = off0;
+                    s_tot = total;
+                }
+            }
+        } else {
+            int start = 0, kh = 0;
+            if (tid < p.BH) {
+                start = p.offsets[tid];
+                kh = p.offsets[tid + 1] - start;
+            }
+            if (tid == 0) {
+                s_off0 = p.offsets[0];
+                s_tot = p.offsets[p.BH] - s_off0;
+                s_work[0] = -1;
+            }
+            __syncthreads();
+            const int total = max(s_tot, 0);
+            const int cs = p.cs;
+            const int slots = max(1, p.grid_target - (cs > 1 ? cs * p.BH : 0));
+            int cl = (total + slots - 1) / slots;
+            cl = max(p.min_chunk, (cl + 15) & ~15);
+            const int c = blockIdx.x;
+            int running = 0;
+            for (int base = 0; base < p.BH; base += C::NT) {
+                const int i = base + tid;
+                int nch = 0, chl = cl;
+                if (base > 0 && i < p.BH) {
+                    start = p.offsets[i];
+                    kh = p.offsets[i + 1] - start;
+                }
+                if (i < p.BH) {
+                    if (kh < 0) {
+                        flag_status(p.status, SDKV_DEV_BAD_LIST);
+                        kh = 0;
+                    }
+                    if (cs > 1) {
+                        nch = cs * max(1, (kh + cs * cl - 1) / (cs * cl));
+                        chl = (((kh + nch - 1) / nch) + 15) & ~15;
+                    } else {
+                        nch = max(1, (kh + cl - 1) / cl);
+                    }
+                }
+                int tile_total;
+                const int excl = block_excl_scan<C::NT>(nch, s_scan, tile_total);
+                const int first = running + excl;
+                if (i < p.BH && c >= first && c < first + nch) {
+                    const int j = c - first;
+                    const int l0 = min(start + j * chl, start + kh);
+                    s_work[0] = i;
+                    s_work[1] = l0;
+                    s_work[2] = max(l0, min(start + (j + 1) * chl, start + kh));
+                    s_work[3] = c;
+                    s_work[4] = nch;
+                    s_work[5] = first;
+                }
+                running += tile_total;
+                __syncthreads();
+                if (s_work[0] >= 0 || running > c) break;
+            }
         }
-        fence_mbar_init();
-        s_abort = 0;
     }
     __syncthreads();
     griddep_launch();
