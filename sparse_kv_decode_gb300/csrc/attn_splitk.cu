@@ -169,9 +169,8 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, KIND>::NT)
         fence_mbar_init();
         s_abort = 0;
     }
-    griddep_wait();
-
     if constexpr (!SPARSE) {
+        // dense: the work item follows from the grid alone
         if (tid == 0) {
             const int bh = blockIdx.x / p.nsplit, sp = blockIdx.x % p.nsplit;
             s_work[0] = bh;
@@ -181,7 +180,10 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, KIND>::NT)
             s_work[4] = p.nsplit;
             s_work[5] = bh * p.nsplit;
         }
-    } else {
+    }
+    griddep_wait();
+
+    if constexpr (SPARSE) {
         // Chunk plan, identical in every CTA.  Chunk length cl = max(min_chunk,
         // ceil(total / (grid_target - cs * BH)) rounded up to 16).  Without
         // clusters head i owns max(1, ceil(k_i / cl)) consecutive chunk ids of

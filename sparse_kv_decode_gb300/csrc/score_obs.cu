@@ -108,7 +108,8 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
         for (int hf = 0; hf < C::HALVES; ++hf)
             tma_prefetch_2d(&tmq, hf * 64, (b * p.Hq + h * p.G) * p.W + row_base);
     }
-    griddep_wait();
+    // barriers and tensor memory are this CTA's own: set up while the previous
+    // kernel finishes
     if (tid == 0) {
 #pragma unroll
         for (int s = 0; s < C::STAGES; ++s) {
@@ -130,6 +131,7 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    griddep_wait();
     griddep_launch();
     volatile int* abort_flag = &s_abort;
 
