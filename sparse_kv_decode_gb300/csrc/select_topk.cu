@@ -36,7 +36,8 @@ struct SelCfg {
     static constexpr int OFF_HIST = kSelKeysPerCta * 4;                 // [2][256] this CTA's histogram
     static constexpr int OFF_RECV = OFF_HIST + 2 * 256 * 4;             // [pass][rank][256] every CTA's
     static constexpr int OFF_TOT = OFF_RECV + kPasses * CS * 256 * 4;   // [256] cluster histogram
-    static constexpr int SMEM = OFF_TOT + 256 * 4;
+    static constexpr int OFF_MBAR = OFF_TOT + 256 * 4;                 // [pass] arrival of the peers' histograms
+    static constexpr int SMEM = OFF_MBAR + kPasses * 8;
 };
 
 // Order-preserving image of an fp32 score: larger score -> larger key;
@@ -48,16 +49,21 @@ __device__ __forceinline__ uint32_t score_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ void st_dsmem_u32(uint32_t addr, uint32_t v) {
-    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-// Split cluster barrier: arrive early, wait where it matters.
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+// Split cluster barrier: arrive early (releasing this CTA's barrier set-up),
+// wait where it matters.
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+// 16 bytes into a peer's shared memory; their arrival counts on the peer's mbarrier.
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint4 v, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     remote_addr),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
+                 : "memory");
 }
 
 __device__ __forceinline__ unsigned warp_sum_u32(unsigned v) {
@@ -129,9 +135,21 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kSelThreads, 1)
         for (int i = tid; i < len; i += kSelThreads) out[n_sink + c0 + i] = cand_lo + c0 + i;
         return;
     }
-    // a peer's shared memory may be written only once that peer has started:
-    // arrive now, wait before the first store into a peer
-    if constexpr (CS > 1) cluster_arrive_relaxed();
+    // Each pass's histograms arrive by asynchronous stores that count bytes on a
+    // per-pass mbarrier of the receiver (all CS slots, this CTA's own included).
+    // A peer's shared memory may be written only once that peer has started and
+    // set up its mbarriers: arrive now, wait before the first store into a peer.
+    const uint32_t mbar0 = smem_u32(smem + C::OFF_MBAR);
+    if constexpr (CS > 1) {
+        if (tid == 0) {
+#pragma unroll
+            for (int ps = 0; ps < kPasses; ++ps) mbar_init(mbar0 + 8 * ps, 1);
+            fence_mbar_init();
+#pragma unroll
+            for (int ps = 0; ps < kPasses; ++ps) mbar_arrive_expect_tx(mbar0 + 8 * ps, CS * 256 * 4);
+        }
+        cluster_arrive_release();
+    }
 #pragma unroll
     for (int u = 0; u < kInFlight; ++u) {
         const int i = tid + u * kSelThreads;
@@ -168,23 +186,26 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kSelThreads, 1)
         if constexpr (CS > 1) {
             if (pass == 0) cluster_wait();   // every CTA of the cluster is running
         }
-        if (tid < 256) {
-            // this CTA's histogram into slot [pass][rank] of every CTA of the cluster
-            const unsigned c = h[tid];
-            if constexpr (CS > 1) {
-                const uint32_t a = smem_u32(recv + (pass * CS + rank) * 256 + tid);
+        if constexpr (CS > 1) {
+            if (tid < 64) {
+                // this CTA's histogram into slot [pass][rank] of every CTA of the cluster
+                const uint4 c4 = *reinterpret_cast<const uint4*>(h + 4 * tid);
+                const uint32_t a = smem_u32(recv + (pass * CS + rank) * 256 + 4 * tid);
 #pragma unroll
-                for (int r = 0; r < CS; ++r) st_dsmem_u32(dsmem_addr(a, r), c);
-            } else {
-                recv[pass * 256 + tid] = c;
+                for (int r = 0; r < CS; ++r) st_async_v4(dsmem_addr(a, r), c4, dsmem_addr(mbar0 + 8 * pass, r));
+            } else if (tid >= 256) {
+                hist[((pass + 1) & 1) * 256 + (tid - 256)] = 0u;   // the next pass's histogram
             }
+            // every CTA's histogram of this pass has arrived here (bounded wait; a
+            // peer that never sends cannot happen with the uniform control flow)
+            if (!mbar_wait(mbar0 + 8 * pass, 0) && tid == 0) flag_status(status, SDKV_DEV_TIMEOUT);
         } else {
-            hist[((pass + 1) & 1) * 256 + (tid - 256)] = 0u;   // the next pass's histogram
-        }
-        if constexpr (CS > 1)
-            cluster_sync_all();   // every CTA's histogram of this pass has arrived everywhere
-        else
+            if (tid < 256)
+                recv[pass * 256 + tid] = h[tid];
+            else
+                hist[((pass + 1) & 1) * 256 + (tid - 256)] = 0u;   // the next pass's histogram
             __syncthreads();
+        }
         if (tid < 256) {
             unsigned c = 0;
 #pragma unroll
