@@ -81,38 +81,67 @@ __global__ void __launch_bounds__(256) compact_kv_kernel(const bf16* __restrict_
                                                           long long sb, long long sh, long long sn, int n_cap, int Hkv,
                                                           int BH, const int* offsets, const int* indices,
                                                           long long rows_cap, bf16* k_out, bf16* v_out, int* status) {
-    const long long p0 = static_cast<long long>(blockIdx.x) * kCompactRows;
+    constexpr int CPR = D / 8;                  // 16-byte chunks of a K (or V) row
+    constexpr int LPR = 2 * CPR;                // lanes per row: K chunks, then V chunks
+    constexpr int RPW = 32 / LPR;               // rows per warp instruction
+    constexpr int WROWS = kCompactRows / 8;     // list positions per warp (8 warps)
+    constexpr int NIT = WROWS / RPW;            // copies in flight per lane
+    static_assert(WROWS <= 32 && WROWS % RPW == 0, "one list position per lane for the look-up");
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int off0 = __ldg(offsets);
     const long long total = __ldg(offsets + BH) - off0;
-    constexpr int CPR = D / 8;                  // 16-byte chunks of a K (or V) row
-    constexpr int RPW = 32 / (2 * CPR);         // rows per warp instruction
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int sub = lane / (2 * CPR), cl = lane % (2 * CPR);
+    const long long pw = static_cast<long long>(blockIdx.x) * kCompactRows + warp * WROWS;
+    // lane j < WROWS looks up position pw + j: its list entry and its head (the
+    // first head whose list ends after the position)
+    int my_idx = 0, my_b = 0, my_h = 0, my_ok = 0;
+    if (lane < WROWS) {
+        const long long p = pw + lane;
+        if (p < total) {
+            if (p >= rows_cap) {
+                flag_status(status, SDKV_DEV_BAD_LIST);
+            } else {
+                int lo = 0, hi = BH;
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (__ldg(offsets + mid + 1) - off0 > p) hi = mid; else lo = mid + 1;
+                }
+                int idx = indices[off0 + p];
+                if (static_cast<unsigned>(idx) >= static_cast<unsigned>(n_cap)) {
+                    flag_status(status, SDKV_DEV_BAD_INDEX);
+                    idx = 0;
+                }
+                my_idx = idx;
+                my_b = lo / Hkv;
+                my_h = lo - my_b * Hkv;
+                my_ok = 1;
+            }
+        }
+    }
+    // every row's chunk is loaded before any is stored
+    const int sub = lane / LPR, cl = lane % LPR;
     const bool is_v = cl >= CPR;
     const int ch = is_v ? cl - CPR : cl;
-    for (int r = warp * RPW + sub; r < kCompactRows; r += (blockDim.x / 32) * RPW) {
-        const long long p = p0 + r;
-        if (p >= total) break;
-        if (p >= rows_cap) {
-            flag_status(status, SDKV_DEV_BAD_LIST);
-            break;
+    uint4 buf[NIT];
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) {
+        const int r = it * RPW + sub;
+        const int idx = __shfl_sync(0xffffffffu, my_idx, r);
+        const int b = __shfl_sync(0xffffffffu, my_b, r);
+        const int h = __shfl_sync(0xffffffffu, my_h, r);
+        const int ok = __shfl_sync(0xffffffffu, my_ok, r);
+        buf[it] = make_uint4(0u, 0u, 0u, 0u);
+        if (ok) {
+            const bf16* src = (is_v ? v : k) + b * sb + h * sh + static_cast<long long>(idx) * sn + ch * 8;
+            buf[it] = __ldg(reinterpret_cast<const uint4*>(src));
         }
-        // the head holding position p: the first whose list ends after p
-        int lo = 0, hi = BH;
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (__ldg(offsets + mid + 1) - off0 > p) hi = mid; else lo = mid + 1;
+    }
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) {
+        const int r = it * RPW + sub;
+        if (__shfl_sync(0xffffffffu, my_ok, r)) {
+            bf16* dst = (is_v ? v_out : k_out) + (pw + r) * D + ch * 8;
+            *reinterpret_cast<uint4*>(dst) = buf[it];
         }
-        const int i = lo;
-        const int b = i / Hkv, h = i - (i / Hkv) * Hkv;
-        int idx = indices[off0 + p];
-        if (static_cast<unsigned>(idx) >= static_cast<unsigned>(n_cap)) {
-            flag_status(status, SDKV_DEV_BAD_INDEX);
-            idx = 0;
-        }
-        const bf16* src = (is_v ? v : k) + b * sb + h * sh + static_cast<long long>(idx) * sn + ch * 8;
-        bf16* dst = (is_v ? v_out : k_out) + p * D + ch * 8;
-        *reinterpret_cast<uint4*>(dst) = __ldg(reinterpret_cast<const uint4*>(src));
     }
 }
 
