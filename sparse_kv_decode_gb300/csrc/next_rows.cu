@@ -44,8 +44,20 @@ __global__ void append_drafts_kernel(const int* base_offsets, const int* base_in
         offsets[i] = out0;
         if (i == BH - 1) offsets[BH] = out0 + len + n_new;
     }
-    for (int e = threadIdx.x; e < len + n_new; e += blockDim.x)
-        indices[out0 + e] = (e < len) ? base_indices[st + e] : n_pos + (e - len);
+    constexpr int U = 8;   // loads in flight per thread
+    for (int e0 = threadIdx.x; e0 < len + n_new; e0 += U * blockDim.x) {
+        int val[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = e0 + u * blockDim.x;
+            val[u] = (e < len) ? base_indices[st + e] : n_pos + (e - len);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = e0 + u * blockDim.x;
+            if (e < len + n_new) indices[out0 + e] = val[u];
+        }
+    }
 }
 
 // Every draft step's lists of one round: set t (grid y) is the base CSR with
@@ -65,9 +77,20 @@ __global__ void draft_lists_kernel(const int* base_offsets, const int* base_indi
         set_off[i] = static_cast<int>(out0);
         if (i == BH - 1) set_off[BH] = static_cast<int>(out0 + len + n_new);
     }
-    for (int e = threadIdx.x; e < len + n_new; e += blockDim.x) {
-        const long long o = out0 + e;
-        if (o < stride) set_idx[o] = (e < len) ? base_indices[st + e] : n_pos + (e - len);
+    constexpr int U = 8;   // loads in flight per thread
+    for (int e0 = threadIdx.x; e0 < len + n_new; e0 += U * blockDim.x) {
+        int val[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = e0 + u * blockDim.x;
+            val[u] = (e < len) ? base_indices[st + e] : n_pos + (e - len);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = e0 + u * blockDim.x;
+            const long long o = out0 + e;
+            if (e < len + n_new && o < stride) set_idx[o] = val[u];
+        }
     }
 }
 
