@@ -146,6 +146,29 @@ def test_sparse_many_short_lists():
     _status_ok(ws)
 
 
+@pytest.mark.parametrize("Hkv", [31, 32, 33])
+def test_sparse_head_count_around_one_warp(Hkv):
+    # up to 32 (sequence, KV head) lists one warp plans the chunks, beyond that
+    # the whole block does: both sides of the switch, ragged lengths incl. empty
+    g = torch.Generator().manual_seed(40 + Hkv)
+    B, d, n = 1, 64, 1500
+    Hq = Hkv
+    k = _rand((B, Hkv, n, d), g)
+    v = _rand((B, Hkv, n, d), g)
+    q = _rand((B, Hq, d), g)
+    rng = np.random.default_rng(40 + Hkv)
+    lens = rng.integers(0, n + 1, size=B * Hkv).tolist()
+    lens[0], lens[-1] = 0, n
+    offs_d, offs = csr(lens, DEV)
+    _, idx = workloads.random_lists(B, Hkv, n, lens, seed=40 + Hkv)
+    ws = sk.new_workspace(sk.workspace_size(sk.OP_SPARSE_DECODE, B, Hq, Hkv, d, 0, 0), DEV)
+    o, lse = sk.sparse_decode_attn(q.to(DEV), k.to(DEV), v.to(DEV), offs_d, idx.to(DEV), scale_of(d), ws=ws)
+    o_ref, l_ref = oracle.sparse_decode(q, k, v, offs, idx.numpy())
+    assert_attn_close(o, o_ref, "sparse %d heads" % Hkv)
+    assert_lse_close(lse, l_ref, "sparse %d heads" % Hkv)
+    _status_ok(ws)
+
+
 def test_sparse_ragged_mha_lists_cross_ranges():
     # SparseMM-like: one query row per KV head, lengths from 0 to the whole cache,
     # so CTA ranges start and end inside lists and span several lists
