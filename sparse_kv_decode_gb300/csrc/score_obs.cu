@@ -40,9 +40,10 @@ struct ScoreParams {
     float* sc_part;   // [n_mg][BH][n]
 };
 
-template <int D>
+template <int D, int RB>
 struct ScoreCfg {
-    static constexpr int ROWS = 128;              // window rows per CTA (MMA M or N)
+    static constexpr int ROWS = 128;              // window rows per row block (MMA M or N)
+    static constexpr int GROWS = RB * ROWS;       // window rows per CTA: RB row blocks share each K tile
     static constexpr int TK = 128;                // keys per tile (MMA N or M)
     static constexpr int STAGES = 3;
     static constexpr int HALVES = D / 64;         // 128-byte K-blocks per row
@@ -50,28 +51,31 @@ struct ScoreCfg {
     static constexpr int NET = NEPI * 32;
     static constexpr int NT = NET + 64;           // + producer warp + MMA warp
     static constexpr int TILE_B = TK * D * 2;
-    static constexpr int Q_B = ROWS * D * 2;
+    static constexpr int QBLK_B = ROWS * D * 2;   // one row block of window queries
+    static constexpr int Q_B = RB * QBLK_B;
     static constexpr int HALF_B = TK * 128;       // one 64-wide K-block of a 128-row operand
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = Q_B;
-    static constexpr int OFF_CB = OFF_K + STAGES * TILE_B;     // pass 2: -(M + log2 L) per row
-    static constexpr int OFF_LIM = OFF_CB + ROWS * 4;          // last visible key per row
-    static constexpr int OFF_RED = OFF_LIM + ROWS * 4;         // [2][TK] half sums / [ROWS][2] stats
-    static constexpr int OFF_BAR = OFF_RED + 2 * TK * 4;
+    static constexpr int OFF_CB = OFF_K + STAGES * TILE_B;     // pass 2: -(M + log2 L) per row (GROWS)
+    static constexpr int OFF_LIM = OFF_CB + GROWS * 4;         // last visible key per row
+    static constexpr int OFF_RED = OFF_LIM + GROWS * 4;        // [GROWS][2] row statistics
+    static constexpr int OFF_BAR = OFF_RED + 2 * GROWS * 4;
     static constexpr int NBAR = 2 * STAGES + 1 + 2 + 2;
     static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_TMEM + 16;
     static constexpr int SMEM_ALLOC = SMEM + 1024;
-    static constexpr uint32_t TMEM_COLS = 2 * TK;  // two accumulator buffers
+    static constexpr uint32_t TMEM_COLS = 2 * RB * TK;  // two accumulator buffers of RB blocks
     static constexpr uint32_t IDESC = idesc_bf16_f32(128, 128);
     static_assert(ROWS == 128 && TK == 128, "one 128x128 MMA shape for both passes");
+    static_assert(RB == 1 || RB == 2, "one or two row blocks per CTA");
+    static_assert(GROWS <= NET, "one epilogue thread per window row of the CTA");
 };
 
-template <int D, bool PASS2>
-__global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
+template <int D, bool PASS2, int RB>
+__global__ void __launch_bounds__(ScoreCfg<D, RB>::NT, 1)
     score_kernel(const __grid_constant__ ScoreParams p, const __grid_constant__ CUtensorMap tmk,
                  const __grid_constant__ CUtensorMap tmq) {
-    using C = ScoreCfg<D>;
+    using C = ScoreCfg<D, RB>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem =
         reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -94,7 +98,7 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
     const int lo = sp * p.chunk;
     const int hi = min(lo + p.chunk, p.n);
     const int ntiles = (hi - lo + C::TK - 1) / C::TK;
-    const int row_base = mg * C::ROWS;   // first window row (of R = G * W) of this CTA
+    const int row_base = mg * C::GROWS;   // first window row (of R = G * W) of this CTA
 
     if (tid == 0) {
         // the first stages' K tiles and this CTA's window rows into L2 while the
@@ -105,8 +109,10 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
 #pragma unroll
             for (int hf = 0; hf < C::HALVES; ++hf) tma_prefetch_4d(&tmk, hf * 64, lo + t * C::TK, h, b);
 #pragma unroll
-        for (int hf = 0; hf < C::HALVES; ++hf)
-            tma_prefetch_2d(&tmq, hf * 64, (b * p.Hq + h * p.G) * p.W + row_base);
+        for (int rb = 0; rb < RB; ++rb)
+#pragma unroll
+            for (int hf = 0; hf < C::HALVES; ++hf)
+                tma_prefetch_2d(&tmq, hf * 64, (b * p.Hq + h * p.G) * p.W + row_base + rb * C::ROWS);
     }
     // barriers and tensor memory are this CTA's own: set up while the previous
     // kernel finishes
@@ -145,8 +151,11 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
             const int qrow0 = (b * p.Hq + h * p.G) * p.W + row_base;
             mbar_arrive_expect_tx(bar_q, C::Q_B);
 #pragma unroll
-            for (int hf = 0; hf < C::HALVES; ++hf)
-                tma_load_2d(sbase + C::OFF_Q + hf * C::HALF_B, &tmq, hf * 64, qrow0, bar_q);
+            for (int rb = 0; rb < RB; ++rb)
+#pragma unroll
+                for (int hf = 0; hf < C::HALVES; ++hf)
+                    tma_load_2d(sbase + C::OFF_Q + rb * C::QBLK_B + hf * C::HALF_B, &tmq, hf * 64,
+                                qrow0 + rb * C::ROWS, bar_q);
             for (int t = 0; t < ntiles; ++t) {
                 const int s = t % C::STAGES;
                 if (t >= C::STAGES && !mbar_wait(bar_kempty + 8 * s, ((t / C::STAGES) & 1) ^ 1)) {
@@ -172,17 +181,22 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
                 if (ok && t >= 2) ok = mbar_wait(bar_tempty + 8 * buf, ((t >> 1) & 1) ^ 1);
                 if (!ok || *abort_flag) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem + buf * C::TK;
                 const uint32_t kst = sbase + C::OFF_K + s * C::TILE_B;
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks >> 2) * C::HALF_B + (ks & 3) * 32;
-                    const uint64_t qd = sw128_kmajor_desc(sbase + C::OFF_Q + off);
-                    const uint64_t kd = sw128_kmajor_desc(kst + off);
-                    if (PASS2)
-                        tc_mma_bf16(d_tmem, kd, qd, C::IDESC, ks > 0);
-                    else
-                        tc_mma_bf16(d_tmem, qd, kd, C::IDESC, ks > 0);
+                for (int rb = 0; rb < RB; ++rb) {
+                    // row block rb of this CTA against the K tile, accumulator rb of the buffer
+                    const uint32_t d_tmem = tmem + (buf * RB + rb) * C::TK;
+                    const uint32_t qblk = sbase + C::OFF_Q + rb * C::QBLK_B;
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint32_t off = (ks >> 2) * C::HALF_B + (ks & 3) * 32;
+                        const uint64_t qd = sw128_kmajor_desc(qblk + off);
+                        const uint64_t kd = sw128_kmajor_desc(kst + off);
+                        if (PASS2)
+                            tc_mma_bf16(d_tmem, kd, qd, C::IDESC, ks > 0);
+                        else
+                            tc_mma_bf16(d_tmem, qd, kd, C::IDESC, ks > 0);
+                    }
                 }
                 tc_commit(bar_kempty + 8 * s);    // the stage is free once these MMAs are done
                 tc_commit(bar_tfull + 8 * buf);   // and the accumulator is ready
@@ -202,26 +216,29 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
         int* lim = reinterpret_cast<int*>(smem + C::OFF_LIM);
         float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
         const int et = ew * 32 + lane;      // 0 .. NET-1
-        if (et < C::ROWS) {
+        if (et < C::GROWS) {
             const int r = row_base + et;
             lim[et] = (r < p.R) ? p.q_pos0 + r % p.W : -1;
         }
         if constexpr (PASS2) {
-            // Row statistics over the key splits of pass 1: thread et merges splits
-            // s = et/128, et/128 + 2, ... of row et%128 (up to 16 loads in flight),
-            // the two halves meet in shared memory.  The exponent bias of a row is
+            // Row statistics over the key splits of pass 1: TPR threads per row of the
+            // CTA, thread et merges splits s = et/GROWS, et/GROWS + TPR, ... of row
+            // et%GROWS (up to 16 loads in flight); with two threads per row the two
+            // halves meet in shared memory.  The exponent bias of a row is
             // -(M + log2 L), so a key's probability is 2^(c*q.k + bias).
-            const int rr = et & (C::ROWS - 1), s0 = et >> 7;
+            constexpr int TPR = C::NET / C::GROWS;
+            static_assert(TPR == 1 || TPR == 2, "one or two threads per row");
+            const int rr = et % C::GROWS, s0 = et / C::GROWS;
             const int r = row_base + rr;
             float mm = -INFINITY, ll = 0.f;
             if (r < p.R) {
                 const float* base = p.st_part + (static_cast<size_t>(bh) * p.nsplit * p.R + r) * 2;
                 const size_t stride = static_cast<size_t>(p.R) * 2;
-                for (int sb = s0; sb < p.nsplit; sb += 32) {
+                for (int sb = s0; sb < p.nsplit; sb += 16 * TPR) {
                     float2 v2[16];
 #pragma unroll
                     for (int u = 0; u < 16; ++u) {
-                        const int sidx = sb + 2 * u;
+                        const int sidx = sb + TPR * u;
                         v2[u] = sidx < p.nsplit ? __ldcg(reinterpret_cast<const float2*>(base + sidx * stride))
                                                 : make_float2(-INFINITY, 0.f);
                     }
@@ -237,31 +254,42 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
                     }
                 }
             }
-            if (s0 == 1) {
+            if (TPR == 2 && s0 == 1) {
                 red[2 * rr] = mm;
                 red[2 * rr + 1] = ll;
             }
             named_bar_sync(1, C::NET);
             if (s0 == 0) {
-                const float m2 = red[2 * rr], l2 = red[2 * rr + 1];
-                const float M = fmaxf(mm, m2);
-                float L = 0.f;
-                if (M != -INFINITY)
-                    L = (mm == -INFINITY ? 0.f : ll * fast_exp2(mm - M)) + (m2 == -INFINITY ? 0.f : l2 * fast_exp2(m2 - M));
+                float M = mm, L = ll;
+                if (TPR == 2) {
+                    const float m2 = red[2 * rr], l2 = red[2 * rr + 1];
+                    M = fmaxf(mm, m2);
+                    L = 0.f;
+                    if (M != -INFINITY)
+                        L = (mm == -INFINITY ? 0.f : ll * fast_exp2(mm - M)) +
+                            (m2 == -INFINITY ? 0.f : l2 * fast_exp2(m2 - M));
+                }
                 cb[rr] = (r < p.R && L > 0.f) ? -(M + fast_log2(L)) : -INFINITY;   // rows past R add nothing
             }
         }
         named_bar_sync(1, C::NET);
         const float c = p.scale_log2;
-        // pass 1 state (row tl)
-        const int my_lim = lim[tl];
-        float m_run = -INFINITY, l_run = 0.f;
+        // pass 1 state: row tl of each row block
+        int my_lim[RB];
+        float m_run[RB], l_run[RB];
+#pragma unroll
+        for (int rb = 0; rb < RB; ++rb) {
+            my_lim[rb] = lim[rb * C::ROWS + tl];
+            m_run[rb] = -INFINITY;
+            l_run[rb] = 0.f;
+        }
         bool aborted = false;
 
         // Epilogue group `half` (warps 2-5 or 6-9) takes the tiles of its parity,
-        // i.e. always accumulator buffer `half`, all 128 columns; the two groups
-        // never meet inside the loop.  Columns are read 64 at a time; the buffer
-        // is handed back to the MMA issuer as soon as the second half is loaded.
+        // i.e. always accumulator buffer `half` (RB accumulators of 128 columns);
+        // the two groups never meet inside the loop.  Columns are read 64 at a
+        // time; the buffer is handed back to the MMA issuer as soon as its last
+        // columns are loaded.
         for (int t = half; t < ntiles; t += 2) {
             const int buf = t & 1;
             if (!mbar_wait(bar_tfull + 8 * buf, (t >> 1) & 1)) {
@@ -269,23 +297,25 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
                 break;
             }
             tc_fence_after();
-            const uint32_t ta = tmem + (static_cast<uint32_t>(32 * quad) << 16) + buf * C::TK;
             const int key0 = lo + t * C::TK;
             float acc = 0.f;   // pass 2: this key's sum over the rows
+#pragma unroll
+            for (int rb = 0; rb < RB; ++rb) {
+            const uint32_t ta = tmem + (static_cast<uint32_t>(32 * quad) << 16) + (buf * RB + rb) * C::TK;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 uint32_t v[64];
                 tmem_ld64_sync(ta + hh * 64, v);
-                if (hh == 1) {
+                if (rb == RB - 1 && hh == 1) {
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar_tempty + 8 * buf);
                 }
                 if constexpr (!PASS2) {
-                    // row tl, columns = keys key0 + hh*64 + i
-                    if (my_lim >= 0) {
+                    // row tl of row block rb, columns = keys key0 + hh*64 + i
+                    if (my_lim[rb] >= 0) {
                         const int kfirst = key0 + hh * 64;
-                        const bool full = (kfirst + 63 < hi) && (kfirst + 63 <= my_lim);
+                        const bool full = (kfirst + 63 < hi) && (kfirst + 63 <= my_lim[rb]);
                         float mx = -INFINITY;
                         if (full) {
 #pragma unroll
@@ -294,13 +324,13 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
 #pragma unroll
                             for (int i = 0; i < 64; ++i) {
                                 const int key = kfirst + i;
-                                const float x = (key < hi && key <= my_lim) ? __uint_as_float(v[i]) : -INFINITY;
+                                const float x = (key < hi && key <= my_lim[rb]) ? __uint_as_float(v[i]) : -INFINITY;
                                 v[i] = __float_as_uint(x);
                                 mx = fmaxf(mx, x);
                             }
                         }
                         if (mx != -INFINITY) {
-                            const float mnew = fmaxf(m_run, mx * c);
+                            const float mnew = fmaxf(m_run[rb], mx * c);
                             // four running sums (lanes i%4) in two paired registers
                             const float2 c2 = make_float2(c, c), nm2 = make_float2(-mnew, -mnew);
                             float2 s01 = make_float2(0.f, 0.f), s23 = s01;
@@ -311,12 +341,12 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
                                 s01 = add2(s01, make_float2(fast_exp2(x01.x), fast_exp2(x01.y)));
                                 s23 = add2(s23, make_float2(fast_exp2(x23.x), fast_exp2(x23.y)));
                             }
-                            l_run = l_run * fast_exp2(m_run - mnew) + ((s01.x + s01.y) + (s23.x + s23.y));
-                            m_run = mnew;
+                            l_run[rb] = l_run[rb] * fast_exp2(m_run[rb] - mnew) + ((s01.x + s01.y) + (s23.x + s23.y));
+                            m_run[rb] = mnew;
                         }
                     }
                 } else {
-                    // lane tl is key key0 + tl; columns are window rows hh*64 + i
+                    // lane tl is key key0 + tl; columns are window rows rb*128 + hh*64 + i
                     const int key = key0 + tl;
                     const bool all_rows = key0 + C::TK - 1 <= p.q_pos0;
                     const float2 c2 = make_float2(c, c);
@@ -325,7 +355,7 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
                         // every window row sees every key of the tile: no mask
 #pragma unroll
                         for (int i = 0; i < 64; i += 4) {
-                            const float4 b4 = *reinterpret_cast<const float4*>(cb + hh * 64 + i);
+                            const float4 b4 = *reinterpret_cast<const float4*>(cb + rb * C::ROWS + hh * 64 + i);
                             const float2 x01 = fma2(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), c2,
                                                     make_float2(b4.x, b4.y));
                             const float2 x23 = fma2(make_float2(__uint_as_float(v[i + 2]), __uint_as_float(v[i + 3])), c2,
@@ -336,8 +366,8 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
                     } else {
 #pragma unroll
                         for (int i = 0; i < 64; i += 4) {
-                            const float4 b4 = *reinterpret_cast<const float4*>(cb + hh * 64 + i);
-                            const int4 l4 = *reinterpret_cast<const int4*>(lim + hh * 64 + i);
+                            const float4 b4 = *reinterpret_cast<const float4*>(cb + rb * C::ROWS + hh * 64 + i);
+                            const int4 l4 = *reinterpret_cast<const int4*>(lim + rb * C::ROWS + hh * 64 + i);
                             const float2 x01 = fma2(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])), c2,
                                                     make_float2(b4.x, b4.y));
                             const float2 x23 = fma2(make_float2(__uint_as_float(v[i + 2]), __uint_as_float(v[i + 3])), c2,
@@ -352,6 +382,7 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
                     }
                     acc += (s01.x + s01.y) + (s23.x + s23.y);
                 }
+            }
             }
             if constexpr (PASS2) {
                 const int key = key0 + tl;
@@ -370,23 +401,29 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
         const bool stop = named_bar_or(1, C::NET, aborted || *abort_flag);
         if (!stop) {
             if constexpr (!PASS2) {
-                // merge the two column halves of each row, store the split's partial
+                // merge the two epilogue groups' statistics of each row, store the split's partial
                 if (half == 1) {
-                    red[2 * tl] = m_run;
-                    red[2 * tl + 1] = l_run;
+#pragma unroll
+                    for (int rb = 0; rb < RB; ++rb) {
+                        red[2 * (rb * C::ROWS + tl)] = m_run[rb];
+                        red[2 * (rb * C::ROWS + tl) + 1] = l_run[rb];
+                    }
                 }
                 named_bar_sync(1, C::NET);
                 if (half == 0) {
-                    const float m2 = red[2 * tl], l2 = red[2 * tl + 1];
-                    const float M = fmaxf(m_run, m2);
-                    float L = 0.f;
-                    if (M != -INFINITY)
-                        L = (m_run == -INFINITY ? 0.f : l_run * fast_exp2(m_run - M)) +
-                            (m2 == -INFINITY ? 0.f : l2 * fast_exp2(m2 - M));
-                    const int r = row_base + tl;
-                    if (r < p.R)
-                        *reinterpret_cast<float2*>(p.st_part + ((static_cast<size_t>(bh) * p.nsplit + sp) * p.R + r) * 2) =
-                            make_float2(M, L);
+#pragma unroll
+                    for (int rb = 0; rb < RB; ++rb) {
+                        const float m2 = red[2 * (rb * C::ROWS + tl)], l2 = red[2 * (rb * C::ROWS + tl) + 1];
+                        const float M = fmaxf(m_run[rb], m2);
+                        float L = 0.f;
+                        if (M != -INFINITY)
+                            L = (m_run[rb] == -INFINITY ? 0.f : l_run[rb] * fast_exp2(m_run[rb] - M)) +
+                                (m2 == -INFINITY ? 0.f : l2 * fast_exp2(m2 - M));
+                        const int r = row_base + rb * C::ROWS + tl;
+                        if (r < p.R)
+                            *reinterpret_cast<float2*>(
+                                p.st_part + ((static_cast<size_t>(bh) * p.nsplit + sp) * p.R + r) * 2) = make_float2(M, L);
+                    }
                 }
             } else if (p.n_mg > 1) {
                 __threadfence();
@@ -470,7 +507,7 @@ __global__ void __launch_bounds__(ScoreCfg<D>::NT, 1)
 namespace {
 
 struct ScorePlan {
-    int n_mg, nsplit, chunk;
+    int rb, n_mg, nsplit, chunk;
     size_t off_t2, off_sp, off_sc, bytes;
 };
 
@@ -479,7 +516,9 @@ ScorePlan score_plan(int B, int Hq, int Hkv, int n, int W, int num_sms) {
     const int BH = B * Hkv;
     const int R = (Hq / Hkv) * W;
     constexpr int ROWS = 128, TK = 128;
-    pl.n_mg = (R + ROWS - 1) / ROWS;
+    // more than one row block per head: two per CTA, sharing each K tile
+    pl.rb = R > ROWS ? 2 : 1;
+    pl.n_mg = (R + pl.rb * ROWS - 1) / (pl.rb * ROWS);
     const int target = std::max(num_sms, 1);   // one CTA per SM (tensor memory + 130 KB of stages)
     // splits per (sequence, KV head, row block): as many as fit one wave; a
     // second wave would double the time for the few CTAs that spill into it
@@ -502,11 +541,11 @@ ScorePlan score_plan(int B, int Hq, int Hkv, int n, int W, int num_sms) {
     return pl;
 }
 
-template <int D, bool PASS2>
+template <int D, bool PASS2, int RB>
 cudaError_t launch_score_pass(const ScoreParams& p, const CUtensorMap& tmk, const CUtensorMap& tmq, int grid,
                               cudaStream_t st) {
-    using C = ScoreCfg<D>;
-    auto kern = score_kernel<D, PASS2>;
+    using C = ScoreCfg<D, RB>;
+    auto kern = score_kernel<D, PASS2, RB>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -567,11 +606,21 @@ int launch_score(const ScoreLaunch& a, const CUtensorMap* tmk, const CUtensorMap
     const int grid = p.BH * pl.n_mg * pl.nsplit;
     cudaError_t e;
     if (a.d == 128) {
-        e = launch_score_pass<128, false>(p, *tmk, *tmq, grid, a.stream);
-        if (e == cudaSuccess) e = launch_score_pass<128, true>(p, *tmk, *tmq, grid, a.stream);
+        if (pl.rb == 2) {
+            e = launch_score_pass<128, false, 2>(p, *tmk, *tmq, grid, a.stream);
+            if (e == cudaSuccess) e = launch_score_pass<128, true, 2>(p, *tmk, *tmq, grid, a.stream);
+        } else {
+            e = launch_score_pass<128, false, 1>(p, *tmk, *tmq, grid, a.stream);
+            if (e == cudaSuccess) e = launch_score_pass<128, true, 1>(p, *tmk, *tmq, grid, a.stream);
+        }
     } else {
-        e = launch_score_pass<64, false>(p, *tmk, *tmq, grid, a.stream);
-        if (e == cudaSuccess) e = launch_score_pass<64, true>(p, *tmk, *tmq, grid, a.stream);
+        if (pl.rb == 2) {
+            e = launch_score_pass<64, false, 2>(p, *tmk, *tmq, grid, a.stream);
+            if (e == cudaSuccess) e = launch_score_pass<64, true, 2>(p, *tmk, *tmq, grid, a.stream);
+        } else {
+            e = launch_score_pass<64, false, 1>(p, *tmk, *tmq, grid, a.stream);
+            if (e == cudaSuccess) e = launch_score_pass<64, true, 1>(p, *tmk, *tmq, grid, a.stream);
+        }
     }
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);
