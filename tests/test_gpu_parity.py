@@ -276,6 +276,7 @@ def test_score_matches_oracle(B, Hq, Hkv, d, n, W, q_pos0):
     (300, 2, 290, 2, 10, 0),
     (300, 2, 290, 2, 10, 288),
     (20000, 0, 19968, 0, 32, 4000),
+    (70000, 0, 69968, 0, 32, 21000),   # long candidate range: 16 CTAs per head
 ])
 def test_select_exact_on_same_scores(n, cand_lo, cand_hi, n_sink, n_recent, K):
     rng = np.random.default_rng(n + K)
