@@ -607,12 +607,12 @@ int launch_specvlm(const SpecLaunch& a, const char** why) {
     if (e == cudaSuccess) {
         const int nW = (nV + 31) / 32;
         const int smem = 4 * nW + (p.keys_in_smem ? 5 * nV : 0);   // bitmap, then keys and flags
-        static unsigned long long attr_set = 0;
+        static std::atomic<unsigned long long> attr_set{0};  // one bit per device
         int dev = 0;
         e = cudaGetDevice(&dev);
-        if (e == cudaSuccess && (dev >= 64 || !(attr_set & (1ull << dev)))) {
+        if (e == cudaSuccess && !attr_done(attr_set, dev)) {
             e = cudaFuncSetAttribute(specvlm_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSpecSmemMax);
-            if (e == cudaSuccess && dev < 64) attr_set |= (1ull << dev);
+            if (e == cudaSuccess) attr_mark(attr_set, dev);
         }
         if (e == cudaSuccess) {
             specvlm_select_kernel<<<a.B, kSpecNT, smem, a.stream>>>(p);

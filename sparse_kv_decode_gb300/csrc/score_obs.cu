@@ -549,11 +549,11 @@ cudaError_t launch_score_pass(const ScoreParams& p, const CUtensorMap& tmk, cons
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    static unsigned long long attr_set = 0;
-    if (dev >= 64 || !(attr_set & (1ull << dev))) {
+    static std::atomic<unsigned long long> attr_set{0};  // one bit per device, per instantiation
+    if (!attr_done(attr_set, dev)) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
         if (e != cudaSuccess) return e;
-        if (dev < 64) attr_set |= (1ull << dev);
+        attr_mark(attr_set, dev);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

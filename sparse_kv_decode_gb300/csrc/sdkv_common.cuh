@@ -7,9 +7,20 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/sdkv.h"
 
 namespace sdkv {
+
+// Kernel attributes are set once per device and kernel instantiation; the
+// per-instantiation bitmask of devices done is shared by host threads.
+inline bool attr_done(const std::atomic<unsigned long long>& set, int dev) {
+    return dev < 64 && ((set.load(std::memory_order_acquire) >> dev) & 1ull);
+}
+inline void attr_mark(std::atomic<unsigned long long>& set, int dev) {
+    if (dev < 64) set.fetch_or(1ull << dev, std::memory_order_release);
+}
 
 using bf16 = __nv_bfloat16;
 

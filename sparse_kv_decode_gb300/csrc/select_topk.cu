@@ -342,10 +342,10 @@ cudaError_t launch_select_cs(const SelectLaunch& a) {
     using C = SelCfg<CS>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    static unsigned long long attr_set = 0;   // one bit per device, per instantiation
-    if (e == cudaSuccess && (dev >= 64 || !(attr_set & (1ull << dev)))) {
+    static std::atomic<unsigned long long> attr_set{0};  // one bit per device, per instantiation
+    if (e == cudaSuccess && !attr_done(attr_set, dev)) {
         e = cudaFuncSetAttribute(select_topk_kernel<CS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e == cudaSuccess && dev < 64) attr_set |= (1ull << dev);
+        if (e == cudaSuccess) attr_mark(attr_set, dev);
     }
     if (e != cudaSuccess) return e;
     return launch_pdl(select_topk_kernel<CS>, dim3(a.B * a.Hkv * CS), dim3(kSelThreads), C::SMEM, a.stream, a.scores,
