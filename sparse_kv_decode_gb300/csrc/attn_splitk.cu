@@ -899,7 +899,8 @@ DensePlan dense_plan(int BH, int n_total, int num_sms) {
     DensePlan pl{};
     pl.cs = per_head >= 16 ? 8 : per_head >= 8 ? 4 : per_head >= 4 ? 2 : 1;
     if (pl.cs > 1) {
-        pl.nsplit = (per_head / pl.cs) * pl.cs;
+        // at most 4 clusters per head: the last one merges their partials
+        pl.nsplit = std::min((per_head / pl.cs) * pl.cs, 4 * pl.cs);
         pl.chunk = (n_total + pl.nsplit - 1) / pl.nsplit;
         pl.chunk = ((pl.chunk + kDenseTK - 1) / kDenseTK) * kDenseTK;
         pl.ncl = pl.nsplit / pl.cs;
