@@ -129,7 +129,7 @@ using namespace sdkv;
 
 extern "C" {
 
-int32_t sdkv_version(void) { return 100; }
+int32_t sdkv_version(void) { return 101; }
 
 const char* sdkv_last_error(void) { return g_last_error.c_str(); }
 

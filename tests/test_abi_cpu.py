@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(L):
     assert len(names) == 16, names
     for name in names:
         assert hasattr(L, name), name
-    assert sk.version() == 100
+    assert sk.version() == 101
 
 
 def test_budgets_match_oracle_exactly(L):
