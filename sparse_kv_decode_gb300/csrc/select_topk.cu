@@ -1,6 +1,7 @@
 // Top-K selection and list assembly (StD 3.2 argTopK; SparseMM K = r + b_score
 // with the local window kept apart; ByteCross: sinks + highest-scoring
-// entries).  A cluster of 8 CTAs (512 threads each) per (batch, KV head):
+// entries).  A cluster of up to 8 CTAs per (batch, KV head), 512 threads each,
+// 1024 when a CTA holds many keys:
 //   1. CTA r of the cluster maps its eighth of the candidates' fp32 scores to an
 //      order-preserving uint32 key (larger score -> larger key) kept in shared
 //      memory;
@@ -27,8 +28,7 @@ namespace sdkv {
 namespace {
 
 constexpr int kMaxCS = 8;                       // CTAs per head at most (portable cluster size)
-constexpr int kSelThreads = 512;
-constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kSelBigCta = 8192;                 // keys per CTA above which a CTA runs 1024 threads
 constexpr int kPasses = 4;                      // 8-bit digits of a 32-bit key
 constexpr int kSelKeysPerCta = 32 * 1024;       // shared-memory keys per CTA
 template <int CS>
@@ -82,10 +82,12 @@ __device__ __forceinline__ unsigned warp_excl_scan_u32(unsigned v, int lane) {
     return incl - v;
 }
 
-template <int CS>
-__global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kSelThreads, 1)
+template <int CS, int NT>
+__global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(NT, 1)
     select_topk_kernel(const float* __restrict__ scores, int n, int cand_lo, int cand_hi, int n_sink,
                        int n_recent, const int* __restrict__ offsets, int* __restrict__ indices, int* status) {
+    static_assert(NT == 512 || NT == 1024, "two histogram parities of 256 entries take 512 threads");
+    constexpr int kSelThreads = NT, kSelWarps = NT / 32;
     extern __shared__ __align__(16) uint8_t smem[];
     uint32_t* keys = reinterpret_cast<uint32_t*>(smem);
     using C = SelCfg<CS>;
@@ -167,7 +169,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kSelThreads, 1)
             if (i < len) keys[i] = score_key(v[u]);
         }
     }
-    hist[tid] = 0u;   // both parities (2 * 256 = kSelThreads entries)
+    if (tid < 512) hist[tid] = 0u;   // both parities (2 * 256 entries)
     __syncthreads();
 
     // ---- radix select of the K-th largest key, 8 bits per pass
@@ -193,7 +195,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kSelThreads, 1)
                 const uint32_t a = smem_u32(recv + (pass * CS + rank) * 256 + 4 * tid);
 #pragma unroll
                 for (int r = 0; r < CS; ++r) st_async_v4(dsmem_addr(a, r), c4, dsmem_addr(mbar0 + 8 * pass, r));
-            } else if (tid >= 256) {
+            } else if (tid >= 256 && tid < 512) {
                 hist[((pass + 1) & 1) * 256 + (tid - 256)] = 0u;   // the next pass's histogram
             }
             // every CTA's histogram of this pass has arrived here (bounded wait; a
@@ -202,7 +204,7 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kSelThreads, 1)
         } else {
             if (tid < 256)
                 recv[pass * 256 + tid] = h[tid];
-            else
+            else if (tid < 512)
                 hist[((pass + 1) & 1) * 256 + (tid - 256)] = 0u;   // the next pass's histogram
             __syncthreads();
         }
@@ -242,12 +244,11 @@ __global__ void __cluster_dims__(CS, 1, 1) __launch_bounds__(kSelThreads, 1)
     // ---- where each CTA's segment of the list starts.  A key is above T when,
     // at the first pass where its digit differs from T's, the digit is larger:
     // rank r holds sum over passes p of its slot-p counts of digits > digit_p.
-    {
+    if (warp < 2 * CS) {
         const int r = warp >> 1, p0 = (warp & 1) * 2;
         unsigned g = 0;
 #pragma unroll
         for (int pp = p0; pp < p0 + 2; ++pp) {
-            if (r >= CS) break;
             const unsigned dig = s_digit[pp];
             const unsigned* hr = recv + (pp * CS + r) * 256;
 #pragma unroll
@@ -337,18 +338,18 @@ int select_cluster_size(int BH, int ncand, int num_sms) {
     return cs;
 }
 
-template <int CS>
+template <int CS, int NT>
 cudaError_t launch_select_cs(const SelectLaunch& a) {
     using C = SelCfg<CS>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     static std::atomic<unsigned long long> attr_set{0};  // one bit per device, per instantiation
     if (e == cudaSuccess && !attr_done(attr_set, dev)) {
-        e = cudaFuncSetAttribute(select_topk_kernel<CS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        e = cudaFuncSetAttribute(select_topk_kernel<CS, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e == cudaSuccess) attr_mark(attr_set, dev);
     }
     if (e != cudaSuccess) return e;
-    return launch_pdl(select_topk_kernel<CS>, dim3(a.B * a.Hkv * CS), dim3(kSelThreads), C::SMEM, a.stream, a.scores,
+    return launch_pdl(select_topk_kernel<CS, NT>, dim3(a.B * a.Hkv * CS), dim3(NT), C::SMEM, a.stream, a.scores,
                       a.n, a.cand_lo, a.cand_hi, a.n_sink, a.n_recent, a.offsets, a.indices, static_cast<int*>(a.ws));
 }
 
@@ -361,11 +362,14 @@ int launch_select(const SelectLaunch& a, const char** why) {
         return SDKV_ERR_UNSUPPORTED;
     }
     cudaError_t e = cudaErrorInvalidValue;
-    switch (select_cluster_size(a.B * a.Hkv, ncand, std::max(a.num_sms, 1))) {
-        case 1: e = launch_select_cs<1>(a); break;
-        case 2: e = launch_select_cs<2>(a); break;
-        case 4: e = launch_select_cs<4>(a); break;
-        default: e = launch_select_cs<8>(a); break;
+    const int cs = select_cluster_size(a.B * a.Hkv, ncand, std::max(a.num_sms, 1));
+    // few keys per CTA: 512 threads reach the barriers sooner; many: 1024 count them faster
+    const bool big = (ncand + cs - 1) / cs > kSelBigCta;
+    switch (cs) {
+        case 1: e = big ? launch_select_cs<1, 1024>(a) : launch_select_cs<1, 512>(a); break;
+        case 2: e = big ? launch_select_cs<2, 1024>(a) : launch_select_cs<2, 512>(a); break;
+        case 4: e = big ? launch_select_cs<4, 1024>(a) : launch_select_cs<4, 512>(a); break;
+        default: e = big ? launch_select_cs<8, 1024>(a) : launch_select_cs<8, 512>(a); break;
     }
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);

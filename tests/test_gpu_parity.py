@@ -312,6 +312,23 @@ def test_select_many_heads(B, Hkv):
     assert np.array_equal(idx.cpu().numpy(), want)
 
 
+@pytest.mark.parametrize("B,Hkv,n", [(1, 2, 70000), (4, 8, 40000), (8, 8, 20000), (16, 8, 12000)])
+def test_select_large_ctas(B, Hkv, n):
+    # more than 8192 candidates per CTA at 8, 4, 2 and 1 CTAs per head: the 1024-thread CTAs
+    rng = np.random.default_rng(n + B)
+    cand_lo, n_recent = 4, 64
+    cand_hi = n - n_recent
+    sc = rng.lognormal(0, 2, (B, Hkv, n)).astype(np.float32)
+    sc[0, 0] = np.round(sc[0, 0] * 4) / 4            # many ties
+    sc[0, 1, ::5] = 0.0
+    sc[B - 1, Hkv - 1, ::13] = np.nan
+    lens = [4 + int(k) + n_recent for k in rng.integers(0, cand_hi - cand_lo + 1, B * Hkv)]
+    offs_d, offs = csr(lens, DEV)
+    idx = sk.select_topk(torch.from_numpy(sc).to(DEV), n, cand_lo, cand_hi, 4, n_recent, offs_d, int(offs[-1]))
+    want = oracle.select_topk(sc, n, cand_lo, cand_hi, 4, n_recent, offs)
+    assert np.array_equal(idx.cpu().numpy(), want)
+
+
 def test_select_ragged_budgets_and_bad_list():
     rng = np.random.default_rng(1)
     B, Hkv, n = 1, 5, 4000
