@@ -18,8 +18,8 @@
 //           key, so each epilogue thread sums its key's 128 row probabilities.
 // Warp roles: warp 0 streams the window rows once and the key tiles through a
 // ring of shared-memory stages with TMA (128-byte swizzle); warp 1 allocates
-// tensor memory and one of its threads issues the MMAs into two accumulator
-// buffers; warps 2..9 read the accumulators (tcgen05.ld) and do the softmax
+// tensor memory and one of its threads issues the MMAs into a ring of two or
+// four accumulator buffers; warps 2..9 read the accumulators (tcgen05.ld) and do the softmax
 // arithmetic.  Every wait is bounded.  A CTA covers 128 window rows (one row
 // block) and one key split; larger groups or windows use more row blocks, whose
 // partial key sums are added in a fixed order by the last one (deterministic).
@@ -60,11 +60,14 @@ struct ScoreCfg {
     static constexpr int OFF_LIM = OFF_CB + GROWS * 4;         // last visible key per row
     static constexpr int OFF_RED = OFF_LIM + GROWS * 4;        // [GROWS][2] row statistics
     static constexpr int OFF_BAR = OFF_RED + 2 * GROWS * 4;
-    static constexpr int NBAR = 2 * STAGES + 1 + 2 + 2;
+    // accumulator buffers: four (all 512 columns) for one row block of d = 128,
+    // where shared memory already holds the SM to one CTA; otherwise two
+    static constexpr int NACC = (D == 128 && RB == 1) ? 4 : 2;
+    static constexpr int NBAR = 2 * STAGES + 1 + 2 * NACC;
     static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_TMEM + 16;
     static constexpr int SMEM_ALLOC = SMEM + 1024;
-    static constexpr uint32_t TMEM_COLS = 2 * RB * TK;  // two accumulator buffers of RB blocks
+    static constexpr uint32_t TMEM_COLS = NACC * RB * TK;  // NACC accumulator buffers of RB blocks
     static constexpr uint32_t IDESC = idesc_bf16_f32(128, 128);
     static_assert(ROWS == 128 && TK == 128, "one 128x128 MMA shape for both passes");
     static_assert(RB == 1 || RB == 2, "one or two row blocks per CTA");
@@ -85,7 +88,7 @@ __global__ void __launch_bounds__(ScoreCfg<D, RB>::NT, 1)
     const uint32_t bar_kempty = bar_kfull + 8 * C::STAGES;
     const uint32_t bar_q = bar_kempty + 8 * C::STAGES;
     const uint32_t bar_tfull = bar_q + 8;
-    const uint32_t bar_tempty = bar_tfull + 16;
+    const uint32_t bar_tempty = bar_tfull + 8 * C::NACC;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM);
     __shared__ int s_abort;
     __shared__ int s_last;
@@ -100,7 +103,7 @@ __global__ void __launch_bounds__(ScoreCfg<D, RB>::NT, 1)
     const int ntiles = (hi - lo + C::TK - 1) / C::TK;
     const int row_base = mg * C::GROWS;   // first window row (of R = G * W) of this CTA
 
-    if (tid == 0) {
+    if (!PASS2 && tid == 0) {
         // the first stages' K tiles and this CTA's window rows into L2 while the
         // previous kernel finishes
         prefetch_tmap(&tmk);
@@ -123,7 +126,7 @@ __global__ void __launch_bounds__(ScoreCfg<D, RB>::NT, 1)
             mbar_init(bar_kempty + 8 * s, 1);
         }
         mbar_init(bar_q, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < C::NACC; ++i) {
             mbar_init(bar_tfull + 8 * i, 1);
             mbar_init(bar_tempty + 8 * i, C::NEPI / 2);   // one epilogue group per buffer
         }
@@ -137,7 +140,14 @@ __global__ void __launch_bounds__(ScoreCfg<D, RB>::NT, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    griddep_wait();
+    // Pass 2 always follows pass 1 of the same call, which writes only the row
+    // statistics (read by the epilogue) and never K or the window rows.  Its
+    // producer and MMA warps therefore start before the grid dependency resolves:
+    // every pass-1 CTA has passed its own wait before any pass-2 CTA starts, so
+    // the caller's K and window rows are complete, and the first tiles stream
+    // from L2 into shared memory and tensor memory while the last pass-1 CTAs
+    // finish.  Only the epilogue waits.
+    if (!PASS2 || warp >= 2) griddep_wait();
     griddep_launch();
     volatile int* abort_flag = &s_abort;
 
@@ -176,9 +186,9 @@ __global__ void __launch_bounds__(ScoreCfg<D, RB>::NT, 1)
         if (lane == 0) {
             bool ok = mbar_wait(bar_q, 0);
             for (int t = 0; ok && t < ntiles; ++t) {
-                const int s = t % C::STAGES, buf = t & 1;
+                const int s = t % C::STAGES, buf = t % C::NACC;
                 ok = mbar_wait(bar_kfull + 8 * s, (t / C::STAGES) & 1);
-                if (ok && t >= 2) ok = mbar_wait(bar_tempty + 8 * buf, ((t >> 1) & 1) ^ 1);
+                if (ok && t >= C::NACC) ok = mbar_wait(bar_tempty + 8 * buf, ((t / C::NACC) & 1) ^ 1);
                 if (!ok || *abort_flag) break;
                 tc_fence_after();
                 const uint32_t kst = sbase + C::OFF_K + s * C::TILE_B;
@@ -242,15 +252,18 @@ __global__ void __launch_bounds__(ScoreCfg<D, RB>::NT, 1)
                         v2[u] = sidx < p.nsplit ? __ldcg(reinterpret_cast<const float2*>(base + sidx * stride))
                                                 : make_float2(-INFINITY, 0.f);
                     }
+                    // the batch's max first, so that its sixteen exponentials are independent
+                    float bm = -INFINITY;
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        if (v2[u].x == -INFINITY) continue;
-                        if (v2[u].x > mm) {
-                            ll = ll * fast_exp2(mm - v2[u].x) + v2[u].y;
-                            mm = v2[u].x;
-                        } else {
-                            ll += v2[u].y * fast_exp2(v2[u].x - mm);
-                        }
+                    for (int u = 0; u < 16; ++u) bm = fmaxf(bm, v2[u].x);
+                    if (bm != -INFINITY) {
+                        const float mnew = fmaxf(mm, bm);
+                        float acc = (mm == -INFINITY) ? 0.f : ll * fast_exp2(mm - mnew);
+#pragma unroll
+                        for (int u = 0; u < 16; ++u)
+                            acc += (v2[u].x == -INFINITY) ? 0.f : v2[u].y * fast_exp2(v2[u].x - mnew);
+                        ll = acc;
+                        mm = mnew;
                     }
                 }
             }
@@ -286,13 +299,13 @@ __global__ void __launch_bounds__(ScoreCfg<D, RB>::NT, 1)
         bool aborted = false;
 
         // Epilogue group `half` (warps 2-5 or 6-9) takes the tiles of its parity,
-        // i.e. always accumulator buffer `half` (RB accumulators of 128 columns);
-        // the two groups never meet inside the loop.  Columns are read 64 at a
+        // i.e. only accumulator buffers of that parity (RB accumulators of 128
+        // columns each); the two groups never meet inside the loop.  Columns are read 64 at a
         // time; the buffer is handed back to the MMA issuer as soon as its last
         // columns are loaded.
         for (int t = half; t < ntiles; t += 2) {
-            const int buf = t & 1;
-            if (!mbar_wait(bar_tfull + 8 * buf, (t >> 1) & 1)) {
+            const int buf = t % C::NACC;
+            if (!mbar_wait(bar_tfull + 8 * buf, (t / C::NACC) & 1)) {
                 aborted = true;
                 break;
             }
