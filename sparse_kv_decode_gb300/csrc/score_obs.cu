@@ -40,12 +40,12 @@ struct ScoreParams {
     float* sc_part;   // [n_mg][BH][n]
 };
 
-template <int D, int RB>
+template <int D, int RB, int ST>
 struct ScoreCfg {
     static constexpr int ROWS = 128;              // window rows per row block (MMA M or N)
     static constexpr int GROWS = RB * ROWS;       // window rows per CTA: RB row blocks share each K tile
     static constexpr int TK = 128;                // keys per tile (MMA N or M)
-    static constexpr int STAGES = 3;
+    static constexpr int STAGES = ST;             // K stages (three, or five for d = 128 with one row block: chosen at launch)
     static constexpr int HALVES = D / 64;         // 128-byte K-blocks per row
     static constexpr int NEPI = 8;                // epilogue warps
     static constexpr int NET = NEPI * 32;
@@ -72,13 +72,14 @@ struct ScoreCfg {
     static_assert(ROWS == 128 && TK == 128, "one 128x128 MMA shape for both passes");
     static_assert(RB == 1 || RB == 2, "one or two row blocks per CTA");
     static_assert(GROWS <= NET, "one epilogue thread per window row of the CTA");
+    static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory of one CTA");
 };
 
-template <int D, bool PASS2, int RB>
-__global__ void __launch_bounds__(ScoreCfg<D, RB>::NT, 1)
+template <int D, bool PASS2, int RB, int ST>
+__global__ void __launch_bounds__(ScoreCfg<D, RB, ST>::NT, 1)
     score_kernel(const __grid_constant__ ScoreParams p, const __grid_constant__ CUtensorMap tmk,
                  const __grid_constant__ CUtensorMap tmq) {
-    using C = ScoreCfg<D, RB>;
+    using C = ScoreCfg<D, RB, ST>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem =
         reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -554,11 +555,11 @@ ScorePlan score_plan(int B, int Hq, int Hkv, int n, int W, int num_sms) {
     return pl;
 }
 
-template <int D, bool PASS2, int RB>
+template <int D, bool PASS2, int RB, int ST>
 cudaError_t launch_score_pass(const ScoreParams& p, const CUtensorMap& tmk, const CUtensorMap& tmq, int grid,
                               cudaStream_t st) {
-    using C = ScoreCfg<D, RB>;
-    auto kern = score_kernel<D, PASS2, RB>;
+    using C = ScoreCfg<D, RB, ST>;
+    auto kern = score_kernel<D, PASS2, RB, ST>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -620,19 +621,25 @@ int launch_score(const ScoreLaunch& a, const CUtensorMap* tmk, const CUtensorMap
     cudaError_t e;
     if (a.d == 128) {
         if (pl.rb == 2) {
-            e = launch_score_pass<128, false, 2>(p, *tmk, *tmq, grid, a.stream);
-            if (e == cudaSuccess) e = launch_score_pass<128, true, 2>(p, *tmk, *tmq, grid, a.stream);
+            e = launch_score_pass<128, false, 2, 3>(p, *tmk, *tmq, grid, a.stream);
+            if (e == cudaSuccess) e = launch_score_pass<128, true, 2, 3>(p, *tmk, *tmq, grid, a.stream);
         } else {
-            e = launch_score_pass<128, false, 1>(p, *tmk, *tmq, grid, a.stream);
-            if (e == cudaSuccess) e = launch_score_pass<128, true, 1>(p, *tmk, *tmq, grid, a.stream);
+            // K stages with one row block of d = 128: pass 2 fills five stages (and the
+            // four accumulators) while pass 1 finishes; pass 1 streams from HBM, where
+            // five stages pay off only for long splits (128K: 84.8 -> 83.3 us per
+            // layer) and cost time for short ones (32K: 24.6 -> 25.1 us)
+            const bool long_split = (pl.chunk + 127) / 128 >= 32;
+            e = long_split ? launch_score_pass<128, false, 1, 5>(p, *tmk, *tmq, grid, a.stream)
+                           : launch_score_pass<128, false, 1, 3>(p, *tmk, *tmq, grid, a.stream);
+            if (e == cudaSuccess) e = launch_score_pass<128, true, 1, 5>(p, *tmk, *tmq, grid, a.stream);
         }
     } else {
         if (pl.rb == 2) {
-            e = launch_score_pass<64, false, 2>(p, *tmk, *tmq, grid, a.stream);
-            if (e == cudaSuccess) e = launch_score_pass<64, true, 2>(p, *tmk, *tmq, grid, a.stream);
+            e = launch_score_pass<64, false, 2, 3>(p, *tmk, *tmq, grid, a.stream);
+            if (e == cudaSuccess) e = launch_score_pass<64, true, 2, 3>(p, *tmk, *tmq, grid, a.stream);
         } else {
-            e = launch_score_pass<64, false, 1>(p, *tmk, *tmq, grid, a.stream);
-            if (e == cudaSuccess) e = launch_score_pass<64, true, 1>(p, *tmk, *tmq, grid, a.stream);
+            e = launch_score_pass<64, false, 1, 3>(p, *tmk, *tmq, grid, a.stream);
+            if (e == cudaSuccess) e = launch_score_pass<64, true, 1, 3>(p, *tmk, *tmq, grid, a.stream);
         }
     }
     if (e != cudaSuccess) {
