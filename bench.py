@@ -26,6 +26,7 @@ import json  # noqa: E402
 import math  # noqa: E402
 import subprocess  # noqa: E402
 import sys  # noqa: E402
+import tempfile  # noqa: E402
 import time  # noqa: E402
 
 import numpy as np  # noqa: E402
@@ -57,6 +58,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (small profiling cases only; reported in config)")
     ap.add_argument("--no-next", action="store_true", help="skip the timings of the next rows (f1..f4)")
+    ap.add_argument("--clocks-log", default="",
+                    help="file for the raw nvidia-smi samples of the timed region (default: a temporary file)")
     return ap.parse_args()
 
 
@@ -108,11 +111,12 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self):
+    def __init__(self, path=""):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench.csv")
+        self.keep = bool(path)
+        self.path = path or os.path.join(tempfile.gettempdir(), "sdkv_clocks_%d.csv" % os.getpid())
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            os.makedirs(os.path.dirname(os.path.abspath(self.path)), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
                                           "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
@@ -142,6 +146,8 @@ class ClockSampler:
                 if uuid and parts[1] and uuid not in parts[1]:
                     continue
                 rows.append((ts, parts))
+        if not self.keep:
+            os.remove(self.path)
         win = [p for ts, p in rows if ts is None or (t0 - 0.3 <= ts <= t1 + 0.3)] or [p for _, p in rows]
         if not win:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
@@ -599,7 +605,7 @@ def run_sdkv(args, world, rank, local):
         uuid = str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         pass
-    sampler = ClockSampler()
+    sampler = ClockSampler(args.clocks_log)
     time.sleep(0.25)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(Path.PHASES) + 1)] for _ in range(K)]
     start = torch.cuda.Event(enable_timing=True)
