@@ -246,6 +246,8 @@ def test_sparse_bad_index_is_flagged_not_faulted():
     (1, 28, 4, 128, 1300, 40, 1260),     # group 7 x window 40 = 280 rows: three row blocks
     (1, 4, 1, 64, 200, 64, 136),         # 256 rows: two full row blocks
     (1, 8, 2, 64, 1001, 48, 950),        # 192 rows: two row blocks, odd key count (unaligned rows)
+    (4, 16, 16, 128, 9000, 32, 8968),    # 64 heads, two splits of 36 tiles: five-stage pass 1
+    (8, 20, 20, 128, 4200, 32, 4100),    # 160 heads, one split of 33 tiles, window before the end
 ])
 def test_score_matches_oracle(B, Hq, Hkv, d, n, W, q_pos0):
     g = torch.Generator().manual_seed(n + W)
