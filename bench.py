@@ -15,7 +15,7 @@ instead (the reference arm: a deliberately slow program, on a bounded sample).
 """
 import os
 
-# The oracle's CPU baseline runs single-threaded BLAS (reported as cores = 1).
+# The oracle's CPU timing runs one single-threaded BLAS per worker process.
 for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
@@ -325,48 +325,134 @@ def traffic_from_profiles(phase):
 
 
 # ----------------------------------------------------------------------------- CPU oracle timing
-def oracle_units(w, layer_fn, n_units, rng_seed=0):
-    """Seconds per unit of the oracle on `n_units` sampled (layer, sequence, KV
-    head) units.  A unit is the whole path of one KV head: its window scores,
-    its top-K list, and the sparse and dense decode of its G query heads."""
+def _oracle_unit(w, kk, vv, qo, qq):
+    """The whole path of one KV head through the oracle: its window scores, its
+    top-K list, and the sparse and dense decode of its G query heads."""
     import oracle
-    L, B, Hkv = w.layers, w.batch, w.hkv
-    G = w.hq // w.hkv
-    rng = np.random.default_rng(rng_seed)
-    units = [(int(rng.integers(L)), int(rng.integers(B)), int(rng.integers(Hkv))) for _ in range(n_units)]
     kh = w.keep[0] if w.keep else w.avg_budget
+    sc = oracle.score_obs_window(qo, kk, w.n, w.q_pos0)
+    offs = np.array([0, kh])
+    idx = oracle.select_topk(sc, w.n, w.cand_lo, w.cand_hi, w.n_sink, w.n_recent, offs)
+    oracle.sparse_decode(qq, kk, vv, offs, idx)
+    oracle.dense_verify(qq[:, :, None, :], kk, vv, w.n - 1)
+
+
+def _unit_inputs(w, lay, b, h):
+    G = w.hq // w.hkv
+    return (lay["k"][b:b + 1, h:h + 1].cpu(), lay["v"][b:b + 1, h:h + 1].cpu(),
+            lay["q_obs"][b:b + 1, h * G:(h + 1) * G].cpu(), lay["q"][b:b + 1, h * G:(h + 1) * G].cpu())
+
+
+def oracle_units(w, layer_fn, n_units, rng_seed=0):
+    """Seconds per unit of the oracle in this process on `n_units` sampled
+    (layer, sequence, KV head) units."""
+    rng = np.random.default_rng(rng_seed)
+    units = [(int(rng.integers(w.layers)), int(rng.integers(w.batch)), int(rng.integers(w.hkv)))
+             for _ in range(n_units)]
     total = 0.0
     for (l, b, h) in units:
-        lay = layer_fn(l)
-        kk = lay["k"][b:b + 1, h:h + 1].cpu()
-        vv = lay["v"][b:b + 1, h:h + 1].cpu()
-        qo = lay["q_obs"][b:b + 1, h * G:(h + 1) * G].cpu()
-        qq = lay["q"][b:b + 1, h * G:(h + 1) * G].cpu()
+        args = _unit_inputs(w, layer_fn(l), b, h)
         t0 = time.perf_counter()
-        sc = oracle.score_obs_window(qo, kk, w.n, w.q_pos0)
-        offs = np.array([0, kh])
-        idx = oracle.select_topk(sc, w.n, w.cand_lo, w.cand_hi, w.n_sink, w.n_recent, offs)
-        oracle.sparse_decode(qq, kk, vv, offs, idx)
-        oracle.dense_verify(qq[:, :, None, :], kk, vv, w.n - 1)
+        _oracle_unit(w, *args)
         total += time.perf_counter() - t0
     return total / n_units
 
 
+def host_cores():
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def _oracle_worker(name, layer, units, rounds, barrier, out_q):
+    """One host core (one process, one BLAS thread): its units of one layer,
+    timed `rounds` times; every round starts at a barrier of all workers."""
+    try:
+        w = workloads.by_name(name)
+        lay = workloads.make_layer(w, layer, device="cpu")
+        data = [_unit_inputs(w, lay, b, h) for (b, h) in units]
+        del lay
+        res = []
+        for _ in range(rounds):
+            barrier.wait(timeout=300)
+            t0 = time.time()
+            for args in data:
+                _oracle_unit(w, *args)
+            res.append((t0, time.time(), len(data)))
+        out_q.put((res, None))
+    except Exception as e:
+        barrier.abort()   # release the other workers at once
+        out_q.put((None, repr(e)))
+
+
+def oracle_parallel(w, cores, per_worker, rounds, timeout=900.0):
+    """Seconds per unit, per round, of the oracle run by `cores` worker
+    processes at once (started with spawn), each on `per_worker` sampled
+    (sequence, KV head) units of its own layer: the wall time of the round over
+    the units all workers processed."""
+    import multiprocessing as mp
+    import queue
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(cores)
+    out_q = ctx.Queue()
+    rng = np.random.default_rng(7)
+    procs = []
+    for i in range(cores):
+        units = [(int(rng.integers(w.batch)), int(rng.integers(w.hkv))) for _ in range(per_worker)]
+        p = ctx.Process(target=_oracle_worker, args=(w.name, (7 * i) % w.layers, units, rounds, barrier, out_q),
+                        daemon=True)
+        p.start()
+        procs.append(p)
+    results, deadline = [], time.time() + timeout
+    try:
+        while len(results) < cores:
+            try:
+                res, err = out_q.get(timeout=5)
+            except queue.Empty:
+                if time.time() > deadline or any(p.exitcode not in (None, 0) for p in procs):
+                    raise RuntimeError("an oracle worker died or timed out")
+                continue
+            if err is not None:
+                raise RuntimeError("oracle worker: " + err)
+            results.append(res)
+    finally:
+        for p in procs:
+            p.join(timeout=30)
+            if p.is_alive():
+                p.terminate()
+    per_round = []
+    for r in range(rounds):
+        t0 = min(res[r][0] for res in results)
+        t1 = max(res[r][1] for res in results)
+        per_round.append((t1 - t0) / sum(res[r][2] for res in results))
+    return per_round
+
+
 def cpu_baseline(w, layer_fn, seconds):
+    """The oracle on all host cores: one worker process per core, each timing
+    a bounded sample of whole-path units; scaled to one step of the workload.
+    Falls back to one core (and says so) if worker processes cannot run."""
     per_unit = oracle_units(w, layer_fn, 1)
-    n_units = max(1, min(64, int(seconds / max(per_unit, 1e-3))))
-    per_unit = oracle_units(w, layer_fn, n_units, rng_seed=1)
+    per_worker = max(1, min(8, int(seconds / max(per_unit, 1e-3))))
     units_per_step = w.layers * w.batch * w.hkv
-    return {
-        "value": per_unit * units_per_step * 1e6,
-        "unit": UNIT,
-        "cores": 1,
-        "kind": "oracle",
-        "sample": "%d (layer, sequence, KV head) units of the %s workload, each the whole path for one KV "
-                  "head (scores, top-K list, sparse and dense decode of its %d query heads), fp64 numpy, "
-                  "one BLAS thread; scaled by %d units per step" % (n_units, w.name, w.hq // w.hkv,
-                                                                    units_per_step),
-    }
+    what = ("whole path for one KV head (scores, top-K list, sparse and dense decode of its %d query heads), "
+            "fp64 numpy" % (w.hq // w.hkv))
+    cores = host_cores()
+    try:
+        per_unit = oracle_parallel(w, cores, per_worker, 1)[0]
+        sample = ("%d (sequence, KV head) units of the %s workload on each of %d worker processes (one per host "
+                  "core, one BLAS thread each, one layer each), timed together; a unit is the %s; wall time "
+                  "over units, scaled by %d units per step" % (per_worker, w.name, cores, what, units_per_step))
+    except Exception as e:   # no worker processes: this process alone
+        cores = 1
+        per_worker = max(1, min(64, int(seconds / max(per_unit, 1e-3))))
+        per_unit = oracle_units(w, layer_fn, per_worker, rng_seed=1)
+        sample = ("%d (layer, sequence, KV head) units of the %s workload in one process (worker processes "
+                  "failed: %s); a unit is the %s; scaled by %d units per step"
+                  % (per_worker, w.name, e, what, units_per_step))
+    return {"value": per_unit * units_per_step * 1e6, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": sample}
 
 
 # ----------------------------------------------------------------------------- arms
@@ -374,30 +460,37 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     w = workloads.by_name(args.workload)
-    cache = {}
-
-    def layer_fn(l):
-        if l not in cache:
-            cache.clear()
-            cache[l] = workloads.make_layer(w, l, device="cpu")
-        return cache[l]
-
     warm = max(args.warmup, 3)
-    samples = []
-    for i in range(warm + args.steps):
-        per = oracle_units(w, layer_fn, 2, rng_seed=100 + i)
-        if i >= warm:
-            samples.append(per)
     units_per_step = w.layers * w.batch * w.hkv
-    us = float(np.mean(samples)) * units_per_step * 1e6
+    cores = host_cores()
+    try:
+        # every step: one whole-path unit on each host core, all cores at once
+        per_round = oracle_parallel(w, cores, 1, warm + args.steps)
+        note = ("fp64 CPU oracle on %d worker processes (one per host core, one BLAS thread each); each step "
+                "times one sampled (sequence, KV head) unit of the whole path per worker, all at once, and "
+                "scales the wall time per unit to the full step" % cores)
+    except Exception as e:
+        cores = 1
+        cache = {}
+
+        def layer_fn(l):
+            if l not in cache:
+                cache.clear()
+                cache[l] = workloads.make_layer(w, l, device="cpu")
+            return cache[l]
+
+        per_round = [oracle_units(w, layer_fn, 2, rng_seed=100 + i) for i in range(warm + args.steps)]
+        note = ("fp64 CPU oracle in one process (worker processes failed: %s); each step times 2 sampled "
+                "(layer, sequence, KV head) units of the whole path and scales to the full step" % e)
+    us = float(np.mean(per_round[warm:])) * units_per_step * 1e6
     line = {
         "impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": warm, "ms_per_step": us / 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "note": "fp64 CPU oracle; each step times 2 sampled (layer, "
-                   "sequence, KV head) units of the whole path and scales to the full step"},
-        "cpu_baseline": {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": "2 (layer, sequence, KV head) units per step, scaled by %d" % units_per_step},
+        "config": {"workload": w.name, "note": note},
+        "cpu_baseline": {"value": us, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "%d unit(s) per step on %d core(s), scaled by %d units per step"
+                                   % (cores, cores, units_per_step)},
         "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
