@@ -314,25 +314,32 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, KIND>::NT)
     if (warp >= C::NCW) {
         if constexpr (KIND == kGather) {
             // Gather: the NPW producer warps own 32 tile rows each; lane j of a warp
-            // holds the list entry of its warp's row j (loaded one tile ahead), and
-            // CPR lanes copy one row as CPR 16-byte chunks per instruction.
+            // holds the list entry of its warp's row j, loaded STAGES tiles ahead (a
+            // register ring), so the first stages' gathers do not each wait for an
+            // index load; CPR lanes copy one row as CPR 16-byte chunks per instruction.
             constexpr int CPR = D / 8;           // 16-byte chunks per row
             constexpr int RPI = 32 / CPR;        // rows per warp instruction
             const int pw = warp - C::NCW;
             const bf16* kb = p.k + b * p.sb + h * p.sh;
             const bf16* vb = p.v + b * p.sb + h * p.sh;
+            // the loads are issued early; an entry is checked (a branch on its value)
+            // only when its tile is gathered, so no load is waited for where it is issued
             auto load_idx = [&](int t) -> int {
                 const int pos = min(lo + t * TK + pw * 32 + lane, hi - 1);
-                int idx = (t < ntiles) ? __ldg(p.indices + pos) : 0;
-                if (static_cast<unsigned>(idx) >= static_cast<unsigned>(p.n_cap)) {
-                    flag_status(p.status, SDKV_DEV_BAD_INDEX);
-                    idx = 0;
-                }
-                return idx;
+                return (t < ntiles) ? __ldg(p.indices + pos) : 0;
             };
-            int idx_cur = load_idx(0);
+            int idx_ring[STAGES];   // entries of tiles t .. t + STAGES - 1
+#pragma unroll
+            for (int j = 0; j < STAGES; ++j) idx_ring[j] = load_idx(j);
             for (int t = 0; t < ntiles; ++t) {
-                const int idx_next = load_idx(t + 1);
+                int idx_cur = idx_ring[0];
+                if (static_cast<unsigned>(idx_cur) >= static_cast<unsigned>(p.n_cap)) {
+                    flag_status(p.status, SDKV_DEV_BAD_INDEX);
+                    idx_cur = 0;
+                }
+#pragma unroll
+                for (int j = 0; j + 1 < STAGES; ++j) idx_ring[j] = idx_ring[j + 1];
+                idx_ring[STAGES - 1] = load_idx(t + STAGES);
                 const int s = t % STAGES;
                 const uint32_t ph = (t / STAGES) & 1;
                 if (t >= STAGES) {
@@ -359,7 +366,6 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, KIND>::NT)
                     cp_async_16(tile_addr<D, TK, SPARSE>(vst, row, chunk), vb + off);
                 }
                 cp_async_mbar_arrive(bar_full + 8 * s);
-                idx_cur = idx_next;
             }
             cp_async_wait_all();
         } else {
