@@ -123,12 +123,12 @@ __global__ void __launch_bounds__(256) compact_kv_kernel(const bf16* __restrict_
             if (p >= rows_cap) {
                 flag_status(status, SDKV_DEV_BAD_LIST);
             } else {
+                int idx = indices[off0 + p];   // in flight during the head search
                 int lo = 0, hi = BH;
                 while (lo < hi) {
                     const int mid = (lo + hi) >> 1;
                     if (__ldg(offsets + mid + 1) - off0 > p) hi = mid; else lo = mid + 1;
                 }
-                int idx = indices[off0 + p];
                 if (static_cast<unsigned>(idx) >= static_cast<unsigned>(n_cap)) {
                     flag_status(status, SDKV_DEV_BAD_INDEX);
                     idx = 0;
