@@ -51,6 +51,28 @@ def test_reference_arm_prints_one_json_line():
     assert rec["warmup"] >= 3
 
 
+def test_cpu_baseline_on_worker_processes():
+    import bench
+    w = workloads.by_name("tiny")
+    lay = workloads.make_layer(w, 0, device="cpu")
+    rec = bench.cpu_baseline(w, lambda l: lay, 0.5)
+    assert rec["kind"] == "oracle" and rec["value"] > 0
+    assert rec["cores"] == bench.host_cores() and "worker processes" in rec["sample"]
+
+
+def test_cpu_baseline_falls_back_to_one_process(monkeypatch):
+    import bench
+
+    def no_workers(*args, **kwargs):
+        raise RuntimeError("no workers here")
+
+    monkeypatch.setattr(bench, "oracle_parallel", no_workers)
+    w = workloads.by_name("tiny")
+    lay = workloads.make_layer(w, 0, device="cpu")
+    rec = bench.cpu_baseline(w, lambda l: lay, 0.5)
+    assert rec["cores"] == 1 and rec["value"] > 0 and "no workers here" in rec["sample"]
+
+
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))
