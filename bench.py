@@ -304,7 +304,10 @@ def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_kv_decode_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
+        path = os.path.join(csrc, name)
+        if not os.path.isfile(path):
+            continue
+        with open(path, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 

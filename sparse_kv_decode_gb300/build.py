@@ -46,7 +46,10 @@ def _digest(extra: str) -> str:
     h = hashlib.sha256(extra.encode())
     for d in (CSRC, os.path.join(ROOT, "include")):
         for name in sorted(os.listdir(d)):
-            with open(os.path.join(d, name), "rb") as f:
+            path = os.path.join(d, name)
+            if not os.path.isfile(path):
+                continue
+            with open(path, "rb") as f:
                 h.update(name.encode())
                 h.update(f.read())
     return h.hexdigest()
