@@ -312,9 +312,10 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def traffic_from_profiles(phase):
+def traffic_from_profiles(phase, workload):
     """DRAM bytes per launch from profiles/dram_traffic.txt, if they were taken
-    with the current kernel sources (same source hash), else None."""
+    with the current kernel sources (same source hash) on this workload's
+    full-size launch, else None."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -322,7 +323,8 @@ def traffic_from_profiles(phase):
     with open(path) as f:
         for line in f:
             parts = line.split()
-            if len(parts) >= 3 and not line.startswith("#") and parts[0] == phase and parts[2] == cur:
+            if (len(parts) >= 4 and not line.startswith("#") and parts[0] == phase and parts[2] == cur
+                    and parts[3] == workload):
                 return float(parts[1])
     return None
 
@@ -744,7 +746,7 @@ def run_sdkv(args, world, rank, local):
                     "sparse": "sdkv_sparse_decode_attn (attn_splitk_kernel, gathered)",
                     "dense": "sdkv_dense_verify_attn (attn_splitk_kernel, dense)"}
     roofline = {"bound": "hbm", "achieved": dom["gbs"], "peak": hbm_peak, "unit": "GB/s",
-                "frac": dom["gbs"] / hbm_peak, "traffic": traffic_from_profiles(dominant),
+                "frac": dom["gbs"] / hbm_peak, "traffic": traffic_from_profiles(dominant, w.name),
                 "kernel": kernel_names[dominant], "peak_kind": peak_kind,
                 "alg_bytes_per_launch": dom["alg_bytes_per_layer"], "us_per_launch": dom["us_per_layer"]}
     keep = ("%d" % w.keep[args.keep_index]) if w.keep else "ragged SparseMM budgets"
