@@ -6,16 +6,23 @@
 // positions, causal among the drafts) ride on the same pass over the rows, so
 // the cache is read exactly once.
 // Sparse (StD 3.2, ByteCross "Speedup Across Context"): every CTA takes one
-// chunk of one (batch, KV head)'s selected-index list and gathers those rows.
+// chunk of one (batch, KV head)'s selected-index list and gathers those rows;
+// the contiguous kind streams the same chunks from buffers the rows were
+// compacted into (ByteCross's deployment).
 //
-// CTA layout: one producer warp streams K and V tiles into a ring of shared
-// memory stages (TMA tensor copies with 128-byte swizzle for dense rows,
-// per-row bulk copies for gathered rows), completing on mbarriers; the
-// consumer warps run QK^T and PV on mma.sync (bf16 in, fp32 accumulate) with
-// an online softmax in the log2 domain.  Each CTA leaves an unnormalised
-// partial (o, m, l) per query row; the last CTA of a head to finish (atomic
-// ticket, no waiting) merges the partials with the log-sum-exp rule
-//     o = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s,   M = max_s m_s.
+// CTA layout: producer warps fill a ring of shared-memory stages (128-byte
+// swizzle), completing on mbarriers: one warp issuing TMA tensor copies for
+// dense and compacted rows, or two warps issuing 16-byte cp.async copies of
+// the listed rows (list entries loaded a ring of stages ahead).  The consumer
+// warps run QK^T and PV on mma.sync (bf16 in, fp32 accumulate) with an online
+// softmax in the log2 domain, each over its own key group of every stage.
+// Merging the unnormalised partials (o, m, l) with the log-sum-exp rule
+//     o = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s,   M = max_s m_s
+// takes up to three levels: the key groups of a CTA in shared memory; the
+// CTAs of a cluster (2 to 8) through distributed shared memory, each CTA
+// reducing a slice of the head dims; and, when a head spans several clusters
+// (or several CTAs without a cluster), the last of them to finish (atomic
+// ticket, no waiting) merges their partials from global memory.
 #include "sdkv_common.cuh"
 #include "sdkv_internal.h"
 

@@ -5,6 +5,7 @@
 //                   "Streaming"; ByteCross "The Attention Baseline")
 //   append_drafts   a draft step's lists: the base selection plus the positions
 //                   drafted so far (StD 3.1)
+//   draft_lists     the lists of all gamma draft steps of a round in one launch
 //   compact_kv      the selected rows of every head gathered once into
 //                   contiguous buffers (ByteCross "Speedup Across Context")
 //   specvlm         importance = mean of the verifier's attention maps; Stage I

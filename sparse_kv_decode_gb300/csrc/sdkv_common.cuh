@@ -1,5 +1,7 @@
-// Shared device helpers of libsdkv: PTX wrappers for mbarriers, bulk / tensor
-// copies (TMA), ldmatrix + mma.sync, bounded waits, and the workspace layout.
+// Shared device helpers of libsdkv: PTX wrappers for mbarriers (with bounded
+// waits), tensor copies and L2 prefetches (TMA), cp.async, ldmatrix + mma.sync,
+// tcgen05 MMA and tensor memory, distributed shared memory, paired fp32
+// arithmetic, programmatic dependent launch, and the workspace layout.
 #pragma once
 
 #include <cuda.h>
