@@ -370,7 +370,7 @@ def host_cores():
         return max(1, os.cpu_count() or 1)
 
 
-def _oracle_worker(name, layer, units, rounds, barrier, out_q):
+def _oracle_worker(name, layer, units, rounds, start_bar, out_q):
     """One host core (one process, one BLAS thread): its units of one layer,
     timed `rounds` times; every round starts at a barrier of all workers."""
     try:
@@ -380,14 +380,14 @@ def _oracle_worker(name, layer, units, rounds, barrier, out_q):
         del lay
         res = []
         for _ in range(rounds):
-            barrier.wait(timeout=300)
+            start_bar.wait(timeout=300)
             t0 = time.time()
             for args in data:
                 _oracle_unit(w, *args)
             res.append((t0, time.time(), len(data)))
         out_q.put((res, None))
     except Exception as e:
-        barrier.abort()   # release the other workers at once
+        start_bar.abort()   # release the other workers at once
         out_q.put((None, repr(e)))
 
 
@@ -399,13 +399,13 @@ def oracle_parallel(w, cores, per_worker, rounds, timeout=900.0):
     import multiprocessing as mp
     import queue
     ctx = mp.get_context("spawn")
-    barrier = ctx.Barrier(cores)
+    start_bar = ctx.Barrier(cores)
     out_q = ctx.Queue()
     rng = np.random.default_rng(7)
     procs = []
     for i in range(cores):
         units = [(int(rng.integers(w.batch)), int(rng.integers(w.hkv))) for _ in range(per_worker)]
-        p = ctx.Process(target=_oracle_worker, args=(w.name, (7 * i) % w.layers, units, rounds, barrier, out_q),
+        p = ctx.Process(target=_oracle_worker, args=(w.name, (7 * i) % w.layers, units, rounds, start_bar, out_q),
                         daemon=True)
         p.start()
         procs.append(p)
