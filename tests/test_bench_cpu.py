@@ -73,6 +73,26 @@ def test_cpu_baseline_falls_back_to_one_process(monkeypatch):
     assert rec["cores"] == 1 and rec["value"] > 0 and "no workers here" in rec["sample"]
 
 
+def test_traffic_figures_only_for_their_sources_and_workload(tmp_path, monkeypatch):
+    import bench
+    csrc = tmp_path / "sparse_kv_decode_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "k.cu").write_text("// kernel\n")
+    (csrc / "__pycache__").mkdir()            # not a regular file: ignored by the hash
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h = bench.kernel_source_hash()
+    (tmp_path / "profiles" / "dram_traffic.txt").write_text(
+        "# phase  bytes_per_call  csrc_hash  workload\n"
+        "score   1.5e+08   %s   llama8b_32k\n"
+        "sparse  4.0e+07   0123456789abcdef   llama8b_32k\n" % h)
+    assert bench.traffic_from_profiles("score", "llama8b_32k") == 1.5e8
+    assert bench.traffic_from_profiles("score", "llama8b_128k") is None   # another workload
+    assert bench.traffic_from_profiles("sparse", "llama8b_32k") is None   # stale sources
+    (csrc / "k.cu").write_text("// kernel, changed\n")
+    assert bench.traffic_from_profiles("score", "llama8b_32k") is None
+
+
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))
