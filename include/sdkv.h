@@ -181,13 +181,18 @@ int sdkv_select_topk(const float* scores, int32_t B, int32_t Hkv, int32_t n,
  *   n_cap    rows per head present in k and v; list entries must lie in
  *            [0, n_cap) (others set SDKV_DEV_BAD_INDEX and read row 0)
  *   offsets, indices  device int32 CSR lists per (b, h), as from sdkv_select_topk
+ *   n_idx    number of int32 entries the `indices` array holds (its length), or
+ *            0.  With n_idx > 0 the kernel, while the previous kernel on
+ *            `stream` finishes, prefetches the offsets and indices[0, n_idx)
+ *            into L2 (prefetches read nothing back; the lists are loaded only
+ *            after that kernel has finished).  n_idx = 0 skips the prefetch.
  *   o        device bf16 [B][Hq][d] (written)
  *   lse      device float [B][Hq] (written) or NULL
  * Needs Hq/Hkv <= 32 and B*Hkv <= 65536.
  */
 int sdkv_sparse_decode_attn(const void* q, const void* k, const void* v,
                             const int64_t kv_strides[3], int32_t n_cap,
-                            const int32_t* offsets, const int32_t* indices,
+                            const int32_t* offsets, const int32_t* indices, int64_t n_idx,
                             int32_t B, int32_t Hq, int32_t Hkv, int32_t d, float scale,
                             void* o, float* lse, void* ws, size_t ws_bytes, void* stream);
 

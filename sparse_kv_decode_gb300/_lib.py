@@ -74,7 +74,7 @@ def lib() -> ctypes.CDLL:
     L.sdkv_select_topk.argtypes = [_c_vp, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_i32,
                                    _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]
     L.sdkv_select_topk.restype = ctypes.c_int
-    L.sdkv_sparse_decode_attn.argtypes = [_c_vp, _c_vp, _c_vp, _I64x3, _c_i32, _c_vp, _c_vp, _c_i32,
+    L.sdkv_sparse_decode_attn.argtypes = [_c_vp, _c_vp, _c_vp, _I64x3, _c_i32, _c_vp, _c_vp, _c_i64, _c_i32,
                                           _c_i32, _c_i32, _c_i32, _c_f, _c_vp, _c_vp, _c_vp, _c_sz, _c_vp]
     L.sdkv_sparse_decode_attn.restype = ctypes.c_int
     L.sdkv_dense_verify_attn.argtypes = [_c_vp, _c_vp, _c_vp, _I64x3, _c_i32, _c_i32, _c_i32, _c_i32,
@@ -204,11 +204,15 @@ def select_topk(scores: torch.Tensor, n: int, cand_lo: int, cand_hi: int, n_sink
 def sparse_decode_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, offsets: torch.Tensor,
                        indices: torch.Tensor, scale: float, o: torch.Tensor | None = None,
                        lse: torch.Tensor | None = None, ws: torch.Tensor | None = None,
-                       want_lse: bool = True):
+                       want_lse: bool = True, early: bool = True):
+    """`early`: pass the length of `indices` as n_idx, so the kernel prefetches the
+    lists into L2 while the previous kernel on the stream finishes."""
     for t, nm in ((q, "q"), (k, "k"), (v, "v")):
         _need(t, nm, torch.bfloat16)
     _need(offsets, "offsets", torch.int32)
     _need(indices, "indices", torch.int32)
+    if not indices.is_contiguous():
+        raise ValueError("indices must be contiguous")
     if not q.is_contiguous():
         raise ValueError("q must be contiguous [B][Hq][d]")
     if k.stride() != v.stride() or k.shape != v.shape:
@@ -222,7 +226,8 @@ def sparse_decode_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, offset
     if ws is None:
         ws = new_workspace(workspace_size(OP_SPARSE_DECODE, B, Hq, Hkv, d, 0, 0), q.device)
     _check(lib().sdkv_sparse_decode_attn(q.data_ptr(), k.data_ptr(), v.data_ptr(), _kv_strides(k), n_cap,
-                                         offsets.data_ptr(), indices.data_ptr(), B, Hq, Hkv, d, scale,
+                                         offsets.data_ptr(), indices.data_ptr(), indices.numel() if early else 0,
+                                         B, Hq, Hkv, d, scale,
                                          o.data_ptr(), _ptr(lse), ws.data_ptr(), ws.numel(), _stream(q)))
     return o, lse
 

@@ -47,6 +47,7 @@ struct AttnParams {
     // sparse
     const int* offsets;
     const int* indices;
+    long long n_idx;   // entries of indices; 0: the lists are not read before the grid dependency resolves
     int n_cap, BH, grid_target, min_chunk;
     // workspace
     int* status;
@@ -120,6 +121,125 @@ __device__ __forceinline__ int block_excl_scan(int v, int* s_scan, int& total) {
     return res;
 }
 
+// Chunk plan of the list decodes, identical in every CTA (all threads call it).
+// Chunk length cl = max(min_chunk, ceil(total / (grid_target - cs * BH)) rounded
+// up to 16).  Without clusters head i owns max(1, ceil(k_i / cl)) consecutive
+// chunk ids of length cl; with clusters of cs CTAs it owns cs * ceil(k_i / (cs *
+// cl)) chunks (a whole number of clusters) of balanced length; trailing ones may
+// be empty.  Either way the chunk count stays within the grid.  The CTA's work
+// item goes to s_work: head, list positions [lo, hi), chunk id, chunks of the
+// head, first chunk of the head (s_work[0] = -1: no chunk for this CTA).
+template <int NT>
+__device__ __forceinline__ void list_plan(const AttnParams& p, int* s_work, int* s_scan, int& s_tot, int& s_off0) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x;
+    const int cs = p.cs;
+    if (p.BH <= 32) {
+        // one warp: each lane a head, the chunk ids by a shuffle scan
+        if (warp == 0) {
+            int start = 0, kh = 0;
+            if (lane < p.BH) {
+                start = __ldcg(p.offsets + lane);
+                kh = __ldcg(p.offsets + lane + 1) - start;
+            }
+            const int off0 = __shfl_sync(0xffffffffu, start, 0);
+            const int total = max(__shfl_sync(0xffffffffu, start + kh, p.BH - 1) - off0, 0);
+            const int slots = max(1, p.grid_target - (cs > 1 ? cs * p.BH : 0));
+            int cl = static_cast<int>(min((static_cast<long long>(total) + slots - 1) / slots, 1ll << 26));
+            cl = max(p.min_chunk, (cl + 15) & ~15);
+            int nch = 0, chl = cl;
+            if (lane < p.BH) {
+                if (kh < 0) {
+                    flag_status(p.status, SDKV_DEV_BAD_LIST);
+                    kh = 0;
+                }
+                if (cs > 1) {
+                    nch = cs * max(1, (kh + cs * cl - 1) / (cs * cl));
+                    chl = (((kh + nch - 1) / nch) + 15) & ~15;
+                } else {
+                    nch = max(1, (kh + cl - 1) / cl);
+                }
+            }
+            int incl = nch;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const int first = incl - nch;
+            const bool mine = lane < p.BH && c >= first && c < first + nch;
+            if (mine) {
+                const int j = c - first;
+                const int l0 = min(start + j * chl, start + kh);
+                s_work[0] = lane;
+                s_work[1] = l0;
+                s_work[2] = max(l0, min(start + (j + 1) * chl, start + kh));
+                s_work[3] = c;
+                s_work[4] = nch;
+                s_work[5] = first;
+            }
+            if (__ballot_sync(0xffffffffu, mine) == 0u && lane == 0) s_work[0] = -1;
+            if (lane == 0) {
+                s_off0 = off0;
+                s_tot = total;
+            }
+        }
+        return;
+    }
+    int start = 0, kh = 0;
+    if (tid < p.BH) {
+        start = __ldcg(p.offsets + tid);
+        kh = __ldcg(p.offsets + tid + 1) - start;
+    }
+    if (tid == 0) {
+        s_off0 = __ldcg(p.offsets);
+        s_tot = __ldcg(p.offsets + p.BH) - s_off0;
+        s_work[0] = -1;
+    }
+    __syncthreads();
+    const int total = max(s_tot, 0);
+    const int slots = max(1, p.grid_target - (cs > 1 ? cs * p.BH : 0));
+    int cl = static_cast<int>(min((static_cast<long long>(total) + slots - 1) / slots, 1ll << 26));
+    cl = max(p.min_chunk, (cl + 15) & ~15);
+    int running = 0;
+    for (int base = 0; base < p.BH; base += NT) {
+        const int i = base + tid;
+        int nch = 0, chl = cl;
+        if (base > 0 && i < p.BH) {
+            start = __ldcg(p.offsets + i);
+            kh = __ldcg(p.offsets + i + 1) - start;
+        }
+        if (i < p.BH) {
+            if (kh < 0) {
+                flag_status(p.status, SDKV_DEV_BAD_LIST);
+                kh = 0;
+            }
+            if (cs > 1) {
+                nch = cs * max(1, (kh + cs * cl - 1) / (cs * cl));
+                chl = (((kh + nch - 1) / nch) + 15) & ~15;
+            } else {
+                nch = max(1, (kh + cl - 1) / cl);
+            }
+        }
+        int tile_total;
+        const int excl = block_excl_scan<NT>(nch, s_scan, tile_total);
+        const int first = running + excl;
+        if (i < p.BH && c >= first && c < first + nch) {
+            const int j = c - first;
+            const int l0 = min(start + j * chl, start + kh);
+            s_work[0] = i;
+            s_work[1] = l0;
+            s_work[2] = max(l0, min(start + (j + 1) * chl, start + kh));
+            s_work[3] = c;
+            s_work[4] = nch;
+            s_work[5] = first;
+        }
+        running += tile_total;
+        __syncthreads();
+        if (s_work[0] >= 0 || running > c) break;
+    }
+}
+
 // Key/value tile address of (row, 16-byte chunk) inside one stage: the 128-byte
 // swizzled layout TMA writes for dense tiles; gathered rows are placed the same way.
 template <int D, int TK, bool SPARSE>
@@ -188,126 +308,32 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, KIND>::NT)
             s_work[5] = bh * p.nsplit;
         }
     }
-    griddep_wait();
-
     if constexpr (SPARSE) {
-        // Chunk plan, identical in every CTA.  Chunk length cl = max(min_chunk,
-        // ceil(total / (grid_target - cs * BH)) rounded up to 16).  Without
-        // clusters head i owns max(1, ceil(k_i / cl)) consecutive chunk ids of
-        // length cl; with clusters of cs CTAs it owns cs * ceil(k_i / (cs * cl))
-        // chunks (a whole number of clusters) of balanced length; trailing ones
-        // may be empty.  Either way the chunk count stays within the grid.
-        if (p.BH <= 32) {
-            // one warp: each lane a head, the chunk ids by a shuffle scan
-            if (warp == 0) {
-                int start = 0, kh = 0;
-                if (lane < p.BH) {
-                    start = p.offsets[lane];
-                    kh = p.offsets[lane + 1] - start;
-                }
-                const int off0 = __shfl_sync(0xffffffffu, start, 0);
-                const int total = max(__shfl_sync(0xffffffffu, start + kh, p.BH - 1) - off0, 0);
-                const int cs = p.cs;
-                const int slots = max(1, p.grid_target - (cs > 1 ? cs * p.BH : 0));
-                int cl = (total + slots - 1) / slots;
-                cl = max(p.min_chunk, (cl + 15) & ~15);
-                int nch = 0, chl = cl;
-                if (lane < p.BH) {
-                    if (kh < 0) {
-                        flag_status(p.status, SDKV_DEV_BAD_LIST);
-                        kh = 0;
-                    }
-                    if (cs > 1) {
-                        nch = cs * max(1, (kh + cs * cl - 1) / (cs * cl));
-                        chl = (((kh + nch - 1) / nch) + 15) & ~15;
-                    } else {
-                        nch = max(1, (kh + cl - 1) / cl);
-                    }
-                }
-                int incl = nch;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += y;
-                }
-                const int first = incl - nch;
-                const int c = blockIdx.x;
-                const bool mine = lane < p.BH && c >= first && c < first + nch;
-                if (mine) {
-                    const int j = c - first;
-                    const int l0 = min(start + j * chl, start + kh);
-                    s_work[0] = lane;
-                    s_work[1] = l0;
-                    s_work[2] = max(l0, min(start + (j + 1) * chl, start + kh));
-                    s_work[3] = c;
-                    s_work[4] = nch;
-                    s_work[5] = first;
-                }
-                if (__ballot_sync(0xffffffffu, mine) == 0u && lane == 0) s_work[0] = -1;
-                if (lane == 0) {
-                    s_off0 = off0;
-                    s_tot = total;
-                }
-            }
-        } else {
-            int start = 0, kh = 0;
-            if (tid < p.BH) {
-                start = p.offsets[tid];
-                kh = p.offsets[tid + 1] - start;
-            }
-            if (tid == 0) {
-                s_off0 = p.offsets[0];
-                s_tot = p.offsets[p.BH] - s_off0;
-                s_work[0] = -1;
-            }
-            __syncthreads();
-            const int total = max(s_tot, 0);
-            const int cs = p.cs;
-            const int slots = max(1, p.grid_target - (cs > 1 ? cs * p.BH : 0));
-            int cl = (total + slots - 1) / slots;
-            cl = max(p.min_chunk, (cl + 15) & ~15);
-            const int c = blockIdx.x;
-            int running = 0;
-            for (int base = 0; base < p.BH; base += C::NT) {
-                const int i = base + tid;
-                int nch = 0, chl = cl;
-                if (base > 0 && i < p.BH) {
-                    start = p.offsets[i];
-                    kh = p.offsets[i + 1] - start;
-                }
-                if (i < p.BH) {
-                    if (kh < 0) {
-                        flag_status(p.status, SDKV_DEV_BAD_LIST);
-                        kh = 0;
-                    }
-                    if (cs > 1) {
-                        nch = cs * max(1, (kh + cs * cl - 1) / (cs * cl));
-                        chl = (((kh + nch - 1) / nch) + 15) & ~15;
-                    } else {
-                        nch = max(1, (kh + cl - 1) / cl);
-                    }
-                }
-                int tile_total;
-                const int excl = block_excl_scan<C::NT>(nch, s_scan, tile_total);
-                const int first = running + excl;
-                if (i < p.BH && c >= first && c < first + nch) {
-                    const int j = c - first;
-                    const int l0 = min(start + j * chl, start + kh);
-                    s_work[0] = i;
-                    s_work[1] = l0;
-                    s_work[2] = max(l0, min(start + (j + 1) * chl, start + kh));
-                    s_work[3] = c;
-                    s_work[4] = nch;
-                    s_work[5] = first;
-                }
-                running += tile_total;
-                __syncthreads();
-                if (s_work[0] >= 0 || running > c) break;
-            }
+        // Before the grid dependency resolves: bring the list offsets and (gathered
+        // kind, n_idx > 0) this CTA's share of the index array, 1/grid of
+        // indices[0, n_idx), into L2, so the plan and the index loads after the
+        // wait hit L2.  Prefetches return nothing, and L2 is where every write
+        // lands, so a line fetched early is never older than what a later load of
+        // it returns.
+        const uint8_t* ob = reinterpret_cast<const uint8_t*>(p.offsets);
+        const long long obytes = 4ll * (p.BH + 1);
+        for (long long x = 128ll * tid; x < obytes; x += 128ll * C::NT) prefetch_l2_line(ob + x);
+        if (KIND == kGather && p.n_idx > 0) {
+            const long long ibytes = 4 * p.n_idx;
+            const long long per = (ibytes + gridDim.x - 1) / gridDim.x;
+            const long long i0 = per * blockIdx.x, i1 = min(ibytes, i0 + per);
+            const uint8_t* ib = reinterpret_cast<const uint8_t*>(p.indices);
+            for (long long x = i0 + 128ll * tid; x < i1; x += 128ll * C::NT) prefetch_l2_line(ib + x);
         }
     }
-    __syncthreads();
+    // This CTA's early work is done.  Once every CTA of the grid is past this
+    // point, the next kernel on the stream may start its own early work in the
+    // slots this grid leaves free; it waits for this grid before using its output.
     griddep_launch();
+    griddep_wait();
+
+    if constexpr (SPARSE) list_plan<C::NT>(p, s_work, s_scan, s_tot, s_off0);
+    __syncthreads();
 
     const int bh = s_work[0];
     if (bh < 0) return;  // no chunk for this CTA (uniform)
@@ -705,9 +731,8 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, KIND>::NT)
             if (ncl_h == 1) return;
             named_bar_sync(1, C::NCT);
             if (tid == 0) {
-                fence_acq_rel_gpu();                       // release this CTA's slice of the partial
-                const int old = atomicAdd(p.tickets + bh * 8 + rank, 1);
-                fence_acq_rel_gpu();                       // acquire the other clusters' (if last)
+                // release this CTA's slice of the partial; acquire the other clusters' (if last)
+                const int old = atom_add_acq_rel_gpu(p.tickets + bh * 8 + rank, 1);
                 s_last = (old == ncl_h - 1);
             }
             named_bar_sync(1, C::NCT);
@@ -763,9 +788,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, KIND>::NT)
     // -------------------------------------------------- last CTA of the head merges the partials
     named_bar_sync(1, C::NCT);
     if (tid == 0) {
-        fence_acq_rel_gpu();                               // release this CTA's partial
-        const int old = atomicAdd(p.tickets + bh, 1);
-        fence_acq_rel_gpu();                               // acquire the others' (if last)
+        const int old = atom_add_acq_rel_gpu(p.tickets + bh, 1);   // release this CTA's partial, acquire the others'
         s_last = (old == nch - 1);
     }
     named_bar_sync(1, C::NCT);
@@ -929,16 +952,66 @@ DensePlan dense_plan(int BH, int n_total, int num_sms) {
     return pl;
 }
 
+// Largest list-decode grid: two CTAs per SM, a whole number of clusters.  It
+// bounds the partial slots of the workspace.
 int sparse_grid_target(int num_sms) { return ((2 * std::max(num_sms, 1)) / kMaxCluster) * kMaxCluster; }
-
-// Clusters for the gathered decode only when every head can own whole clusters
-// and still leave the grid half free for long lists.
-int sparse_cluster(int BH, int grid_target) {
-    for (int cs = kMaxCluster; cs > 1; cs /= 2)
-        if (2 * cs * BH <= grid_target) return cs;
-    return 1;
-}
 int sparse_max_chunks(int BH, int grid_target, int cs) { return cs > 1 ? grid_target : grid_target + BH; }
+
+template <int D, int MT, int KW, int TK, int STAGES, int KIND>
+cudaError_t ensure_smem_attr(int dev) {
+    using C = AttnCfg<D, MT, KW, TK, STAGES, KIND>;
+    static std::atomic<unsigned long long> attr_set{0};  // one bit per device, per instantiation
+    if (attr_done(attr_set, dev)) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(attn_splitk_kernel<D, MT, KW, TK, STAGES, KIND>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+    if (e == cudaSuccess) attr_mark(attr_set, dev);
+    return e;
+}
+
+// CTAs of one instantiation that the current device holds at once when they are
+// launched in clusters of cs (occupancy query, once per device and cluster
+// size).  A grid larger than this runs in two waves, and its last CTAs, which
+// start only when others finish, hold back the next kernel's early start.
+template <int D, int MT, int KW, int TK, int STAGES, int KIND>
+int attn_capacity(int dev, int num_sms, int cs) {
+    using C = AttnCfg<D, MT, KW, TK, STAGES, KIND>;
+    static std::atomic<int> cache[64][4];   // 0: not queried yet
+    const int ci = cs >= 8 ? 3 : cs >= 4 ? 2 : cs >= 2 ? 1 : 0;
+    const bool cached = dev >= 0 && dev < 64;
+    if (cached) {
+        const int v = cache[dev][ci].load(std::memory_order_relaxed);
+        if (v > 0) return v;
+    }
+    int cap = 0;
+    if (ensure_smem_attr<D, MT, KW, TK, STAGES, KIND>(dev) == cudaSuccess) {
+        auto kern = attn_splitk_kernel<D, MT, KW, TK, STAGES, KIND>;
+        if (cs <= 1) {
+            int per_sm = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::NT, C::SMEM_ALLOC) == cudaSuccess)
+                cap = per_sm * num_sms;
+        } else {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(cs * 16);
+            cfg.blockDim = dim3(C::NT);
+            cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = cs;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int ncl = 0;
+            if (cudaOccupancyMaxActiveClusters(&ncl, kern, &cfg) == cudaSuccess) cap = ncl * cs;
+        }
+    }
+    if (cap <= 0) {
+        (void)cudaGetLastError();   // a failed query leaves no error behind; assume two CTAs per SM
+        cap = 2 * std::max(num_sms, 1);
+    }
+    if (cached) cache[dev][ci].store(cap, std::memory_order_relaxed);
+    return cap;
+}
 
 template <int D, int MT, int KW, int TK, int STAGES, int KIND>
 cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tmk, const CUtensorMap& tmv, int grid,
@@ -948,12 +1021,8 @@ cudaError_t launch_attn(const AttnParams& p, const CUtensorMap& tmk, const CUten
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    static std::atomic<unsigned long long> attr_set{0};  // one bit per device, per instantiation
-    if (!attr_done(attr_set, dev)) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
-        if (e != cudaSuccess) return e;
-        attr_mark(attr_set, dev);
-    }
+    e = ensure_smem_attr<D, MT, KW, TK, STAGES, KIND>(dev);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(C::NT);
@@ -1060,21 +1129,33 @@ namespace {
 
 // Sparse decode over index lists (KIND = kGather: rows gathered from the caches)
 // or over the lists' rows compacted into contiguous buffers (KIND = kContig).
-template <int KIND>
-int launch_list_decode(const AttnLaunch& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int num_sms,
-                       const char** why) {
-    AttnParams p = make_params(a);
-    const int BH = a.B * a.Hkv;
-    p.offsets = a.offsets;
-    p.indices = a.indices;
-    p.n_cap = a.n_cap;
-    p.BH = BH;
-    p.grid_target = sparse_grid_target(num_sms);
-    p.min_chunk = 4 * kSparseTK;   // short lists: one cluster per head, no cross-cluster merge
-    p.cs = sparse_cluster(BH, p.grid_target);
+// Clusters only when every head can own whole clusters and still leave the grid
+// half free for long lists; the grid is what one wave of such clusters holds.
+template <int D, int MT, int KW, int KIND>
+int list_decode_launch(AttnParams& p, const AttnLaunch& a, const CUtensorMap& tmk, const CUtensorMap& tmv,
+                       int num_sms, const char** why) {
+    constexpr int TK = kSparseTK, ST = kSparseStages;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        *why = cudaGetErrorString(e);
+        return SDKV_ERR_CUDA;
+    }
+    const int base = sparse_grid_target(num_sms);
+    p.cs = 1;
+    p.grid_target = base;
+    for (int cs = kMaxCluster; cs > 1; cs /= 2) {
+        int cap = std::min(base, attn_capacity<D, MT, KW, TK, ST, KIND>(dev, num_sms, cs));
+        cap -= cap % cs;
+        if (2 * cs * p.BH <= cap) {
+            p.cs = cs;
+            p.grid_target = cap;
+            break;
+        }
+    }
     p.ncl = 1;
-    const int max_chunks = sparse_max_chunks(BH, p.grid_target, p.cs);
-    WsLayout L = attn_ws_layout(a.ws, BH, p.R, a.d, max_chunks);
+    const int max_chunks = sparse_max_chunks(p.BH, p.grid_target, p.cs);
+    WsLayout L = attn_ws_layout(a.ws, p.BH, p.R, a.d, max_chunks);
     if (a.ws_bytes < L.bytes) {
         *why = "workspace smaller than sdkv_workspace_size(SDKV_OP_SPARSE_DECODE, ...)";
         return SDKV_ERR_WORKSPACE;
@@ -1083,26 +1164,37 @@ int launch_list_decode(const AttnLaunch& a, const CUtensorMap& tmk, const CUtens
     p.tickets = L.tickets;
     p.part_o = L.part_o;
     p.part_ml = L.part_ml;
-    const int MT = (p.R + 15) / 16;
-    cudaError_t e = cudaErrorInvalidValue;
-    if (a.d == 128) {
-        switch (MT) {
-            case 1: e = launch_attn<128, 1, 4, kSparseTK, kSparseStages, KIND>(p, tmk, tmv, max_chunks, a.stream, p.cs); break;
-            case 2: e = launch_attn<128, 2, 2, kSparseTK, kSparseStages, KIND>(p, tmk, tmv, max_chunks, a.stream, p.cs); break;
-            default: *why = "Hq/Hkv must be <= 32"; return SDKV_ERR_UNSUPPORTED;
-        }
-    } else {
-        switch (MT) {
-            case 1: e = launch_attn<64, 1, 4, kSparseTK, kSparseStages, KIND>(p, tmk, tmv, max_chunks, a.stream, p.cs); break;
-            case 2: e = launch_attn<64, 2, 2, kSparseTK, kSparseStages, KIND>(p, tmk, tmv, max_chunks, a.stream, p.cs); break;
-            default: *why = "Hq/Hkv must be <= 32"; return SDKV_ERR_UNSUPPORTED;
-        }
-    }
+    e = launch_attn<D, MT, KW, TK, ST, KIND>(p, tmk, tmv, max_chunks, a.stream, p.cs);
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);
         return SDKV_ERR_CUDA;
     }
     return SDKV_OK;
+}
+
+template <int KIND>
+int launch_list_decode(const AttnLaunch& a, const CUtensorMap& tmk, const CUtensorMap& tmv, int num_sms,
+                       const char** why) {
+    AttnParams p = make_params(a);
+    p.offsets = a.offsets;
+    p.indices = a.indices;
+    p.n_idx = a.n_idx;
+    p.n_cap = a.n_cap;
+    p.BH = a.B * a.Hkv;
+    p.min_chunk = 4 * kSparseTK;   // short lists: one cluster per head, no cross-cluster merge
+    const int MT = (p.R + 15) / 16;
+    if (a.d == 128) {
+        switch (MT) {
+            case 1: return list_decode_launch<128, 1, 4, KIND>(p, a, tmk, tmv, num_sms, why);
+            case 2: return list_decode_launch<128, 2, 2, KIND>(p, a, tmk, tmv, num_sms, why);
+            default: *why = "Hq/Hkv must be <= 32"; return SDKV_ERR_UNSUPPORTED;
+        }
+    }
+    switch (MT) {
+        case 1: return list_decode_launch<64, 1, 4, KIND>(p, a, tmk, tmv, num_sms, why);
+        case 2: return list_decode_launch<64, 2, 2, KIND>(p, a, tmk, tmv, num_sms, why);
+        default: *why = "Hq/Hkv must be <= 32"; return SDKV_ERR_UNSUPPORTED;
+    }
 }
 
 }  // namespace

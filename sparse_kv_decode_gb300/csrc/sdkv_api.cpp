@@ -129,7 +129,7 @@ using namespace sdkv;
 
 extern "C" {
 
-int32_t sdkv_version(void) { return 101; }
+int32_t sdkv_version(void) { return 102; }
 
 const char* sdkv_last_error(void) { return g_last_error.c_str(); }
 
@@ -289,8 +289,9 @@ int sdkv_select_topk(const float* scores, int32_t B, int32_t Hkv, int32_t n, int
 }
 
 int sdkv_sparse_decode_attn(const void* q, const void* k, const void* v, const int64_t kv_strides[3], int32_t n_cap,
-                            const int32_t* offsets, const int32_t* indices, int32_t B, int32_t Hq, int32_t Hkv,
-                            int32_t d, float scale, void* o, float* lse, void* ws, size_t ws_bytes, void* stream) {
+                            const int32_t* offsets, const int32_t* indices, int64_t n_idx, int32_t B, int32_t Hq,
+                            int32_t Hkv, int32_t d, float scale, void* o, float* lse, void* ws, size_t ws_bytes,
+                            void* stream) {
     int rc = check_heads(B, Hq, Hkv, d);
     if (rc) return rc;
     if (!q || !o || !offsets || !indices) return fail(SDKV_ERR_INVALID_ARG, "null pointer");
@@ -298,6 +299,7 @@ int sdkv_sparse_decode_attn(const void* q, const void* k, const void* v, const i
     if (!v) return fail(SDKV_ERR_INVALID_ARG, "null V pointer");
     if ((rc = check_kv(k, v, kv_strides, d))) return rc;
     if (n_cap <= 0) return fail(SDKV_ERR_INVALID_ARG, "n_cap must be positive");
+    if (n_idx < 0) return fail(SDKV_ERR_INVALID_ARG, "n_idx must be >= 0");
     if (Hq / Hkv > 32) return fail(SDKV_ERR_UNSUPPORTED, "Hq/Hkv must be <= 32");
     if (static_cast<int64_t>(B) * Hkv > 65536) return fail(SDKV_ERR_UNSUPPORTED, "B*Hkv must be <= 65536");
     if (!std::isfinite(scale)) return fail(SDKV_ERR_INVALID_ARG, "scale must be finite");
@@ -321,6 +323,7 @@ int sdkv_sparse_decode_attn(const void* q, const void* k, const void* v, const i
     a.scale = scale;
     a.offsets = offsets;
     a.indices = indices;
+    a.n_idx = n_idx;
     a.n_cap = n_cap;
     a.ws = ws;
     a.ws_bytes = ws_bytes;
@@ -533,6 +536,7 @@ int sdkv_sparse_decode_compact(const void* q, const void* k_c, const void* v_c, 
     a.scale = scale;
     a.offsets = offsets;
     a.indices = nullptr;
+    a.n_idx = 0;   // no index array
     a.n_cap = static_cast<int>(rows_cap);
     a.ws = ws;
     a.ws_bytes = ws_bytes;

@@ -212,6 +212,14 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
 // CTA's earlier global writes ahead of a following relaxed atomic (release side),
 // and after an atomic it orders the later reads behind it (acquire side).
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+// Atomic add with acquire-release semantics at GPU scope: after a CTA barrier it
+// publishes the CTA's earlier global writes, and the CTA's later reads (after
+// another barrier) see what the other CTAs published before their own add.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* ptr, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+    return old;
+}
 // The mbarrier receives one arrival once every cp.async this thread issued so
 // far has landed (the arrival is counted in the barrier's expected count).
 __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
@@ -236,6 +244,12 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, 
                      reinterpret_cast<uint64_t>(map)),
                  "r"(c0), "r"(c1)
                  : "memory");
+}
+// Bring the cache line holding a global address into L2 (a load-unit prefetch:
+// no register result, no tensor-copy unit).  Same safety argument as the
+// tensor prefetches above.
+__device__ __forceinline__ void prefetch_l2_line(const void* src) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(src) : "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -281,7 +295,6 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
 }
-// 32 consecutive fp32 columns of this thread's lane (warp w may touch lanes 32*(w%4) .. +31).
 // 64 consecutive accumulator columns of this warp's 32 lanes, loaded and waited
 // for in one statement: the destination registers of tcgen05.ld are written
 // asynchronously, so the compiler must not see them (or reuse them) before the

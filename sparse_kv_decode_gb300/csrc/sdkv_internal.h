@@ -35,6 +35,7 @@ struct AttnLaunch {
     // sparse
     const int32_t* offsets;
     const int32_t* indices;
+    int64_t n_idx;   // entries of indices (0: no early reads of the lists)
     int n_cap;
     void* ws;
     size_t ws_bytes;

@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(L):
     assert len(names) == 16, names
     for name in names:
         assert hasattr(L, name), name
-    assert sk.version() == 101
+    assert sk.version() == 102
 
 
 def test_budgets_match_oracle_exactly(L):
@@ -86,7 +86,10 @@ def test_gpu_calls_reject_bad_arguments_without_launching(L):
     assert L.sdkv_dense_verify_attn(P, P, P, _strides(*st), 1, 4, 4, 96, 10, 1, 0.1, P, None, P, 1 << 20,
                                     None) == _lib.SDKV_ERR_UNSUPPORTED
     # Hq not a multiple of Hkv
-    assert L.sdkv_sparse_decode_attn(P, P, P, _strides(*st), 64, P, P, 1, 6, 4, 128, 0.1, P, None, P,
+    assert L.sdkv_sparse_decode_attn(P, P, P, _strides(*st), 64, P, P, 0, 1, 6, 4, 128, 0.1, P, None, P,
+                                     1 << 20, None) == _lib.SDKV_ERR_INVALID_ARG
+    # negative index-array length
+    assert L.sdkv_sparse_decode_attn(P, P, P, _strides(*st), 64, P, P, -1, 1, 8, 4, 128, 0.1, P, None, P,
                                      1 << 20, None) == _lib.SDKV_ERR_INVALID_ARG
     # null q
     assert L.sdkv_dense_verify_attn(None, P, P, _strides(*st), 1, 4, 4, 128, 10, 1, 0.1, P, None, P,
