@@ -1,17 +1,24 @@
 #!/usr/bin/env python
 """Benchmark of the sparse-KV decode hot path on one GB300 (or N replicas).
 
-One step = one pass of the whole path over one batch of synthetic input:
-  a1 head budgets (host)           -> per-head list lengths, copied to the device
+Headline (`value`): one decode step of the Llama-3.1-8B-shaped 32K workload,
+i.e. the gathered sparse decode (a4) of every layer over per-head lists that
+were fixed after selection, in one CUDA graph of the per-layer library calls.
+Before it, once per sequence (the prefill), the step's lists come from the
+library itself:
+  a1 head budgets (host)           -> per-head list lengths
   a2 window scoring, every layer   -> fp32 scores
   a3 top-K selection, every layer  -> per-head index lists
-  a4 sparse decode, every layer    -> o over the selected rows
-  a5 dense decode (split-K), every layer -> o over the full cache
-Each of a2..a5 is one CUDA graph of the per-layer library calls; CUDA events
-between the phases give each kernel's share of the step.
+Measured beside the headline, in the same run:
+  a5 dense decode (split-K) of every layer, the comparison of the pages;
+  a2 + a3 of every layer (`prefill_select`, once per sequence);
+  the 128K workload (keep 10/30/50%, dense, gamma=8 verify), the video workload
+  (StD draft decode, dense, gamma=5 verify; the StD I/O model and the measured
+  verify-over-dense ratio), and the SparseMM ragged-budget workload;
+  the rows around the hot path (compaction, window lists, SpecVLM, StD round).
 
 Prints ONE JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
-instead (the reference arm: a deliberately slow program, on a bounded sample).
+instead (the reference arm: a deliberately slow program) on whole decode steps.
 """
 import os
 
@@ -20,6 +27,7 @@ for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
 import argparse  # noqa: E402
+import ctypes  # noqa: E402
 import dataclasses  # noqa: E402
 import hashlib  # noqa: E402
 import json  # noqa: E402
@@ -44,7 +52,7 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
@@ -54,13 +62,13 @@ def parse():
     ap.add_argument("--keep-index", type=int, default=0, help="which keep ratio of the workload")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-configs", action="store_true", help="skip the 128K, video and SparseMM blocks")
+    ap.add_argument("--no-next", action="store_true", help="skip the timings of the next rows (f1..f4)")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (small profiling cases only; reported in config)")
-    ap.add_argument("--no-next", action="store_true", help="skip the timings of the next rows (f1..f4)")
     ap.add_argument("--clocks-log", default="",
                     help="file for the raw nvidia-smi samples of the timed region (default: a temporary file)")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def peaks():
@@ -71,6 +79,22 @@ def peaks():
         return float(pk["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def workload_config(w, keep_index=0):
+    """The `config` of both arms' JSON lines (identical strings in both)."""
+    if w.keep:
+        keep = "%d per head (%d sinks + %d recent + top-K)" % (w.keep[keep_index], w.n_sink, w.n_recent)
+    else:
+        keep = ("ragged SparseMM budgets, average %d per head (w=%d, rho=%.1f; %d recent + top-K)"
+                % (w.avg_budget, w.w_local, w.rho, w.n_recent))
+    return {
+        "workload": "%s: %d layers x (%d q / %d KV heads, d=%d), batch %d, context %d, keep %s; one decode step "
+                    "= the sparse decode of every layer over lists fixed after selection" % (
+                        w.name, w.layers, w.hq, w.hkv, w.d, w.batch, w.n, keep),
+        "l2": "inputs larger than L2: %d distinct layers of K/V (%.2f GB)" % (
+            w.layers, w.layers * 2 * w.batch * w.hkv * w.n * w.d * 2 / 1e9),
+    }
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -163,141 +187,163 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(win)}
 
 
-# ----------------------------------------------------------------------------- the path
-class Path:
-    """Device buffers and CUDA graphs of one step of the whole hot path."""
+# ----------------------------------------------------------------------------- device state
+class Decode:
+    """Device state of one workload after its prefill: K/V caches and queries
+    of `distinct` layers (cycled when fewer than the workload's layers), the
+    per-head lists of each keep ratio from the library's own a1..a3, and the
+    per-layer library calls of each phase."""
 
-    PHASES = ("score", "select", "sparse", "dense")
-
-    def __init__(self, w, keep_index, dev):
+    def __init__(self, w, dev, distinct=0, verify=False):
         import sparse_kv_decode_gb300 as sk
-        self.sk = sk
-        self.w = w
-        self.dev = dev
+        self.sk, self.w, self.dev = sk, w, dev
         L, B, Hq, Hkv, d, n = w.layers, w.batch, w.hq, w.hkv, w.d, w.n
         self.L, self.B, self.Hq, self.Hkv, self.d, self.n = L, B, Hq, Hkv, d, n
         self.BH = B * Hkv
         self.scale = 1.0 / math.sqrt(d)
-        self.layers = [workloads.make_layer(w, l, device=dev) for l in range(L)]
-        # a1 inputs: head scores over the L x Hkv heads of one sequence
+        nd = min(L, distinct) if distinct else L
+        self.lays = [workloads.make_layer(w, l, device=dev) for l in range(nd)]
+        self.q_de = [lay["q"][:, :, None, :].contiguous() for lay in self.lays]
         self.s_heads = workloads.head_scores(w).numpy()
-        if w.keep:
-            k_h = w.keep[keep_index]
-            self.budget_args = (L * Hkv * k_h, w.n_recent, 0.1, n)
-        else:
-            self.budget_args = (w.avg_budget * L * Hkv, w.w_local, w.rho, n)
-        # two pinned staging buffers for the a1 output, so the host never writes
-        # one that a copy still reads
-        self.offs_pinned = [torch.zeros((L, self.BH + 1), dtype=torch.int32).pin_memory() for _ in range(2)]
-        self.offs_done = [None, None]
-        self.flip = 0
-        self.offs_host = self.offs_pinned[0]
-        self.offs_dev = torch.zeros((L, self.BH + 1), dtype=torch.int32, device=dev)
-        self.budgets()
-        self.totals = [int(x) for x in self.offs_host[:, -1]]
-        self.offs_dev.copy_(self.offs_host)
         self.scores = torch.empty((L, B, Hkv, n), dtype=torch.float32, device=dev)
-        self.idx = torch.empty((L, max(max(self.totals), 1)), dtype=torch.int32, device=dev)
         self.o_sp = torch.empty((L, B, Hq, d), dtype=torch.bfloat16, device=dev)
         self.l_sp = torch.empty((L, B, Hq), dtype=torch.float32, device=dev)
         self.o_de = torch.empty((L, B, Hq, 1, d), dtype=torch.bfloat16, device=dev)
         self.l_de = torch.empty((L, B, Hq, 1), dtype=torch.float32, device=dev)
-        self.q_de = [lay["q"][:, :, None, :].contiguous() for lay in self.layers]
         self.ws_score = sk.new_workspace(sk.workspace_size(sk.OP_SCORE, B, Hq, Hkv, d, n, w.window), dev)
         self.ws_sel = sk.new_workspace(sk.workspace_size(sk.OP_SELECT, B, 0, Hkv, 0, n, 0), dev)
         self.ws_sp = sk.new_workspace(sk.workspace_size(sk.OP_SPARSE_DECODE, B, Hq, Hkv, d, 0, 0), dev)
         self.ws_de = sk.new_workspace(sk.workspace_size(sk.OP_DENSE_VERIFY, B, Hq, Hkv, d, n, 1), dev)
-        self.graphs = {}
+        self.verify = verify
+        if verify:
+            self.o_v = torch.empty((L, B, Hq, w.gamma, d), dtype=torch.bfloat16, device=dev)
+            self.ws_v = sk.new_workspace(sk.workspace_size(sk.OP_DENSE_VERIFY, B, Hq, Hkv, d, n, w.gamma), dev)
+        self.lists = {}          # keep index -> (offsets [L][BH+1] int32 device, indices [L][max] int32, totals)
 
-    def budgets(self):
-        """a1 on the host: budgets of all L x Hkv heads; every sequence of the
-        batch gets lists of the same lengths."""
-        total_B, w_loc, rho, cap = self.budget_args
-        b = self.sk.head_budgets(self.s_heads, total_B, w_loc, rho, cap).reshape(self.L, self.Hkv)
-        per = np.tile(b, (1, self.B))                      # [L][B*Hkv], sequence-major
-        offs = self.offs_host.numpy()
-        offs[:, 0] = 0
-        np.cumsum(per, axis=1, out=offs[:, 1:])
-        return b
+    def lay(self, l):
+        return self.lays[l % len(self.lays)]
 
-    def phase_score(self):
+    def workspaces(self):
+        out = [self.ws_score, self.ws_sel, self.ws_sp, self.ws_de]
+        return out + ([self.ws_v] if self.verify else [])
+
+    # a1 on the host: budgets of all L x Hkv heads; every sequence of the batch gets lists of the same lengths
+    def budgets(self, ki):
         w = self.w
-        for l, lay in enumerate(self.layers):
-            self.sk.score_obs_window(lay["q_obs"], lay["k"], self.n, w.q_pos0, self.scale,
-                                     scores=self.scores[l], ws=self.ws_score)
+        if w.keep:
+            args = (self.L * self.Hkv * w.keep[ki], w.n_recent, 0.1, self.n)
+        else:
+            args = (w.avg_budget * self.L * self.Hkv, w.w_local, w.rho, self.n)
+        b = self.sk.head_budgets(self.s_heads, *args).reshape(self.L, self.Hkv)
+        per = np.tile(b, (1, self.B))                      # [L][B*Hkv], sequence-major
+        offs = np.zeros((self.L, self.BH + 1), dtype=np.int32)
+        np.cumsum(per, axis=1, out=offs[:, 1:])
+        return offs
 
-    def phase_select(self):
+    def score_all(self):
         w = self.w
         for l in range(self.L):
-            self.sk.select_topk(self.scores[l], self.n, w.cand_lo, w.cand_hi, w.n_sink, w.n_recent,
-                                self.offs_dev[l], self.totals[l], indices=self.idx[l], ws=self.ws_sel)
+            lay = self.lay(l)
+            self.sk.score_obs_window(lay["q_obs"], lay["k"], self.n, w.q_pos0, self.scale, scores=self.scores[l],
+                                     ws=self.ws_score)
 
-    def phase_sparse(self):
-        for l, lay in enumerate(self.layers):
-            self.sk.sparse_decode_attn(lay["q"], lay["k"], lay["v"], self.offs_dev[l], self.idx[l], self.scale,
-                                       o=self.o_sp[l], lse=self.l_sp[l], ws=self.ws_sp)
+    def select_all(self, ki):
+        w = self.w
+        offs, idx, totals = self.lists[ki]
+        for l in range(self.L):
+            self.sk.select_topk(self.scores[l], self.n, w.cand_lo, w.cand_hi, w.n_sink, w.n_recent, offs[l],
+                                totals[l], indices=idx[l], ws=self.ws_sel)
 
-    def phase_dense(self):
-        for l, lay in enumerate(self.layers):
-            self.sk.dense_verify_attn(self.q_de[l], lay["k"], lay["v"], self.n - 1, self.scale,
+    def prefill(self, keep_indices=(0,)):
+        """a1 (host) for every keep ratio, a2 once, a3 per keep ratio."""
+        for ki in keep_indices:
+            offs = self.budgets(ki)
+            totals = [int(x) for x in offs[:, -1]]
+            idx = torch.empty((self.L, max(max(totals), 1)), dtype=torch.int32, device=self.dev)
+            self.lists[ki] = (torch.from_numpy(offs).to(self.dev), idx, totals)
+        self.score_all()
+        for ki in keep_indices:
+            self.select_all(ki)
+        torch.cuda.synchronize()
+
+    def sparse_step(self, ki):
+        offs, idx, _ = self.lists[ki]
+        for l in range(self.L):
+            lay = self.lay(l)
+            self.sk.sparse_decode_attn(lay["q"], lay["k"], lay["v"], offs[l], idx[l], self.scale, o=self.o_sp[l],
+                                       lse=self.l_sp[l], ws=self.ws_sp)
+
+    def dense_step(self):
+        for l in range(self.L):
+            lay = self.lay(l)
+            self.sk.dense_verify_attn(self.q_de[l % len(self.lays)], lay["k"], lay["v"], self.n - 1, self.scale,
                                       o=self.o_de[l], lse=self.l_de[l], ws=self.ws_de)
 
-    def capture(self):
-        # eager pass first (sets kernel attributes, checks everything runs)
-        for ph in self.PHASES:
-            getattr(self, "phase_" + ph)()
+    def verify_step(self):
+        g = self.w.gamma
+        for l in range(self.L):
+            lay = self.lay(l)
+            self.sk.dense_verify_attn(lay["q_ver"], lay["k"], lay["v"], self.n - g, self.scale, o=self.o_v[l],
+                                      ws=self.ws_v, want_lse=False)
+
+    def prefill_step(self, ki):
+        self.score_all()
+        self.select_all(ki)
+
+    def mean_total(self, ki):
+        return float(np.mean(self.lists[ki][2]))
+
+    def alg_bytes(self, phase, ki=0):
+        """Algorithmic bytes of one layer's launch of a phase."""
+        w, B, Hq, Hkv, d, n = self.w, self.B, self.Hq, self.Hkv, self.d, self.n
+        if phase == "sparse":
+            return ba.sparse_decode_bytes(B, Hq, d, int(self.mean_total(ki)))
+        if phase == "dense":
+            return ba.dense_verify_bytes(B, Hq, Hkv, d, n - 1, 1)
+        if phase == "verify":
+            return ba.dense_verify_bytes(B, Hq, Hkv, d, n - w.gamma, w.gamma)
+        if phase == "score":
+            return ba.score_bytes(B, Hq, Hkv, d, n, w.window)
+        if phase == "select":
+            return ba.select_bytes(B, Hkv, n, int(self.mean_total(ki)))
+        raise KeyError(phase)
+
+
+def capture(fn):
+    """One eager run of `fn` (sets kernel attributes, checks it runs), then a
+    CUDA graph of its launches."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(g, reps, flush=None):
+    """Median device time (µs) of one replay of `g` over `reps` replays after 3
+    untimed ones; with `flush`, an L2-sized write before every replay."""
+    ts = []
+    for r in range(reps + 3):
+        if flush is not None:
+            flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
         torch.cuda.synchronize()
-        for ph in self.PHASES:
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                getattr(self, "phase_" + ph)()
-            self.graphs[ph] = g
-        torch.cuda.synchronize()
+        if r >= 3:
+            ts.append(a.elapsed_time(b) * 1e3)
+    return float(np.median(ts))
 
-    def step_budgets(self):
-        """a1 on the host and the copy of its lists' offsets to the device."""
-        self.flip ^= 1
-        if self.offs_done[self.flip] is not None:
-            self.offs_done[self.flip].synchronize()
-        self.offs_host = self.offs_pinned[self.flip]
-        self.budgets()
-        self.offs_dev.copy_(self.offs_host, non_blocking=True)
-        ev = torch.cuda.Event()
-        ev.record()
-        self.offs_done[self.flip] = ev
 
-    def layer_ops(self, l):
-        """a2..a5 of layer l through the public API (eager, current stream)."""
-        w, lay = self.w, self.layers[l]
-        self.sk.score_obs_window(lay["q_obs"], lay["k"], self.n, w.q_pos0, self.scale, scores=self.scores[l],
-                                 ws=self.ws_score)
-        self.sk.select_topk(self.scores[l], self.n, w.cand_lo, w.cand_hi, w.n_sink, w.n_recent, self.offs_dev[l],
-                            self.totals[l], indices=self.idx[l], ws=self.ws_sel)
-        self.sk.sparse_decode_attn(lay["q"], lay["k"], lay["v"], self.offs_dev[l], self.idx[l], self.scale,
-                                   o=self.o_sp[l], lse=self.l_sp[l], ws=self.ws_sp)
-        self.sk.dense_verify_attn(self.q_de[l], lay["k"], lay["v"], self.n - 1, self.scale, o=self.o_de[l],
-                                  lse=self.l_de[l], ws=self.ws_de)
-
-    def step(self, evs=None):
-        self.step_budgets()
-        for i, ph in enumerate(self.PHASES):
-            if evs is not None:
-                evs[i].record()
-            self.graphs[ph].replay()
-        if evs is not None:
-            evs[len(self.PHASES)].record()
-
-    def launches_per_step(self):
-        return self.L * (2 + 1 + 1 + 1)   # score = 2 kernels, select, sparse, dense
-
-    def alg_bytes_per_layer(self):
-        mean_total = float(np.mean(self.totals))
-        return {
-            "score": ba.score_bytes(self.B, self.Hq, self.Hkv, self.d, self.n, self.w.window),
-            "select": ba.select_bytes(self.B, self.Hkv, self.n, int(mean_total)),
-            "sparse": ba.sparse_decode_bytes(self.B, self.Hq, self.d, int(mean_total)),
-            "dense": ba.dense_verify_bytes(self.B, self.Hq, self.Hkv, self.d, self.n - 1, 1),
-        }
+def phase_record(us_step, layers, alg_bytes_per_layer, hbm_peak):
+    per_layer = us_step / layers
+    gbs = alg_bytes_per_layer / (per_layer * 1e-6) / 1e9
+    return {"us_per_step": us_step, "us_per_layer": per_layer, "alg_bytes_per_layer": alg_bytes_per_layer,
+            "gbs": gbs, "frac_of_measured_hbm": gbs / hbm_peak, "frac_of_8tbs_nominal": gbs / NOMINAL_HBM_GBS}
 
 
 def kernel_source_hash():
@@ -330,39 +376,6 @@ def traffic_from_profiles(phase, workload):
 
 
 # ----------------------------------------------------------------------------- CPU oracle timing
-def _oracle_unit(w, kk, vv, qo, qq):
-    """The whole path of one KV head through the oracle: its window scores, its
-    top-K list, and the sparse and dense decode of its G query heads."""
-    import oracle
-    kh = w.keep[0] if w.keep else w.avg_budget
-    sc = oracle.score_obs_window(qo, kk, w.n, w.q_pos0)
-    offs = np.array([0, kh])
-    idx = oracle.select_topk(sc, w.n, w.cand_lo, w.cand_hi, w.n_sink, w.n_recent, offs)
-    oracle.sparse_decode(qq, kk, vv, offs, idx)
-    oracle.dense_verify(qq[:, :, None, :], kk, vv, w.n - 1)
-
-
-def _unit_inputs(w, lay, b, h):
-    G = w.hq // w.hkv
-    return (lay["k"][b:b + 1, h:h + 1].cpu(), lay["v"][b:b + 1, h:h + 1].cpu(),
-            lay["q_obs"][b:b + 1, h * G:(h + 1) * G].cpu(), lay["q"][b:b + 1, h * G:(h + 1) * G].cpu())
-
-
-def oracle_units(w, layer_fn, n_units, rng_seed=0):
-    """Seconds per unit of the oracle in this process on `n_units` sampled
-    (layer, sequence, KV head) units."""
-    rng = np.random.default_rng(rng_seed)
-    units = [(int(rng.integers(w.layers)), int(rng.integers(w.batch)), int(rng.integers(w.hkv)))
-             for _ in range(n_units)]
-    total = 0.0
-    for (l, b, h) in units:
-        args = _unit_inputs(w, layer_fn(l), b, h)
-        t0 = time.perf_counter()
-        _oracle_unit(w, *args)
-        total += time.perf_counter() - t0
-    return total / n_units
-
-
 def host_cores():
     try:
         return max(1, len(os.sched_getaffinity(0)))
@@ -370,20 +383,54 @@ def host_cores():
         return max(1, os.cpu_count() or 1)
 
 
-def _oracle_worker(name, layer, units, rounds, start_bar, out_q):
-    """One host core (one process, one BLAS thread): its units of one layer,
-    timed `rounds` times; every round starts at a barrier of all workers."""
+def step_units(w):
+    """The (layer, sequence, KV head) units of one decode step."""
+    return [(l, b, h) for l in range(w.layers) for b in range(w.batch) for h in range(w.hkv)]
+
+
+def _unit_lists_budgets(w, keep_index):
+    """Per-(layer, KV head) list lengths: the oracle's own head budgets (a1)."""
+    import oracle
+    s = workloads.head_scores(w).numpy()
+    if w.keep:
+        b = oracle.head_budgets(s, w.layers * w.hkv * w.keep[keep_index], w.n_recent, 0.1, w.n)
+    else:
+        b = oracle.head_budgets(s, w.avg_budget * w.layers * w.hkv, w.w_local, w.rho, w.n)
+    return np.asarray(b).reshape(w.layers, w.hkv)
+
+
+def _decode_worker(name, keep_index, units, rounds, start_bar, out_q):
+    """One host core (one process, one BLAS thread).  Set-up, untimed: its
+    units' inputs and their lists from the oracle's own budgets, window scores
+    and top-K selection (once per sequence, as on the GPU).  Then `rounds`
+    timed rounds, each the oracle's sparse decode of every unit; every round
+    starts at a barrier of all workers."""
     try:
+        import oracle
         w = workloads.by_name(name)
-        lay = workloads.make_layer(w, layer, device="cpu")
-        data = [_unit_inputs(w, lay, b, h) for (b, h) in units]
-        del lay
+        budgets = _unit_lists_budgets(w, keep_index)
+        G = w.group
+        data, cache = [], {}
+        for (l, b, h) in units:
+            if l not in cache:
+                cache.clear()
+                cache[l] = workloads.make_layer(w, l, device="cpu")
+            lay = cache[l]
+            kk = lay["k"][b:b + 1, h:h + 1].clone()
+            vv = lay["v"][b:b + 1, h:h + 1].clone()
+            qo = lay["q_obs"][b:b + 1, h * G:(h + 1) * G]
+            qq = lay["q"][b:b + 1, h * G:(h + 1) * G].clone()
+            sc = oracle.score_obs_window(qo, kk, w.n, w.q_pos0)
+            offs = np.array([0, int(budgets[l, h])])
+            idx = oracle.select_topk(sc, w.n, w.cand_lo, w.cand_hi, w.n_sink, w.n_recent, offs)
+            data.append((qq, kk, vv, offs, idx))
+        cache.clear()
         res = []
         for _ in range(rounds):
-            start_bar.wait(timeout=300)
+            start_bar.wait(timeout=900)
             t0 = time.time()
-            for args in data:
-                _oracle_unit(w, *args)
+            for (qq, kk, vv, offs, idx) in data:
+                oracle.sparse_decode(qq, kk, vv, offs, idx)
             res.append((t0, time.time(), len(data)))
         out_q.put((res, None))
     except Exception as e:
@@ -391,21 +438,21 @@ def _oracle_worker(name, layer, units, rounds, start_bar, out_q):
         out_q.put((None, repr(e)))
 
 
-def oracle_parallel(w, cores, per_worker, rounds, timeout=900.0):
-    """Seconds per unit, per round, of the oracle run by `cores` worker
-    processes at once (started with spawn), each on `per_worker` sampled
-    (sequence, KV head) units of its own layer: the wall time of the round over
-    the units all workers processed."""
+def oracle_decode_rounds(w, keep_index, units, cores, rounds, timeout=1800.0):
+    """Wall seconds of each round of the oracle's sparse decode of `units`, run
+    by `cores` worker processes at once (started with spawn; worker i takes a
+    contiguous block of the units, so it draws few layers)."""
     import multiprocessing as mp
     import queue
     ctx = mp.get_context("spawn")
+    cores = max(1, min(cores, len(units)))
     start_bar = ctx.Barrier(cores)
     out_q = ctx.Queue()
-    rng = np.random.default_rng(7)
+    per = (len(units) + cores - 1) // cores
     procs = []
     for i in range(cores):
-        units = [(int(rng.integers(w.batch)), int(rng.integers(w.hkv))) for _ in range(per_worker)]
-        p = ctx.Process(target=_oracle_worker, args=(w.name, (7 * i) % w.layers, units, rounds, start_bar, out_q),
+        p = ctx.Process(target=_decode_worker,
+                        args=(w.name, keep_index, units[i * per:(i + 1) * per], rounds, start_bar, out_q),
                         daemon=True)
         p.start()
         procs.append(p)
@@ -426,195 +473,296 @@ def oracle_parallel(w, cores, per_worker, rounds, timeout=900.0):
             p.join(timeout=30)
             if p.is_alive():
                 p.terminate()
-    per_round = []
+    out = []
     for r in range(rounds):
         t0 = min(res[r][0] for res in results)
         t1 = max(res[r][1] for res in results)
-        per_round.append((t1 - t0) / sum(res[r][2] for res in results))
-    return per_round
+        out.append(t1 - t0)
+    return out, cores
 
 
-def cpu_baseline(w, layer_fn, seconds):
-    """The oracle on all host cores: one worker process per core, each timing
-    a bounded sample of whole-path units; scaled to one step of the workload.
-    Falls back to one core (and says so) if worker processes cannot run."""
-    per_unit = oracle_units(w, layer_fn, 1)
-    per_worker = max(1, min(8, int(seconds / max(per_unit, 1e-3))))
-    units_per_step = w.layers * w.batch * w.hkv
-    what = ("whole path for one KV head (scores, top-K list, sparse and dense decode of its %d query heads), "
-            "fp64 numpy" % (w.hq // w.hkv))
-    cores = host_cores()
+def oracle_step_plan(w, max_units):
+    """Units timed per step: the whole step when it has at most `max_units`
+    units, else an evenly spaced sample (the value is then scaled to the step
+    and the line says so)."""
+    units = step_units(w)
+    if len(units) <= max_units:
+        return units, False
+    stride = len(units) / max_units
+    return [units[int(i * stride)] for i in range(max_units)], True
+
+
+def oracle_decode_inline(w, keep_index, units, rounds):
+    """The same rounds in this process (one core), for when worker processes
+    cannot start."""
+    import queue
+
+    class _Bar:
+        def wait(self, timeout=None):
+            pass
+
+        def abort(self):
+            pass
+    q = queue.Queue()
+    _decode_worker(w.name, keep_index, units, rounds, _Bar(), q)
+    res, err = q.get()
+    if err is not None:
+        raise RuntimeError("oracle: " + err)
+    return [t1 - t0 for (t0, t1, _) in res]
+
+
+def cpu_baseline(w, keep_index, timed_rounds=2, max_units=512):
+    """The oracle's decode step on all host cores (one worker process per core),
+    whole steps timed (1 untimed round, then `timed_rounds`).  Falls back to
+    this process alone (and says so) if worker processes cannot run."""
+    units, sampled = oracle_step_plan(w, max_units)
+    total = len(step_units(w))
+    where = ""
     try:
-        per_unit = oracle_parallel(w, cores, per_worker, 1)[0]
-        sample = ("%d (sequence, KV head) units of the %s workload on each of %d worker processes (one per host "
-                  "core, one BLAS thread each, one layer each), timed together; a unit is the %s; wall time "
-                  "over units, scaled by %d units per step" % (per_worker, w.name, cores, what, units_per_step))
-    except Exception as e:   # no worker processes: this process alone
-        cores = 1
-        per_worker = max(1, min(64, int(seconds / max(per_unit, 1e-3))))
-        per_unit = oracle_units(w, layer_fn, per_worker, rng_seed=1)
-        sample = ("%d (layer, sequence, KV head) units of the %s workload in one process (worker processes "
-                  "failed: %s); a unit is the %s; scaled by %d units per step"
-                  % (per_worker, w.name, e, what, units_per_step))
-    return {"value": per_unit * units_per_step * 1e6, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": sample}
+        rounds, used = oracle_decode_rounds(w, keep_index, units, host_cores(), 1 + timed_rounds)
+        where = "%d worker processes (one per host core, one BLAS thread each)" % used
+    except Exception as e:
+        units, sampled = oracle_step_plan(w, 16)
+        rounds, used = oracle_decode_inline(w, keep_index, units, 1 + timed_rounds), 1
+        where = "this process alone (worker processes failed: %s)" % e
+    per_step = float(np.mean(rounds[1:])) * (total / len(units))
+    sample = ("the oracle's sparse decode (fp64 numpy) of %s%d (layer, sequence, KV head) units of the %s workload, "
+              "on %s, lists from the oracle's own budgets, window scores and top-K selection; mean of %d timed "
+              "rounds after 1 untimed"
+              % ("" if not sampled else "a sample of ", len(units), w.name, where, timed_rounds)
+              + ("" if not sampled else "; scaled by %d / %d units per step" % (total, len(units))))
+    return {"value": per_step * 1e6, "unit": UNIT, "cores": used, "kind": "oracle", "sample": sample,
+            "units_timed_per_step": len(units), "units_per_step": total, "extrapolated": sampled}
 
 
 # ----------------------------------------------------------------------------- arms
 def run_reference(args, world, rank):
+    """The reference arm: the fp64 oracle's decode step on the host cores."""
     if rank != 0:
         return
     w = workloads.by_name(args.workload)
+    if args.layers:
+        w = dataclasses.replace(w, layers=args.layers)
     warm = max(args.warmup, 3)
-    units_per_step = w.layers * w.batch * w.hkv
-    cores = host_cores()
-    try:
-        # every step: one whole-path unit on each host core, all cores at once
-        per_round = oracle_parallel(w, cores, 1, warm + args.steps)
-        note = ("fp64 CPU oracle on %d worker processes (one per host core, one BLAS thread each); each step "
-                "times one sampled (sequence, KV head) unit of the whole path per worker, all at once, and "
-                "scales the wall time per unit to the full step" % cores)
-    except Exception as e:
-        cores = 1
-        cache = {}
-
-        def layer_fn(l):
-            if l not in cache:
-                cache.clear()
-                cache[l] = workloads.make_layer(w, l, device="cpu")
-            return cache[l]
-
-        per_round = [oracle_units(w, layer_fn, 2, rng_seed=100 + i) for i in range(warm + args.steps)]
-        note = ("fp64 CPU oracle in one process (worker processes failed: %s); each step times 2 sampled "
-                "(layer, sequence, KV head) units of the whole path and scales to the full step" % e)
-    us = float(np.mean(per_round[warm:])) * units_per_step * 1e6
+    units, sampled = oracle_step_plan(w, 512)
+    total = len(step_units(w))
+    t_start = time.time()
+    rounds, cores = oracle_decode_rounds(w, args.keep_index, units, host_cores(), warm + args.steps)
+    scale = total / len(units)
+    us = float(np.mean(rounds[warm:])) * scale * 1e6
+    sample = ("the oracle's sparse decode (fp64 numpy) of %s%d (layer, sequence, KV head) units per step on %d "
+              "worker processes (one per host core, one BLAS thread each), lists from the oracle's own budgets, "
+              "window scores and top-K selection (set-up, untimed)"
+              % ("a sample of " if sampled else "all ", len(units), cores)
+              + ("; scaled by %d / %d units per step" % (total, len(units)) if sampled else ""))
     line = {
         "impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": warm, "ms_per_step": us / 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "note": note},
-        "cpu_baseline": {"value": us, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": "%d unit(s) per step on %d core(s), scaled by %d units per step"
-                                   % (cores, cores, units_per_step)},
+        "config": workload_config(w, args.keep_index),
+        "units_timed_per_step": len(units), "units_per_step": total, "extrapolated": sampled,
+        "timed_wall_s": float(np.sum(rounds[warm:])), "run_wall_s": time.time() - t_start,
+        "cpu_baseline": {"value": us, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
 
 
-def run_e2e(path, K, world):
-    """The same step through the public API with the inputs in pinned host
-    memory: every step copies all layers' K, V, window queries and decode
-    queries to the device and reads the decode outputs back.  Layer l's inputs
-    go over on a copy stream while layer l - 1 computes (the host link, about
-    0.2 TB/s here, is the bound; the compute hides behind it)."""
-    host = []
-    h2d = 0
-    for lay in path.layers:
-        hl = {}
-        for name in ("k", "v", "q_obs", "q"):
-            t = torch.empty(lay[name].shape, dtype=lay[name].dtype, pin_memory=True)
-            t.copy_(lay[name])
-            hl[name] = t
-            h2d += t.numel() * t.element_size()
-        host.append(hl)
-    outs = [path.o_sp, path.l_sp, path.o_de, path.l_de]
-    out_host = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
-    d2h = sum(o.numel() * o.element_size() for o in outs)
-
-    comp = torch.cuda.current_stream()
-    copy_st = torch.cuda.Stream()
-    arrived = [torch.cuda.Event() for _ in path.layers]
-    done = torch.cuda.Event()
-    done.record(comp)
+def run_e2e(D, ki, K, world):
+    """The decode step end to end through the C ABI (sdkv_sparse_decode_attn once
+    per layer, arguments marshalled once): every step copies all layers' decode
+    queries from pinned host memory to the device and reads o and lse back.
+    The caches and lists are device state from the prefill, not step inputs."""
+    sk = D.sk
+    L = sk.lib()
+    offs, idx, _ = D.lists[ki]
+    q_dev = torch.stack([D.lay(l)["q"] for l in range(D.L)]).contiguous()
+    q_host = torch.empty(q_dev.shape, dtype=q_dev.dtype, pin_memory=True)
+    q_host.copy_(q_dev)
+    o_host = torch.empty(D.o_sp.shape, dtype=D.o_sp.dtype, pin_memory=True)
+    l_host = torch.empty(D.l_sp.shape, dtype=D.l_sp.dtype, pin_memory=True)
+    st = torch.cuda.current_stream().cuda_stream
+    keep_alive, calls = [], []
+    for l in range(D.L):
+        lay = D.lay(l)
+        strides = (ctypes.c_int64 * 3)(*lay["k"].stride()[:3])
+        keep_alive.append(strides)
+        calls.append((q_dev[l].data_ptr(), lay["k"].data_ptr(), lay["v"].data_ptr(), strides, lay["k"].shape[2],
+                      offs[l].data_ptr(), idx[l].data_ptr(), idx[l].numel(), D.B, D.Hq, D.Hkv, D.d,
+                      ctypes.c_float(D.scale), D.o_sp[l].data_ptr(), D.l_sp[l].data_ptr(), D.ws_sp.data_ptr(),
+                      D.ws_sp.numel(), st))
 
     def step():
-        path.step_budgets()
-        copy_st.wait_event(done)          # the previous step no longer reads the inputs
-        for l, (lay, hl) in enumerate(zip(path.layers, host)):
-            with torch.cuda.stream(copy_st):
-                for name in ("k", "v", "q_obs", "q"):
-                    lay[name].copy_(hl[name], non_blocking=True)
-                arrived[l].record(copy_st)
-            comp.wait_event(arrived[l])
-            path.q_de[l].copy_(lay["q"][:, :, None, :], non_blocking=True)
-            path.layer_ops(l)
-        for o, oh in zip(outs, out_host):
-            oh.copy_(o, non_blocking=True)
-        done.record(comp)
+        q_dev.copy_(q_host, non_blocking=True)
+        for c in calls:
+            rc = L.sdkv_sparse_decode_attn(*c)
+            if rc != 0:
+                raise RuntimeError("sdkv_sparse_decode_attn: %s" % L.sdkv_last_error().decode())
+        o_host.copy_(D.o_sp, non_blocking=True)
+        l_host.copy_(D.l_sp, non_blocking=True)
 
     step()
     torch.cuda.synchronize()
     s = torch.cuda.Event(enable_timing=True)
     e = torch.cuda.Event(enable_timing=True)
     barrier(world)
+    torch.cuda.synchronize()
     s.record()
     for _ in range(K):
         step()
     e.record()
     torch.cuda.synchronize()
     ms = max_over_ranks(s.elapsed_time(e), world)
-    return {"value": ms / K * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": K}
+    return {"value": ms / K * 1e3, "unit": UNIT, "h2d_bytes_per_step": q_host.numel() * q_host.element_size(),
+            "d2h_bytes_per_step": o_host.numel() * o_host.element_size() + l_host.numel() * l_host.element_size(),
+            "steps": K, "path": "C ABI: sdkv_sparse_decode_attn per layer; decode queries copied from pinned "
+                                "host memory and o, lse read back every step"}
 
 
-def time_graph_us(fn, reps: int = 10, flush: torch.Tensor | None = None) -> float:
-    """Median device time (µs) of one CUDA-graph replay of `fn`'s launches,
-    with an L2 flush (a write larger than L2) before every replay."""
-    fn()
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        fn()
-    ts = []
-    for r in range(reps + 3):
-        if flush is not None:
-            flush.zero_()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record()
-        g.replay()
-        b.record()
-        torch.cuda.synchronize()
-        if r >= 3:
-            ts.append(a.elapsed_time(b) * 1e3)
-    return float(np.median(ts))
+def sparse_dense_block(D, kis, hbm_peak, reps, with_verify=False, with_select=False, flush=None):
+    """Per-layer times of the sparse decode at each keep ratio, the dense decode
+    and (optionally) the gamma verify and the prefill selection of workload D.
+    `flush`: an L2-sized write before every replay (for steps whose inputs fit
+    in L2)."""
+    out = {}
+    for ki in kis:
+        g = capture(lambda: D.sparse_step(ki))
+        us = time_graph(g, reps, flush)
+        tag = ("keep_%dpct" % round(100 * D.w.keep[ki] / D.n)) if D.w.keep else "ragged"
+        out[tag] = phase_record(us, D.L, D.alg_bytes("sparse", ki), hbm_peak)
+        out[tag]["kept_per_head_mean"] = D.mean_total(ki) / D.BH
+        del g
+    g = capture(D.dense_step)
+    out["dense"] = phase_record(time_graph(g, reps, flush), D.L, D.alg_bytes("dense"), hbm_peak)
+    del g
+    if with_verify:
+        g = capture(D.verify_step)
+        out["verify_gamma%d" % D.w.gamma] = phase_record(time_graph(g, reps, flush), D.L, D.alg_bytes("verify"),
+                                                         hbm_peak)
+        del g
+    if with_select:
+        g = capture(lambda: D.prefill_step(kis[0]))
+        us = time_graph(g, reps, flush)
+        out["prefill_select"] = {"us_per_sequence": us, "us_per_layer": us / D.L}
+        del g
+    for ws in D.workspaces():
+        st = D.sk.workspace_status(ws)
+        if st != 0:
+            raise SystemExit("device status %d raised during the bench" % st)
+    return out
 
 
-def next_rows_timings(path, hbm_peak, dev):
-    """Timings of the rows beyond the hot path (each a separate measurement,
-    outside the step):
+def config_blocks(hbm_peak, dev, reps):
+    """The other single-GPU workloads, each a separate measurement."""
+    out = {}
+    # Llama-3.1-8B shape at 128K: keep 10 / 30 / 50%, dense, gamma = 8 verify
+    w = workloads.by_name("llama8b_128k")
+    D = Decode(w, dev, verify=True)
+    D.prefill((0, 1, 2))
+    blk = sparse_dense_block(D, (0, 1, 2), hbm_peak, reps, with_verify=True, with_select=True)
+    blk["sparse_vs_dense"] = {k: blk["dense"]["us_per_layer"] / v["us_per_layer"] for k, v in blk.items()
+                              if k.startswith("keep_")}
+    blk["byte_bound"] = {k: blk["dense"]["alg_bytes_per_layer"] / v["alg_bytes_per_layer"] for k, v in blk.items()
+                         if k.startswith("keep_")}
+    out["llama8b_128k"] = blk
+    del D
+    torch.cuda.empty_cache()
+    # SparseMM: ragged head budgets, batch 8, 32 MHA heads; 8 distinct layers (4.3 GB of K/V each) cycled
+    w = workloads.by_name("sparsemm")
+    D = Decode(w, dev, distinct=8)
+    D.prefill((0,))
+    blk = sparse_dense_block(D, (0,), hbm_peak, max(3, reps // 4))
+    blk["note"] = "8 distinct layers cycled over the 32 launches of a step; each layer's K/V (4.3 GB) exceeds L2"
+    out["sparsemm"] = blk
+    del D
+    torch.cuda.empty_cache()
+    # video (Qwen2-7B shape): the StD draft decode over 256 text + 768 visual, dense decode, gamma = 5 verify
+    w = workloads.by_name("video")
+    D = Decode(w, dev, verify=True)
+    D.prefill((0,))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # the step's 59 MB of kept rows fit in L2
+    blk = sparse_dense_block(D, (0,), hbm_peak, reps, with_verify=True, with_select=True, flush=flush)
+    blk["note"] = "L2 flushed (256 MB write) before every replay"
+    out["video"] = blk
+    del flush
+    del D
+    torch.cuda.empty_cache()
+    return out
+
+
+def io_model(video, llama128):
+    """The StD I/O model (3.3) for the video workload, and the measured
+    counterparts: verify over dense decode (SpecVLM's T_t^gamma / T_t) and
+    draft over dense decode (T_d / T_t), attention kernels only."""
+    w = workloads.by_name("video")
+    gamma, m_t, m_v = w.gamma, w.text_tokens, w.frames * w.frame_tokens
+    K = w.keep[0] - m_t
+    t_draft = next(v["us_per_layer"] for k, v in video.items() if k.startswith("keep_"))
+    t_dense = video["dense"]["us_per_layer"]
+    t_ver = video["verify_gamma%d" % gamma]["us_per_layer"]
+    round_us = gamma * t_draft + t_ver
+    res = {
+        "io_model": {
+            "workload": "video", "gamma": gamma, "K_visual": K, "m_t": m_t, "m_v": m_v,
+            "io_sparse_entries": ba.std_io_sparse(gamma, K, m_t),
+            "io_dense_entries": ba.std_io_dense(m_v, m_t),
+            "io_total_entries": ba.std_io_total(gamma, K, m_t, m_v),
+            "io_average_entries_alpha_1": ba.std_io_average(gamma, K, m_t, m_v, 1.0),
+            "io_vanilla_entries_per_token": m_v + m_t,
+            "alpha_threshold_io": ba.std_alpha_threshold(gamma, K, m_t, m_v),
+            "measured_us_per_layer": {"draft_decode": t_draft, "verify": t_ver, "dense_decode": t_dense,
+                                      "round": round_us},
+            "alpha_threshold_time": round_us / (gamma * t_dense),
+            "note": "alpha_threshold_time: the accepted fraction of the gamma drafts above which a round "
+                    "(gamma draft decodes + one verify) costs less attention time per accepted token than "
+                    "dense decoding; alpha_threshold_io is the page's entry-count condition",
+        },
+        "verify_over_dense": {
+            "video_gamma5": t_ver / t_dense,
+            "llama8b_128k_gamma8": llama128["verify_gamma8"]["us_per_layer"] / llama128["dense"]["us_per_layer"],
+        },
+        "draft_over_dense": {"video": t_draft / t_dense},
+    }
+    td, ttg = t_draft / t_dense, t_ver / t_dense
+    res["sd_speedup_model_video"] = {"gamma": gamma, "td_over_tt": td, "ttg_over_tt": ttg,
+                                     "by_accept_length": {str(tau): ba.sd_speedup(tau, gamma, td, ttg)
+                                                          for tau in range(1, gamma + 2)},
+                                     "note": "SpecVLM's speed-up model with the measured attention kernel times; "
+                                             "the accept length needs a model and is not measured"}
+    return res
+
+
+def next_rows_timings(D, hbm_peak, dev):
+    """Timings of the rows beyond the hot path (each a separate measurement):
       f1  compaction of the selected rows (once per selection) and the decode
-          over the compacted rows, on this workload's lists, every layer;
+          over the compacted rows, on the headline lists, every layer;
       f2  decode over sink + recent lists (4 + 64), every layer;
       f3  SpecVLM selection for one request of the video workload (28 layers x
           4 KV heads of window scores over 12,800 tokens, 12,544 of them video);
       f4  one StD round of the video workload per layer: 5 draft steps (list
           append on the device + sparse decode over the 1,024 kept + drafted
           rows) and the verify of the 5 drafts, in one graph."""
-    sk = path.sk
-    L, B, Hq, Hkv, d, n = path.L, path.B, path.Hq, path.Hkv, path.d, path.n
+    sk = D.sk
+    L, B, Hq, Hkv, d, n = D.L, D.B, D.Hq, D.Hkv, D.d, D.n
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     out = {}
-    # f1
-    kc, vc = [], []
-    for l, lay in enumerate(path.layers):
-        tot = path.totals[l]
-        kc.append(torch.empty((max(tot, 1), d), dtype=torch.bfloat16, device=dev))
-        vc.append(torch.empty((max(tot, 1), d), dtype=torch.bfloat16, device=dev))
+    offs, idx, totals = D.lists[0]
+    kc = [torch.empty((max(t, 1), d), dtype=torch.bfloat16, device=dev) for t in totals]
+    vc = [torch.empty((max(t, 1), d), dtype=torch.bfloat16, device=dev) for t in totals]
     ws_c = sk.new_workspace(sk.workspace_size(sk.OP_COMPACT, B, 0, Hkv, d, 0, 0), dev)
 
     def compact():
-        for l, lay in enumerate(path.layers):
-            sk.compact_kv(lay["k"], lay["v"], path.offs_dev[l], path.idx[l], path.totals[l], k_out=kc[l],
-                          v_out=vc[l], ws=ws_c)
+        for l in range(L):
+            lay = D.lay(l)
+            sk.compact_kv(lay["k"], lay["v"], offs[l], idx[l], totals[l], k_out=kc[l], v_out=vc[l], ws=ws_c)
 
     def contig():
-        for l, lay in enumerate(path.layers):
-            sk.sparse_decode_compact(lay["q"], kc[l], vc[l], path.offs_dev[l], Hkv, path.scale, o=path.o_sp[l],
-                                     lse=path.l_sp[l], ws=path.ws_sp)
-    t_comp = time_graph_us(compact, flush=flush) / L
-    t_contig = time_graph_us(contig, flush=flush) / L
-    mean_total = float(np.mean(path.totals))
+        for l in range(L):
+            sk.sparse_decode_compact(D.lay(l)["q"], kc[l], vc[l], offs[l], Hkv, D.scale, o=D.o_sp[l],
+                                     lse=D.l_sp[l], ws=D.ws_sp)
+    t_comp = time_graph(capture(compact), 10, flush) / L
+    t_contig = time_graph(capture(contig), 10, flush) / L
+    mean_total = float(np.mean(totals))
     b_comp = 2 * mean_total * 4 * d                                  # read and write K and V rows
     b_contig = mean_total * 4 * d + B * Hq * 4 * d                   # K/V rows + q in / o out
     out["f1_compaction"] = {"us_per_layer": t_comp, "alg_bytes_per_layer": b_comp,
@@ -622,16 +770,17 @@ def next_rows_timings(path, hbm_peak, dev):
     out["f1_contiguous_decode"] = {"us_per_layer": t_contig, "alg_bytes_per_layer": b_contig,
                                    "gbs": b_contig / t_contig / 1e3,
                                    "frac_of_measured_hbm": b_contig / t_contig / 1e3 / hbm_peak}
-    assert sk.workspace_status(ws_c) == 0 and sk.workspace_status(path.ws_sp) == 0
+    assert sk.workspace_status(ws_c) == 0 and sk.workspace_status(D.ws_sp) == 0
     del kc, vc
     # f2
     w_offs, w_idx = sk.window_lists(B, Hkv, n, 4, 64, dev)
 
     def window():
-        for l, lay in enumerate(path.layers):
-            sk.sparse_decode_attn(lay["q"], lay["k"], lay["v"], w_offs, w_idx, path.scale, o=path.o_sp[l],
-                                  lse=path.l_sp[l], ws=path.ws_sp)
-    t_win = time_graph_us(window, flush=flush) / L
+        for l in range(L):
+            lay = D.lay(l)
+            sk.sparse_decode_attn(lay["q"], lay["k"], lay["v"], w_offs, w_idx, D.scale, o=D.o_sp[l],
+                                  lse=D.l_sp[l], ws=D.ws_sp)
+    t_win = time_graph(capture(window), 10, flush) / L
     b_win = B * Hkv * 68 * (4 * d + 4) + B * Hq * 4 * d
     out["f2_window_decode"] = {"us_per_layer": t_win, "alg_bytes_per_layer": b_win, "lists": "4 sinks + 64 recent"}
     # f3 and f4 on the video workload
@@ -647,7 +796,7 @@ def next_rows_timings(path, hbm_peak, dev):
 
     def spec():
         sk.specvlm_select(scores, 0, v_hi, 0.5, 0.9, v_hi, vw.n, importance=imp, indices=sidx, counts=cnt, ws=ws_s)
-    t_spec = time_graph_us(spec, flush=flush)
+    t_spec = time_graph(capture(spec), 10, flush)
     out["f3_specvlm_select"] = {"us_per_request": t_spec, "units": units, "tokens": vw.n, "video_tokens": v_hi,
                                 "lam_r": 0.5, "r": 0.9, "kept": int(cnt.item())}
     gam = vw.gamma
@@ -665,7 +814,6 @@ def next_rows_timings(path, hbm_peak, dev):
     ws_sp = sk.new_workspace(sk.workspace_size(sk.OP_SPARSE_DECODE, vw.batch, vw.hq, vw.hkv, vw.d, 0, 0), dev)
     ws_de = sk.new_workspace(sk.workspace_size(sk.OP_DENSE_VERIFY, vw.batch, vw.hq, vw.hkv, vw.d, vw.n + gam, gam),
                              dev)
-
     q_step = [lay["q_ver"][:, :, t].contiguous() for t in range(gam)]   # each draft step's query
 
     def round_():
@@ -675,7 +823,7 @@ def next_rows_timings(path, hbm_peak, dev):
             sk.sparse_decode_attn(q_step[t], lay["k"], lay["v"], d_offs[t], d_idx[t], vs, o=o_d, ws=ws_sp,
                                   want_lse=False)
         sk.dense_verify_attn(lay["q_ver"], lay["k"], lay["v"], vw.n, vs, o=o_v, ws=ws_de, want_lse=False)
-    t_round = time_graph_us(round_, flush=flush)
+    t_round = time_graph(capture(round_), 10, flush)
     out["f4_std_round"] = {"us_per_layer": t_round, "us_per_step_all_layers": t_round * vw.layers, "gamma": gam,
                            "kept_per_head": kh, "launches_per_layer": gam + 2}
     return out
@@ -690,12 +838,14 @@ def run_sdkv(args, world, rank, local):
     if args.layers:
         w = dataclasses.replace(w, layers=args.layers)
     hbm_peak, peak_kind = peaks()
-    path = Path(w, args.keep_index, dev)
-    path.capture()
+    ki = args.keep_index
+    D = Decode(w, dev)
+    D.prefill((ki,))
+    step_graph = capture(lambda: D.sparse_step(ki))          # the decode step: a4 of every layer
     warm = max(args.warmup, 3)
     K = args.steps
     for _ in range(warm):
-        path.step()
+        step_graph.replay()
     torch.cuda.synchronize()
 
     uuid = None
@@ -705,84 +855,79 @@ def run_sdkv(args, world, rank, local):
         pass
     sampler = ClockSampler(args.clocks_log)
     time.sleep(0.25)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(Path.PHASES) + 1)] for _ in range(K)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.time()
     start.record()
-    for i in range(K):
-        path.step(evs[i])
+    for _ in range(K):
+        step_graph.replay()
     end.record()
     torch.cuda.synchronize()
     barrier(world)
     t1 = time.time()
     clocks = sampler.stop(t0, t1, uuid)
-    total_ms = max_over_ranks(start.elapsed_time(end), world)
-    phase_ms = {ph: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)) / K
-                for j, ph in enumerate(Path.PHASES)}
-    us_step = total_ms / K * 1e3
-
-    # device-side status words must be clean
-    for wsb in (path.ws_score, path.ws_sel, path.ws_sp, path.ws_de):
-        st = path.sk.workspace_status(wsb)
+    us_step = max_over_ranks(start.elapsed_time(end), world) / K * 1e3
+    for ws in D.workspaces():
+        st = D.sk.workspace_status(ws)
         if st != 0:
             raise SystemExit("device status %d raised during the bench" % st)
 
-    alg = path.alg_bytes_per_layer()
-    L = path.L
-    breakdown = {}
-    for ph in Path.PHASES:
-        per_layer_us = phase_ms[ph] * 1e3 / L
-        gbs = alg[ph] / (per_layer_us * 1e-6) / 1e9
-        breakdown[ph] = {"us_per_step": phase_ms[ph] * 1e3, "us_per_layer": per_layer_us,
-                         "alg_bytes_per_layer": alg[ph], "gbs": gbs,
-                         "frac_of_measured_hbm": gbs / hbm_peak, "frac_of_8tbs_nominal": gbs / NOMINAL_HBM_GBS}
-    dominant = max(Path.PHASES, key=lambda ph: phase_ms[ph])
-    dom = breakdown[dominant]
-    kernel_names = {"score": "sdkv_score_obs_window (score_kernel pass 1 + pass 2)",
-                    "select": "sdkv_select_topk (select_topk_kernel)",
-                    "sparse": "sdkv_sparse_decode_attn (attn_splitk_kernel, gathered)",
-                    "dense": "sdkv_dense_verify_attn (attn_splitk_kernel, dense)"}
-    roofline = {"bound": "hbm", "achieved": dom["gbs"], "peak": hbm_peak, "unit": "GB/s",
-                "frac": dom["gbs"] / hbm_peak, "traffic": traffic_from_profiles(dominant, w.name),
-                "kernel": kernel_names[dominant], "peak_kind": peak_kind,
-                "alg_bytes_per_launch": dom["alg_bytes_per_layer"], "us_per_launch": dom["us_per_layer"]}
-    keep = ("%d" % w.keep[args.keep_index]) if w.keep else "ragged SparseMM budgets"
+    L = D.L
+    reps = max(10, min(K, 50))
+    breakdown = {"sparse": phase_record(us_step, L, D.alg_bytes("sparse", ki), hbm_peak)}
+    breakdown["sparse"]["kept_per_head_mean"] = D.mean_total(ki) / D.BH
+    g = capture(D.dense_step)
+    breakdown["dense"] = phase_record(time_graph(g, reps), L, D.alg_bytes("dense"), hbm_peak)
+    del g
+    g = capture(D.score_all)
+    breakdown["score"] = phase_record(time_graph(g, reps), L, D.alg_bytes("score"), hbm_peak)
+    del g
+    g = capture(lambda: D.select_all(ki))
+    breakdown["select"] = phase_record(time_graph(g, reps), L, D.alg_bytes("select", ki), hbm_peak)
+    del g
+    prefill_us = breakdown["score"]["us_per_step"] + breakdown["select"]["us_per_step"]
+    sp = breakdown["sparse"]
+    roofline = {"bound": "hbm", "achieved": sp["gbs"], "peak": hbm_peak, "unit": "GB/s",
+                "frac": sp["gbs"] / hbm_peak, "traffic": traffic_from_profiles("sparse", w.name),
+                "kernel": "sdkv_sparse_decode_attn (attn_splitk_kernel, gathered)", "peak_kind": peak_kind,
+                "alg_bytes_per_launch": sp["alg_bytes_per_layer"], "us_per_launch": sp["us_per_layer"]}
     line = {
         "metric": METRIC, "value": us_step, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": warm,
         "ms_per_step": us_step / 1e3, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "%s: %d layers x (%d q / %d KV heads, d=%d), batch %d, context %d, window %d, "
-                               "keep %s per head (%d sinks + %d recent + top-K)" % (
-                                   w.name, w.layers, w.hq, w.hkv, w.d, w.batch, w.n, w.window, keep,
-                                   w.n_sink, w.n_recent),
-                   "l2": "inputs larger than L2: %d distinct layers, %.2f GB of K/V per step" % (
-                       L, L * 2 * w.batch * w.hkv * w.n * w.d * 2 / 1e9),
-                   "step": "a1 budgets (host) + a2 score + a3 select + a4 sparse decode + a5 dense decode, "
-                           "all layers; a2..a5 one CUDA graph each"},
+        "config": workload_config(w, ki),
+        "dense_decode_us_per_step": breakdown["dense"]["us_per_step"],
+        "prefill_select": {"us_per_sequence": prefill_us, "us_per_layer": prefill_us / L,
+                           "what": "a2 window scoring + a3 top-K selection of every layer, once per sequence"},
         "sparse_vs_dense": {
-            "sparse_us_per_step": breakdown["sparse"]["us_per_step"],
+            "sparse_us_per_step": us_step,
             "dense_us_per_step": breakdown["dense"]["us_per_step"],
-            "speedup": breakdown["dense"]["us_per_step"] / breakdown["sparse"]["us_per_step"],
-            "byte_bound": alg["dense"] / alg["sparse"],
-            "sparse_frac_of_measured_hbm": breakdown["sparse"]["frac_of_measured_hbm"],
+            "speedup": breakdown["dense"]["us_per_step"] / us_step,
+            "byte_bound": D.alg_bytes("dense") / D.alg_bytes("sparse", ki),
+            "sparse_frac_of_measured_hbm": sp["frac_of_measured_hbm"],
             "dense_frac_of_measured_hbm": breakdown["dense"]["frac_of_measured_hbm"],
-            "sparse_frac_of_8tbs": breakdown["sparse"]["frac_of_8tbs_nominal"],
+            "sparse_frac_of_8tbs": sp["frac_of_8tbs_nominal"],
             "dense_frac_of_8tbs": breakdown["dense"]["frac_of_8tbs_nominal"],
         },
         "breakdown": breakdown,
         "roofline": roofline,
-        "gpu_launches": path.launches_per_step() * K,
+        "gpu_launches": L * K,
         "clocks": clocks,
     }
     if not args.no_e2e:
-        line["e2e"] = run_e2e(path, min(K, 5), world)
+        line["e2e"] = run_e2e(D, ki, max(3, min(K, 20)), world)
     if rank == 0 and not args.no_next:
-        line["next_rows"] = next_rows_timings(path, hbm_peak, dev)
+        line["next_rows"] = next_rows_timings(D, hbm_peak, dev)
+    del D, step_graph
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_configs:
+        cfg = config_blocks(hbm_peak, dev, 20)
+        line["configs"] = cfg
+        line.update(io_model(cfg["video"], cfg["llama8b_128k"]))
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, lambda l: path.layers[l], args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(w, ki)
     if rank == 0:
         print(json.dumps(line))
 

@@ -65,3 +65,41 @@ def score_bytes(B: int, Hq: int, Hkv: int, d: int, n: int, W: int) -> int:
 def select_bytes(B: int, Hkv: int, n: int, total_selected: int) -> int:
     """fp32 scores in + int32 list out."""
     return B * Hkv * n * 4 + 4 * total_selected
+
+
+# --- the StD I/O model (Sparse-to-Dense page, 3.3 I/O complexity) -------------
+# Counted in KV entries read per decode round: the sparse draft model reads the
+# K selected visual entries and all m_t text entries for each of gamma drafted
+# tokens; the dense verify reads all m_v + m_t entries once.
+
+def std_io_sparse(gamma: int, K: int, m_t: int) -> int:
+    return gamma * (K + m_t)
+
+
+def std_io_dense(m_v: int, m_t: int) -> int:
+    return m_v + m_t
+
+
+def std_io_total(gamma: int, K: int, m_t: int, m_v: int) -> int:
+    return std_io_sparse(gamma, K, m_t) + std_io_dense(m_v, m_t)
+
+
+def std_io_average(gamma: int, K: int, m_t: int, m_v: int, alpha: float) -> float:
+    """Entries read per accepted token when a fraction alpha of the gamma drafts
+    is accepted: I/O_total / (alpha gamma)."""
+    return std_io_total(gamma, K, m_t, m_v) / (alpha * gamma)
+
+
+def std_alpha_threshold(gamma: int, K: int, m_t: int, m_v: int) -> float:
+    """Acceptance ratio above which StD reads fewer entries per token than
+    vanilla decoding (m_v + m_t per token): (K + m_t) / (m_v + m_t) + 1 / gamma."""
+    return (K + m_t) / (m_v + m_t) + 1.0 / gamma
+
+
+# --- the speculative-decoding speed-up model (SpecVLM page, SD in 60 seconds) --
+
+def sd_speedup(tau: float, gamma: int, td_over_tt: float, ttg_over_tt: float) -> float:
+    """tau / (gamma T_d / T_t + T_t^gamma / T_t): accept length over the cost of
+    gamma draft passes plus one verification of gamma tokens, in units of one
+    target decode pass."""
+    return tau / (gamma * td_over_tt + ttg_over_tt)

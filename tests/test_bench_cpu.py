@@ -38,7 +38,7 @@ def test_keep_lengths_of_the_workloads():
 def test_reference_arm_prints_one_json_line():
     env = dict(os.environ, PYTHONPATH=ROOT)
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
-                        "tiny", "--steps", "1", "--warmup", "0"], capture_output=True, text=True, env=env,
+                        "tiny", "--steps", "2", "--warmup", "0"], capture_output=True, text=True, env=env,
                        timeout=600)
     assert r.returncode == 0, r.stderr
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
@@ -49,15 +49,20 @@ def test_reference_arm_prints_one_json_line():
     assert rec["e2e"]["h2d_bytes_per_step"] == 0
     assert rec["cpu_baseline"]["kind"] == "oracle"
     assert rec["warmup"] >= 3
+    # whole steps are timed (the tiny workload has 4 units), so the line's time fits its own run
+    assert rec["units_timed_per_step"] == rec["units_per_step"] == 4 and not rec["extrapolated"]
+    assert rec["ms_per_step"] * rec["steps"] / 1e3 <= rec["run_wall_s"]
+    # the same config as the GPU arm prints
+    import bench
+    assert rec["config"] == bench.workload_config(workloads.by_name("tiny"), 0)
 
 
 def test_cpu_baseline_on_worker_processes():
     import bench
-    w = workloads.by_name("tiny")
-    lay = workloads.make_layer(w, 0, device="cpu")
-    rec = bench.cpu_baseline(w, lambda l: lay, 0.5)
+    rec = bench.cpu_baseline(workloads.by_name("tiny"), 0, timed_rounds=1)
     assert rec["kind"] == "oracle" and rec["value"] > 0
-    assert rec["cores"] == bench.host_cores() and "worker processes" in rec["sample"]
+    assert rec["cores"] == min(bench.host_cores(), 4) and "worker processes" in rec["sample"]
+    assert not rec["extrapolated"]
 
 
 def test_cpu_baseline_falls_back_to_one_process(monkeypatch):
@@ -66,11 +71,19 @@ def test_cpu_baseline_falls_back_to_one_process(monkeypatch):
     def no_workers(*args, **kwargs):
         raise RuntimeError("no workers here")
 
-    monkeypatch.setattr(bench, "oracle_parallel", no_workers)
-    w = workloads.by_name("tiny")
-    lay = workloads.make_layer(w, 0, device="cpu")
-    rec = bench.cpu_baseline(w, lambda l: lay, 0.5)
+    monkeypatch.setattr(bench, "oracle_decode_rounds", no_workers)
+    rec = bench.cpu_baseline(workloads.by_name("tiny"), 0, timed_rounds=1)
     assert rec["cores"] == 1 and rec["value"] > 0 and "no workers here" in rec["sample"]
+
+
+def test_oracle_step_plan_samples_large_steps_evenly():
+    import bench
+    w = workloads.by_name("sparsemm")
+    units, sampled = bench.oracle_step_plan(w, 512)
+    assert sampled and len(units) == 512 and len(set(units)) == 512
+    assert units[0] == (0, 0, 0) and units[-1][0] == w.layers - 1
+    units, sampled = bench.oracle_step_plan(workloads.by_name("llama8b_32k"), 512)
+    assert not sampled and len(units) == 32 * 8
 
 
 def test_traffic_figures_only_for_their_sources_and_workload(tmp_path, monkeypatch):
@@ -125,3 +138,25 @@ def test_bench_max_over_ranks_gloo_two_ranks():
         p.join(timeout=60)
         assert p.exitcode == 0
     assert res == [(0, 2, 15.0), (1, 2, 15.0)]
+
+
+def test_std_io_model_of_the_video_workload():
+    # StD 3.3: I/O_sparse = gamma (K + m_t), I/O_dense = m_v + m_t, average over alpha gamma
+    # accepted tokens; video workload: gamma 5, K = 768 visual, m_t = 256 text, m_v = 12 544
+    assert ba.std_io_sparse(5, 768, 256) == 5 * 1024
+    assert ba.std_io_dense(12544, 256) == 12800
+    assert ba.std_io_total(5, 768, 256, 12544) == 17920
+    # every draft accepted: 17 920 / 5 entries per token against 12 800 for vanilla decoding
+    assert ba.std_io_average(5, 768, 256, 12544, 1.0) == 3584.0
+    a = ba.std_alpha_threshold(5, 768, 256, 12544)
+    assert abs(a - (1024 / 12800 + 0.2)) < 1e-15
+    # at the threshold the average equals the vanilla per-token I/O, below it StD reads more
+    assert abs(ba.std_io_average(5, 768, 256, 12544, a) - 12800) < 1e-9
+    assert ba.std_io_average(5, 768, 256, 12544, 0.9 * a) > 12800
+
+
+def test_sd_speedup_model():
+    # SpecVLM: Speedup = tau / (gamma T_d/T_t + T_t^gamma/T_t); a free draft and a verify as
+    # cheap as one decode give the accept length itself
+    assert ba.sd_speedup(3.0, 4, 0.0, 1.0) == 3.0
+    assert abs(ba.sd_speedup(4.0, 4, 0.25, 1.0) - 2.0) < 1e-15
