@@ -233,20 +233,31 @@ int sdkv_dense_verify_attn(const void* q, const void* k, const void* v,
  * than that returns SDKV_ERR_UNSUPPORTED (use sdkv_dense_verify_attn then).
  *  - The first call on a device looks up the array's device address (once per
  *    device, with that device current); make that first call before any
- *    stream capture.
+ *    stream capture.  The address belongs to the device's current CUDA
+ *    context: after a device reset (cudaDeviceReset, from any runtime in the
+ *    process) the next call, in the new context, looks it up again, so that
+ *    call too belongs before any capture.
  *  - Each call clears the counters and status word it needs (an asynchronous
  *    memset on `stream`, not an allocation) and calls no cudaMalloc/cudaFree.
  *  - Every call on a device uses that device's one copy of the array: calls
  *    that may overlap on the same GPU (for example on different streams) race
  *    on it and give wrong results.  Serialise them.
- * Device-side errors set the array's status word, which this API does not
- * expose; argument errors are reported as for sdkv_dense_verify_attn.
+ * Device-side errors (a bounded wait that ran out) set the array's status
+ * word: read it with sdkv_dense_verify_attn_noalloc_status before the next
+ * call clears it.  Argument errors are reported as for sdkv_dense_verify_attn.
  */
 #define SDKV_NOALLOC_SCRATCH_BYTES (8u << 20)   /* 8 MiB */
 int sdkv_dense_verify_attn_noalloc(const void* q, const void* k, const void* v,
                                    const int64_t kv_strides[3], int32_t B, int32_t Hq,
                                    int32_t Hkv, int32_t d, int32_t n_prefix, int32_t gamma,
                                    float scale, void* o, float* lse, void* stream);
+
+/*
+ * Synchronous diagnostic for sdkv_dense_verify_attn_noalloc: waits for
+ * `stream`, copies the status word of the current device's fixed array to
+ * *status (one of SDKV_DEV_*), then clears it.  Allocates nothing.
+ */
+int sdkv_dense_verify_attn_noalloc_status(int32_t* status, void* stream);
 
 /*
  * Synchronous diagnostic: waits for `stream`, copies the device status word of

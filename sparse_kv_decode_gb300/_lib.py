@@ -83,6 +83,8 @@ def lib() -> ctypes.CDLL:
     L.sdkv_dense_verify_attn_noalloc.argtypes = [_c_vp, _c_vp, _c_vp, _I64x3, _c_i32, _c_i32, _c_i32, _c_i32,
                                                  _c_i32, _c_i32, _c_f, _c_vp, _c_vp, _c_vp]
     L.sdkv_dense_verify_attn_noalloc.restype = ctypes.c_int
+    L.sdkv_dense_verify_attn_noalloc_status.argtypes = [ctypes.POINTER(_c_i32), _c_vp]
+    L.sdkv_dense_verify_attn_noalloc_status.restype = ctypes.c_int
     L.sdkv_workspace_status.argtypes = [_c_vp, ctypes.POINTER(_c_i32), _c_vp]
     L.sdkv_workspace_status.restype = ctypes.c_int
     L.sdkv_window_lists.argtypes = [_c_i32, _c_i32, _c_i32, _c_i32, _c_i32, _c_vp, _c_vp, _c_vp]

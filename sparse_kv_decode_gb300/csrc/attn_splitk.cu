@@ -1219,10 +1219,41 @@ int launch_sparse_decode_compact(const AttnLaunch& a, const CUtensorMap* tmk, co
 // -------------------------------------------------------------------------------------
 static __device__ __align__(256) uint8_t g_noalloc_scratch[SDKV_NOALLOC_SCRATCH_BYTES];
 
-int dense_verify_noalloc(const AttnLaunch& a_in, const CUtensorMap* tmk, const CUtensorMap* tmv, int num_sms,
-                         const char** why) {
+namespace {
+
+// Unique id of the calling thread's current CUDA context (0 if it cannot be
+// read).  A device reset destroys the context the array's address belongs to;
+// the next context has another id, so the address is looked up again.
+unsigned long long current_ctx_id() {
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, &id) == CUDA_SUCCESS)
+        return id;
+    return 0;
+}
+
+// Device address of the array on the current device: looked up with
+// cudaGetSymbolAddress once per device and context, cached after that.
+int noalloc_scratch(void** out, const char** why) {
     static std::mutex mu;
     static void* dev_ptr[64] = {};
+    static unsigned long long dev_ctx[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) {
@@ -1233,6 +1264,28 @@ int dense_verify_noalloc(const AttnLaunch& a_in, const CUtensorMap* tmk, const C
         *why = "device ordinal above 63";
         return SDKV_ERR_UNSUPPORTED;
     }
+    // 0 before the thread has a current context: the lookup below creates it,
+    // and the next call, seeing the real id, looks the address up once more
+    const unsigned long long ctx = current_ctx_id();
+    std::lock_guard<std::mutex> lock(mu);
+    if (!dev_ptr[dev] || dev_ctx[dev] != ctx) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess || ptr == nullptr) {
+            *why = e != cudaSuccess ? cudaGetErrorString(e) : "cudaGetSymbolAddress returned null";
+            return SDKV_ERR_CUDA;
+        }
+        dev_ptr[dev] = ptr;
+        dev_ctx[dev] = ctx;
+    }
+    *out = dev_ptr[dev];
+    return SDKV_OK;
+}
+
+}  // namespace
+
+int dense_verify_noalloc(const AttnLaunch& a_in, const CUtensorMap* tmk, const CUtensorMap* tmv, int num_sms,
+                         const char** why) {
     const size_t need = dense_ws_bytes(a_in.B, a_in.Hq, a_in.Hkv, a_in.d, a_in.n_prefix + a_in.gamma, a_in.gamma,
                                        num_sms);
     if (need > static_cast<size_t>(SDKV_NOALLOC_SCRATCH_BYTES)) {
@@ -1241,22 +1294,11 @@ int dense_verify_noalloc(const AttnLaunch& a_in, const CUtensorMap* tmk, const C
         return SDKV_ERR_UNSUPPORTED;
     }
     void* ptr = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (!dev_ptr[dev]) {
-            void* p = nullptr;
-            e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-            if (e != cudaSuccess || p == nullptr) {
-                *why = e != cudaSuccess ? cudaGetErrorString(e) : "cudaGetSymbolAddress returned null";
-                return SDKV_ERR_CUDA;
-            }
-            dev_ptr[dev] = p;
-        }
-        ptr = dev_ptr[dev];
-    }
+    int rc = noalloc_scratch(&ptr, why);
+    if (rc) return rc;
     // The array keeps the previous call's contents: the status word and the
     // per-head counters must start at zero.
-    e = cudaMemsetAsync(ptr, 0, kWsHeader + align256(attn_ticket_bytes(a_in.B * a_in.Hkv)), a_in.stream);
+    cudaError_t e = cudaMemsetAsync(ptr, 0, kWsHeader + align256(attn_ticket_bytes(a_in.B * a_in.Hkv)), a_in.stream);
     if (e != cudaSuccess) {
         *why = cudaGetErrorString(e);
         return SDKV_ERR_CUDA;
@@ -1265,6 +1307,20 @@ int dense_verify_noalloc(const AttnLaunch& a_in, const CUtensorMap* tmk, const C
     a.ws = ptr;
     a.ws_bytes = SDKV_NOALLOC_SCRATCH_BYTES;
     return launch_dense_verify(a, tmk, tmv, num_sms, why);
+}
+
+int noalloc_status(int32_t* status, cudaStream_t st, const char** why) {
+    void* ptr = nullptr;
+    int rc = noalloc_scratch(&ptr, why);
+    if (rc) return rc;
+    cudaError_t e = cudaMemcpyAsync(status, ptr, sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ptr, 0, sizeof(int32_t), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) {
+        *why = cudaGetErrorString(e);
+        return SDKV_ERR_CUDA;
+    }
+    return SDKV_OK;
 }
 
 }  // namespace sdkv

@@ -424,6 +424,15 @@ int sdkv_dense_verify_attn_noalloc(const void* q, const void* k, const void* v, 
     return SDKV_OK;
 }
 
+int sdkv_dense_verify_attn_noalloc_status(int32_t* status, void* stream) {
+    if (!status) return fail(SDKV_ERR_INVALID_ARG, "null pointer");
+    const char* why = "";
+    const int rc = noalloc_status(status, static_cast<cudaStream_t>(stream), &why);
+    if (rc) return fail(rc, why);
+    g_last_error.clear();
+    return SDKV_OK;
+}
+
 int sdkv_workspace_status(void* ws, int32_t* status, void* stream) {
     if (!ws || !status) return fail(SDKV_ERR_INVALID_ARG, "null pointer");
     cudaStream_t st = static_cast<cudaStream_t>(stream);

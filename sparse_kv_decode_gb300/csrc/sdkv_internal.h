@@ -52,6 +52,8 @@ int launch_sparse_decode_compact(const AttnLaunch& a, const CUtensorMap* tmk, co
 // dense verify with its scratch in the library's fixed device array (no allocation)
 int dense_verify_noalloc(const AttnLaunch& a, const CUtensorMap* tmk, const CUtensorMap* tmv, int num_sms,
                          const char** why);
+// status word of the fixed array on the current device: read, then cleared (synchronous on st)
+int noalloc_status(int32_t* status, cudaStream_t st, const char** why);
 
 // ---- observation-window scoring (score_obs.cu) --------------------------------
 struct ScoreLaunch {

@@ -7,8 +7,10 @@ sdkv_dense_verify_attn_noalloc keeps its scratch in a fixed array inside the
 library.  This test calls it through the C ABI, twice in a row (the second call
 sees the first call's leftovers in the shared array), and checks each result
 against sdkv_dense_verify_attn with a workspace, within the tolerances of the
-other GPU tests.  It also checks that a shape needing more scratch than the
-array holds is refused with an error.  The file sorts last on purpose.
+other GPU tests; one small case is also checked against the fp64 oracle, with
+the array's status word read after each call.  It also checks that a shape
+needing more scratch than the array holds is refused with an error.  The file
+sorts last on purpose.
 """
 import ctypes
 import math
@@ -69,6 +71,35 @@ def test_noalloc_matches_workspace_call_twice(B, Hq, Hkv, d, n_prefix, gamma):
         assert torch.isfinite(o).all()
         assert diff.max().item() <= MAX_ABS and diff.mean().item() <= MEAN_ABS, (call, diff.max().item())
         assert (lse - l_ref).abs().max().item() <= LSE_ABS
+
+
+def _status():
+    st = ctypes.c_int32(-1)
+    rc = sk.lib().sdkv_dense_verify_attn_noalloc_status(ctypes.byref(st), torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, sk.lib().sdkv_last_error()
+    return st.value
+
+
+def test_noalloc_matches_oracle_and_reports_a_clean_status():
+    # the tiny workload's gamma = 4 verify, checked against the fp64 oracle itself
+    # (not only against the workspace call), twice, reading the status word after each
+    import numpy as np
+    import oracle
+    import workloads
+    w = workloads.by_name("tiny")
+    t = workloads.make_layer(w, 0, device="cpu")
+    k, v = t["k"].to(DEV), t["v"].to(DEV)
+    n_prefix, scale = w.n - w.gamma, 1.0 / math.sqrt(w.d)
+    o_ref, l_ref = oracle.dense_verify(t["q_ver"], t["k"], t["v"], n_prefix, scale)
+    for _ in range(2):
+        q = t["q_ver"].to(DEV)
+        o = torch.full_like(q, float("nan"))
+        lse = torch.full(q.shape[:3], float("nan"), device=DEV)
+        assert _noalloc(q, k, v, n_prefix, scale, o, lse) == 0, sk.lib().sdkv_last_error()
+        assert _status() == 0
+        diff = np.abs(o.cpu().double().numpy() - o_ref)
+        assert diff.max() <= MAX_ABS and diff.mean() <= MEAN_ABS
+        assert np.abs(lse.cpu().double().numpy() - l_ref).max() <= LSE_ABS
 
 
 def test_noalloc_refuses_shapes_beyond_its_scratch():
