@@ -253,6 +253,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, KIND>::NT)
                        const __grid_constant__ CUtensorMap tmv) {
     using C = AttnCfg<D, MT, KW, TK, STAGES, KIND>;
     constexpr bool SPARSE = (KIND != kDense);    // list-driven chunk plan, no causal limits
+    constexpr bool kTwoTermP = (MT == 1);        // P as hi + lo bf16 terms (see the PV product)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem =
         reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -538,17 +539,33 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, KIND>::NT)
                 for (int nt = 0; nt < 2; ++nt) {
                     x[nt][2 * i] = fast_exp2(x[nt][2 * i] - muse);
                     x[nt][2 * i + 1] = fast_exp2(x[nt][2 * i + 1] - muse);
+                    if constexpr (!kTwoTermP) {
+                        // the weights the PV product will use, rounded once to bf16
+                        x[nt][2 * i] = __bfloat162float(__float2bfloat16_rn(x[nt][2 * i]));
+                        x[nt][2 * i + 1] = __bfloat162float(__float2bfloat16_rn(x[nt][2 * i + 1]));
+                    }
                     l_r[i] += x[nt][2 * i] + x[nt][2 * i + 1];
                 }
             }
-            // P as two bf16 terms, p = hi + lo (about 16 significant bits): the
-            // weights of the PV product then match the fp32 sum l closely even
-            // when a few keys carry the whole softmax
+            // One row tile (decode): P as two bf16 terms, p = hi + lo (about 16
+            // significant bits), so the weights of the PV product match the fp32
+            // sum l even when a few keys carry the whole softmax.  Several row
+            // tiles (the gamma-query verify, where the contraction is the limit):
+            // P as one bf16 term and l summed from those same rounded weights, so
+            // the output is an exactly normalised average with weights within
+            // 2^-9 relative of the fp32 ones.
             uint32_t pa[4], pl[4];
-            split_bf16(x[0][0], x[0][1], pa[0], pl[0]);
-            split_bf16(x[0][2], x[0][3], pa[1], pl[1]);
-            split_bf16(x[1][0], x[1][1], pa[2], pl[2]);
-            split_bf16(x[1][2], x[1][3], pa[3], pl[3]);
+            if constexpr (kTwoTermP) {
+                split_bf16(x[0][0], x[0][1], pa[0], pl[0]);
+                split_bf16(x[0][2], x[0][3], pa[1], pl[1]);
+                split_bf16(x[1][0], x[1][1], pa[2], pl[2]);
+                split_bf16(x[1][2], x[1][3], pa[3], pl[3]);
+            } else {
+                pa[0] = pack_bf16(x[0][0], x[0][1]);
+                pa[1] = pack_bf16(x[0][2], x[0][3]);
+                pa[2] = pack_bf16(x[1][0], x[1][1]);
+                pa[3] = pack_bf16(x[1][2], x[1][3]);
+            }
 #pragma unroll
             for (int jj = 0; jj < D / 16; ++jj) {
                 uint32_t vb[4];
@@ -556,8 +573,10 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, KIND>::NT)
                 ldsm_x4_t(vb, tile_addr<D, TK, SPARSE>(vst, row, 2 * jj + (lane >> 4)));
                 mma_bf16_16816(o_acc[2 * jj], pa, vb[0], vb[1]);
                 mma_bf16_16816(o_acc[2 * jj + 1], pa, vb[2], vb[3]);
-                mma_bf16_16816(o_acc[2 * jj], pl, vb[0], vb[1]);
-                mma_bf16_16816(o_acc[2 * jj + 1], pl, vb[2], vb[3]);
+                if constexpr (kTwoTermP) {
+                    mma_bf16_16816(o_acc[2 * jj], pl, vb[0], vb[1]);
+                    mma_bf16_16816(o_acc[2 * jj + 1], pl, vb[2], vb[3]);
+                }
             }
         }
         __syncwarp();

@@ -11,7 +11,7 @@ import torch
 import oracle
 import sparse_kv_decode_gb300 as sk
 import workloads
-from gpu_common import (assert_attn_close, assert_lse_close, assert_scores_close,
+from gpu_common import (LSE_MAX_ABS, assert_attn_close, assert_lse_close, assert_scores_close,
                         check_selection_gap_rule, csr, f64, scale_of)
 
 pytestmark = pytest.mark.gpu
@@ -95,7 +95,9 @@ def test_verify_equals_sequential_single_decodes_on_gpu():
     for t in range(gamma):
         o1, l1 = sk.dense_verify_attn(q[:, :, t:t + 1].contiguous(), k, v, n_prefix + t, scale_of(d))
         assert (f64(o[:, :, t]) - f64(o1[:, :, 0])).__abs__().max() <= 1e-2
-        assert (f64(lse[:, :, t]) - f64(l1[:, :, 0])).__abs__().max() <= 1e-4
+        # the verify sums its bf16-rounded weights (several row tiles), the decode
+        # its fp32 ones: they agree within the lse tolerance both keep to the oracle
+        assert (f64(lse[:, :, t]) - f64(l1[:, :, 0])).__abs__().max() <= LSE_MAX_ABS
 
 
 # ---------------------------------------------------------------------------
