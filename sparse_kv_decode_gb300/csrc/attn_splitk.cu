@@ -490,82 +490,91 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, KIND>::NT)
         }
         const uint32_t kst = sbase + C::OFF_K + s * C::TILE_B;
         const uint32_t vst = sbase + C::OFF_V + s * C::TILE_B;
+        // Scores of all KPW keys of this warp's group first: the sub-steps of 16
+        // keys are independent accumulator chains, interleaved over the head dims
+        constexpr int NSUB = C::KPW / 16;
+        float sacc[2 * NSUB][4];
 #pragma unroll
-        for (int sub = 0; sub < C::KPW / 16; ++sub) {
-            const int krow0 = kw * C::KPW + sub * 16;
-            float sacc[2][4];
+        for (int nt = 0; nt < 2 * NSUB; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+        for (int ks = 0; ks < D / 16; ++ks) {
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
+            for (int sub = 0; sub < NSUB; ++sub) {
                 uint32_t kb[4];
-                const int row = krow0 + (lane & 7) + ((lane >> 4) << 3);
+                const int row = kw * C::KPW + sub * 16 + (lane & 7) + ((lane >> 4) << 3);
                 ldsm_x4(kb, tile_addr<D, TK, SPARSE>(kst, row, 2 * ks + ((lane >> 3) & 1)));
-                mma_bf16_16816(sacc[0], qa[ks], kb[0], kb[1]);
-                mma_bf16_16816(sacc[1], qa[ks], kb[2], kb[3]);
+                mma_bf16_16816(sacc[2 * sub], qa[ks], kb[0], kb[1]);
+                mma_bf16_16816(sacc[2 * sub + 1], qa[ks], kb[2], kb[3]);
             }
-            // scale into the log2 domain and mask
-            const int cpos = t * TK + krow0 + 2 * (lane & 3);  // position within [lo, hi) of column (0, 0)
-            float x[2][4];
+        }
+        // scale into the log2 domain and mask
+        const int cpos = t * TK + kw * C::KPW + 2 * (lane & 3);  // position within [lo, hi) of column (0, 0)
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < 2 * NSUB; ++nt) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int col = cpos + nt * 8 + (e & 1);
-                    bool valid = col < nkeys;
-                    if constexpr (!SPARSE) valid = valid && (lo + col <= lim[e >> 1]);
-                    x[nt][e] = valid ? sacc[nt][e] * p.scale_log2 : -INFINITY;
-                }
+            for (int e = 0; e < 4; ++e) {
+                const int col = cpos + nt * 8 + (e & 1);
+                bool valid = col < nkeys;
+                if constexpr (!SPARSE) valid = valid && (lo + col <= lim[e >> 1]);
+                sacc[nt][e] = valid ? sacc[nt][e] * p.scale_log2 : -INFINITY;
             }
-            // online softmax per row (rows r0 and r0 + 8; a quad shares a row)
+        }
+        // online softmax per row over the group's keys (rows r0 and r0 + 8; a quad shares a row)
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                float mx = fmaxf(fmaxf(x[0][2 * i], x[0][2 * i + 1]), fmaxf(x[1][2 * i], x[1][2 * i + 1]));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                const float mnew = fmaxf(m_r[i], mx);
-                const float muse = (mnew == -INFINITY) ? 0.f : mnew;
-                if (mnew != m_r[i]) {
-                    const float alpha = fast_exp2(m_r[i] - muse);
-                    l_r[i] *= alpha;
+        for (int i = 0; i < 2; ++i) {
+            float mx = -INFINITY;
 #pragma unroll
-                    for (int j = 0; j < D / 8; ++j) {
-                        o_acc[j][2 * i] *= alpha;
-                        o_acc[j][2 * i + 1] *= alpha;
-                    }
-                    m_r[i] = mnew;
+            for (int nt = 0; nt < 2 * NSUB; ++nt) mx = fmaxf(mx, fmaxf(sacc[nt][2 * i], sacc[nt][2 * i + 1]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float mnew = fmaxf(m_r[i], mx);
+            const float muse = (mnew == -INFINITY) ? 0.f : mnew;
+            if (mnew != m_r[i]) {
+                const float alpha = fast_exp2(m_r[i] - muse);
+                l_r[i] *= alpha;
+#pragma unroll
+                for (int j = 0; j < D / 8; ++j) {
+                    o_acc[j][2 * i] *= alpha;
+                    o_acc[j][2 * i + 1] *= alpha;
                 }
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    x[nt][2 * i] = fast_exp2(x[nt][2 * i] - muse);
-                    x[nt][2 * i + 1] = fast_exp2(x[nt][2 * i + 1] - muse);
-                    if constexpr (!kTwoTermP) {
-                        // the weights the PV product will use, rounded once to bf16
-                        x[nt][2 * i] = __bfloat162float(__float2bfloat16_rn(x[nt][2 * i]));
-                        x[nt][2 * i + 1] = __bfloat162float(__float2bfloat16_rn(x[nt][2 * i + 1]));
-                    }
-                    l_r[i] += x[nt][2 * i] + x[nt][2 * i + 1];
-                }
+                m_r[i] = mnew;
             }
-            // One row tile (decode): P as two bf16 terms, p = hi + lo (about 16
-            // significant bits), so the weights of the PV product match the fp32
-            // sum l even when a few keys carry the whole softmax.  Several row
-            // tiles (the gamma-query verify, where the contraction is the limit):
-            // P as one bf16 term and l summed from those same rounded weights, so
-            // the output is an exactly normalised average with weights within
-            // 2^-9 relative of the fp32 ones.
+#pragma unroll
+            for (int nt = 0; nt < 2 * NSUB; ++nt) {
+                sacc[nt][2 * i] = fast_exp2(sacc[nt][2 * i] - muse);
+                sacc[nt][2 * i + 1] = fast_exp2(sacc[nt][2 * i + 1] - muse);
+                if constexpr (!kTwoTermP) {
+                    // the weights the PV product will use, rounded once to bf16
+                    sacc[nt][2 * i] = __bfloat162float(__float2bfloat16_rn(sacc[nt][2 * i]));
+                    sacc[nt][2 * i + 1] = __bfloat162float(__float2bfloat16_rn(sacc[nt][2 * i + 1]));
+                }
+                l_r[i] += sacc[nt][2 * i] + sacc[nt][2 * i + 1];
+            }
+        }
+        // One row tile (decode): P as two bf16 terms, p = hi + lo (about 16
+        // significant bits), so the weights of the PV product match the fp32
+        // sum l even when a few keys carry the whole softmax.  Several row
+        // tiles (the gamma-query verify, where the contraction is the limit):
+        // P as one bf16 term and l summed from those same rounded weights, so
+        // the output is an exactly normalised average with weights within
+        // 2^-9 relative of the fp32 ones.
+#pragma unroll
+        for (int sub = 0; sub < NSUB; ++sub) {
+            const float(&x0)[4] = sacc[2 * sub];
+            const float(&x1)[4] = sacc[2 * sub + 1];
             uint32_t pa[4], pl[4];
             if constexpr (kTwoTermP) {
-                split_bf16(x[0][0], x[0][1], pa[0], pl[0]);
-                split_bf16(x[0][2], x[0][3], pa[1], pl[1]);
-                split_bf16(x[1][0], x[1][1], pa[2], pl[2]);
-                split_bf16(x[1][2], x[1][3], pa[3], pl[3]);
+                split_bf16(x0[0], x0[1], pa[0], pl[0]);
+                split_bf16(x0[2], x0[3], pa[1], pl[1]);
+                split_bf16(x1[0], x1[1], pa[2], pl[2]);
+                split_bf16(x1[2], x1[3], pa[3], pl[3]);
             } else {
-                pa[0] = pack_bf16(x[0][0], x[0][1]);
-                pa[1] = pack_bf16(x[0][2], x[0][3]);
-                pa[2] = pack_bf16(x[1][0], x[1][1]);
-                pa[3] = pack_bf16(x[1][2], x[1][3]);
+                pa[0] = pack_bf16(x0[0], x0[1]);
+                pa[1] = pack_bf16(x0[2], x0[3]);
+                pa[2] = pack_bf16(x1[0], x1[1]);
+                pa[3] = pack_bf16(x1[2], x1[3]);
             }
+            const int krow0 = kw * C::KPW + sub * 16;
 #pragma unroll
             for (int jj = 0; jj < D / 16; ++jj) {
                 uint32_t vb[4];
