@@ -931,11 +931,12 @@ struct WsLayout {
     size_t bytes;
 };
 
-WsLayout attn_ws_layout(void* ws, int BH, int R, int d, int max_chunks) {
+// ml_floats: floats of a partial row's softmax record ((m, l), or wider)
+WsLayout attn_ws_layout(void* ws, int BH, int R, int d, int max_chunks, int ml_floats = 2) {
     const size_t off_tickets = kWsHeader;
     const size_t off_po = align256(off_tickets + attn_ticket_bytes(BH));
     const size_t off_pml = align256(off_po + sizeof(float) * static_cast<size_t>(max_chunks) * R * d);
-    const size_t end = align256(off_pml + sizeof(float) * static_cast<size_t>(max_chunks) * R * 2);
+    const size_t end = align256(off_pml + sizeof(float) * static_cast<size_t>(max_chunks) * R * ml_floats);
     WsLayout L{};
     L.bytes = end;
     if (ws) {
@@ -1093,11 +1094,17 @@ AttnParams make_params(const AttnLaunch& a) {
 
 }  // namespace
 
+AttnWs attn_ws(void* ws, int BH, int R, int d, int max_chunks, int ml_floats) {
+    const WsLayout L = attn_ws_layout(ws, BH, R, d, max_chunks, ml_floats);
+    return AttnWs{L.status, L.tickets, L.part_o, L.part_ml, L.bytes};
+}
+
 size_t dense_ws_bytes(int B, int Hq, int Hkv, int d, int n_total, int gamma, int num_sms) {
     const int BH = B * Hkv;
     const DensePlan pl = dense_plan(BH, n_total, num_sms);
     const int R = (Hq / Hkv) * gamma;
-    return attn_ws_layout(nullptr, BH, R, d, BH * pl.nsplit).bytes;
+    const size_t tc = verify_tc_ws_bytes(B, Hq, Hkv, d, n_total, gamma, num_sms);
+    return std::max(attn_ws_layout(nullptr, BH, R, d, BH * pl.nsplit).bytes, tc);
 }
 
 size_t sparse_ws_bytes(int B, int Hq, int Hkv, int d, int num_sms) {
@@ -1108,6 +1115,9 @@ size_t sparse_ws_bytes(int B, int Hq, int Hkv, int d, int num_sms) {
 
 int launch_dense_verify(const AttnLaunch& a, const CUtensorMap* tmk, const CUtensorMap* tmv, int num_sms,
                         const char** why) {
+    // more than 16 query rows per KV head at d = 128: the tensor-core verify
+    if (verify_tc_ws_bytes(a.B, a.Hq, a.Hkv, a.d, a.n_prefix + a.gamma, a.gamma, num_sms) > 0)
+        return launch_verify_tc(a, tmk, tmv, num_sms, why);
     AttnParams p = make_params(a);
     const int BH = a.B * a.Hkv;
     p.n_prefix = a.n_prefix;

@@ -41,7 +41,22 @@ struct AttnLaunch {
     size_t ws_bytes;
     cudaStream_t stream;
 };
+// Workspace of the split-K kernels: status word, per-head tickets (BH x 8), and
+// partials o fp32 [max_chunks][R][d] and softmax records [max_chunks][R][ml_floats].
+struct AttnWs {
+    int* status;
+    int* tickets;
+    float* part_o;
+    float* part_ml;
+    size_t bytes;
+};
+AttnWs attn_ws(void* ws, int BH, int R, int d, int max_chunks, int ml_floats);
 size_t dense_ws_bytes(int B, int Hq, int Hkv, int d, int n_total, int gamma, int num_sms);
+// gamma-query verify on tcgen05 (verify_tc.cu): d = 128, 16 < (Hq/Hkv) * gamma <= 64.
+// verify_tc_ws_bytes is its workspace size, 0 for shapes it does not take.
+size_t verify_tc_ws_bytes(int B, int Hq, int Hkv, int d, int n_total, int gamma, int num_sms);
+int launch_verify_tc(const AttnLaunch& a, const CUtensorMap* tmk, const CUtensorMap* tmv, int num_sms,
+                     const char** why);
 size_t sparse_ws_bytes(int B, int Hq, int Hkv, int d, int num_sms);
 int launch_dense_verify(const AttnLaunch& a, const CUtensorMap* tmk, const CUtensorMap* tmv,
                         int num_sms, const char** why);

@@ -47,6 +47,9 @@ def _status_ok(ws):
     (1, 32, 8, 128, 5000, 8),     # 32 rows per KV head (two row tiles)
     (1, 28, 4, 128, 2000, 5),     # video shape: 35 rows (three row tiles)
     (1, 4, 1, 128, 700, 16),      # 64 rows (four row tiles)
+    (1, 64, 32, 128, 3000, 9),    # 18 rows, clusters of two
+    (8, 32, 8, 128, 600, 5),      # 20 rows, several chunks a head, no cluster
+    (2, 8, 2, 128, 40, 5),        # 20 rows, one chunk a head
     (3, 6, 3, 64, 77, 3),         # short cache, fewer keys than a tile per split
     (1, 2, 2, 128, 0, 1),         # a single key
 ])
@@ -62,6 +65,27 @@ def test_dense_verify_matches_oracle(B, Hq, Hkv, d, n_prefix, gamma):
     assert_attn_close(o, o_ref, "dense")
     assert_lse_close(lse, l_ref, "dense")
     _status_ok(ws)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,n_prefix,gamma", [(1, 32, 8, 6000, 8), (40, 32, 8, 300, 5), (40, 28, 4, 300, 5)])
+def test_dense_verify_rising_scores(B, Hq, Hkv, n_prefix, gamma):
+    # keys whose norm grows along the cache: a row's running max rises by many
+    # binades inside a chunk, so the output accumulated so far must be rescaled.
+    # Such rows put nearly all weight on one or two keys, so an output is about
+    # one value row; values are scaled to stay below 2, where rounding the bf16
+    # output costs at most 2^-8 (a randn row can reach 4, where it costs 2^-7,
+    # past the 1e-2 bound whatever the kernel does).
+    g = torch.Generator().manual_seed(77 + B)
+    d = 128
+    rows = n_prefix + gamma
+    ramp = torch.linspace(0.2, 6.0, rows, dtype=torch.float64).view(1, 1, rows, 1)
+    k = (_rand((B, Hkv, rows, d), g).double() * ramp).to(torch.bfloat16)
+    v = _rand((B, Hkv, rows, d), g, 0.4)
+    q = _rand((B, Hq, gamma, d), g, 1.5)
+    o, lse = sk.dense_verify_attn(q.to(DEV), k.to(DEV), v.to(DEV), n_prefix, scale_of(d))
+    o_ref, l_ref = oracle.dense_verify(q, k, v, n_prefix)
+    assert_attn_close(o, o_ref, "dense")
+    assert_lse_close(lse, l_ref, "dense")
 
 
 def test_dense_verify_strided_cache_and_repeat_calls():
