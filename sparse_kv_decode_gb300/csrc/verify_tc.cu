@@ -1,18 +1,20 @@
 // Multi-query verify on the 5th-generation tensor cores (StD 3.1: the dense
 // model checks all gamma drafted positions in one pass over the full cache;
 // ByteCross "The Attention Baseline": split-K dense attention), for KV heads
-// with 17..32 query rows (R = G * gamma) at d = 128, where the warp-level
+// with 17..64 query rows (R = G * gamma) at d = 128, where the warp-level
 // mma.sync path of attn_splitk.cu waits on the latency of its chained MMAs.
 //
 // The products run transposed, so that the 128 rows of each MMA are keys or
 // head dims and never padding (a tcgen05.mma costs at least ~48 cycles
 // whatever its N, so the work per key is what the row count M buys):
-//   S^T = K Q^T    M = 128 keys of the tile, N = 32 query rows, K = 128 dims.
+//   S^T = K Q^T    M = 128 keys of the tile, N = 32 * NG query rows (NG = 1 or
+//                  2 groups of 32), K = 128 dims.
 //                  A = the K tile, B = the query rows, both K-major with
 //                  128-byte swizzle as TMA writes them; S^T in tensor memory
 //                  (lane = key), two buffers.
-//   softmax        four warps, one thread per key (its tensor-memory lane),
-//                  holding that key's 32 scores.  Every row r has one
+//   softmax        4 * NG warps, one thread per (key, row group): a warp reads
+//                  its own quarter of the tensor-memory lanes (keys) and, for
+//                  its group, 32 scores per key.  Every row r has one
 //                  reference m_r, the same in all threads; a weight is
 //                  2^(scale*log2e*s - m_r), rounded to bf16 into P^T.  The
 //                  threads vote once per tile (a named barrier with an OR)
@@ -26,15 +28,15 @@
 //                  the log-sum-exp; the sums are reduced over the threads at
 //                  the end.  Causal mask: query t of a row sees keys <=
 //                  n_prefix + t; interior tiles skip it.
-//   O^T += V^T P^T M = 128 head dims, N = 64 (the 32 rows padded to a
-//                  128-byte swizzle row of P^T), K = 128 keys.  A = the V tile
+//   O^T += V^T P^T M = 128 head dims, N = 64 (the rows, padded to a 128-byte
+//                  swizzle row of P^T), K = 128 keys.  A = the V tile
 //                  as TMA wrote it ([keys][dims]: MN-major), B = P^T
 //                  ([keys][rows]: MN-major), both 128-byte swizzle.
-// Warps 0 and 6 issue the TMA copies of the K and V tiles, each in stages of
-// their own (a K stage frees as soon as its score is done, so K copies run
-// well ahead of the scores); one thread of warp 1 the MMAs,
+// Warp 0 and the last warp issue the TMA copies of the K and V tiles, each in
+// stages of their own (a K stage frees as soon as its score is done, so K
+// copies run well ahead of the scores); one thread of warp 1 the MMAs,
 // the score of tile t before the PV product of tile t - 1 so that the softmax
-// of a tile overlaps the next score; warps 2..5 the softmax.  A CTA takes one
+// of a tile overlaps the next score; warps 2 .. 1 + 4 * NG the softmax.  A CTA takes one
 // (sequence, KV head) and one chunk of its keys; the chunks of a head form
 // clusters of up to 8 CTAs (one CTA per SM, all in one wave) whose partials (o, m, l, l_exact)
 // merge through distributed shared memory, and the last cluster of a head
@@ -51,47 +53,54 @@ namespace {
 
 constexpr int kVD = 128;            // head dim
 constexpr int kVTK = 128;           // keys per tile: M of the score product
-constexpr int kVNQ = 32;            // query rows: N of the score product
+constexpr int kVNQ = 32;            // query rows of a row group (a softmax thread's rows)
 constexpr int kVNP = 64;            // N of the PV product: a P^T row is 64 bf16
 constexpr int kVRmin = 17;          // fewer rows go to the mma.sync path
+constexpr int kVRmax = 64;          // two row groups
 constexpr int kVKSt = 3;            // K stages: free once their score is done
 constexpr int kVVSt = 2;            // V stages: held until their PV product is done
 constexpr int kVMaxCluster = 8;
-constexpr int kVNT = 224;           // warp 0 K and query copies, warp 1 MMA, warps 2..5 softmax, warp 6 V copies
 constexpr int kVBar = 1;            // named barrier of the softmax warps
 constexpr float kVRescale = 8.f;    // growth past a row's reference (log2 units) that raises it
 
+template <int NG>
 struct VCfg {
-    static constexpr int Q_B = 2 * kVNQ * 128;               // two 64-dim halves of 32 rows
+    static constexpr int NQ = kVNQ * NG;                     // query rows: N of the score product
+    static constexpr int NT = 32 * (3 + 4 * NG);             // warp 0 K copies, 1 MMA, 4*NG softmax, last V copies
+    static constexpr int VWARP = 2 + 4 * NG;
+    static constexpr int NSOFT = 128 * NG;                   // softmax threads
+    static constexpr int Q_B = 2 * NQ * 128;                 // two 64-dim halves of NQ rows
     static constexpr int T_B = 2 * kVTK * 128;               // a K or V tile: two halves of 128 keys
     static constexpr int P_B = kVTK * 128;                   // P^T: 128 keys x 64 bf16
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + Q_B;
     static constexpr int OFF_V = OFF_K + kVKSt * T_B;
     static constexpr int OFF_P = OFF_V + kVVSt * T_B;
-    static constexpr int OFF_RED = OFF_P + 2 * P_B;          // [4 warps][32 rows] tile maxima
-    static constexpr int OFF_BAR = OFF_RED + 4 * kVNQ * 4;
+    static constexpr int OFF_RED = OFF_P + 2 * P_B;          // [group][4 warps][32 rows] tile maxima
+    static constexpr int OFF_M = OFF_RED + NG * 4 * kVNQ * 4;  // [2][NQ] row references (double-buffered)
+    static constexpr int OFF_BAR = OFF_M + 2 * NQ * 4;
     static constexpr int NBAR = 2 * kVKSt + 2 * kVVSt + 1 + 2 + 2 + 2 + 1 + 1;
     static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_TMEM + 16;
     static constexpr int SMEM_ALLOC = SMEM + 1024;
-    // after the loop the K and V stages hold: the threads' sums [2][128][33],
-    // the output rows o [32][128], the rows' records (m, l, l_exact, -) [32],
+    // after the loop the K and V stages hold: the threads' sums [2][128][NQ+1],
+    // the output rows o [NQ][128], the rows' records (m, l, l_exact, -) [NQ],
     // and what the cluster's CTAs push: o slices [cs][R][128/cs] and records [8][R]
-    static constexpr int LR_LD = kVNQ + 1;
+    static constexpr int LR_LD = NQ + 1;
     static constexpr int OFF_LR = OFF_K;
     static constexpr int OFF_CMB = OFF_LR + 2 * kVTK * LR_LD * 4;
-    static constexpr int OFF_SUM = OFF_CMB + kVNQ * kVD * 4;
-    static constexpr int OFF_RCV = OFF_SUM + kVNQ * 16;
-    static constexpr int OFF_RML = OFF_RCV + kVNQ * kVD * 4;
-    static constexpr int END_MERGE = OFF_RML + kVMaxCluster * kVNQ * 16;
-    static constexpr uint32_t TMEM_COLS = 128;                // S^T: two buffers of 32 columns; O^T: 64
-    static constexpr uint32_t COL_O = 64;
-    static constexpr uint32_t IDESC_S = idesc_bf16_f32(kVTK, kVNQ);
+    static constexpr int OFF_SUM = OFF_CMB + NQ * kVD * 4;
+    static constexpr int OFF_RCV = OFF_SUM + NQ * 16;
+    static constexpr int OFF_RML = OFF_RCV + NQ * kVD * 4;
+    static constexpr int END_MERGE = OFF_RML + kVMaxCluster * NQ * 16;
+    static constexpr uint32_t TMEM_COLS = NG == 1 ? 128 : 256;   // S^T: two buffers of NQ columns; O^T: 64
+    static constexpr uint32_t COL_O = 2 * NQ;
+    static constexpr uint32_t IDESC_S = idesc_bf16_f32(kVTK, NQ);
     static constexpr uint32_t IDESC_PV = idesc_bf16_f32_amn_bmn(kVD, kVNP);
     static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory of one CTA");
     static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && OFF_P % 1024 == 0, "128-byte swizzle atoms");
     static_assert(END_MERGE <= OFF_P, "the merge buffers fit the K and V stages");
+    static_assert(COL_O + kVNP <= TMEM_COLS, "tensor-memory columns");
 };
 
 struct VParams {
@@ -120,10 +129,12 @@ __device__ __forceinline__ void halve_max(float (&x)[kVNQ], int lane) {
     }
 }
 
-__global__ void __launch_bounds__(kVNT, 1)
+template <int NG>
+__global__ void __launch_bounds__(VCfg<NG>::NT, 1)
     verify_tc_kernel(const __grid_constant__ VParams p, const __grid_constant__ CUtensorMap tmq,
                      const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
-    using C = VCfg;
+    using C = VCfg<NG>;
+    constexpr int NQ = C::NQ;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem =
         reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -141,6 +152,7 @@ __global__ void __launch_bounds__(kVNT, 1)
     const uint32_t bar_od = bar_pv + 8;                      // every product issued is done (one phase)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM);
     float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
+    float* mref = reinterpret_cast<float*>(smem + C::OFF_M);
     __shared__ int s_abort;
     __shared__ int s_last;
     __shared__ int s_issued_k, s_issued_v;   // K and V tiles whose copies were issued
@@ -181,8 +193,8 @@ __global__ void __launch_bounds__(kVNT, 1)
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_sf + 8 * i, 1);
-            mbar_init(bar_se + 8 * i, 4);
-            mbar_init(bar_pf + 8 * i, 4);
+            mbar_init(bar_se + 8 * i, 4 * NG);
+            mbar_init(bar_pf + 8 * i, 4 * NG);
         }
         mbar_init(bar_pv, 1);
         mbar_init(bar_od, 1);
@@ -191,6 +203,9 @@ __global__ void __launch_bounds__(kVNT, 1)
         s_issued_k = 0;
         s_issued_v = 0;
     }
+    // row references, the same for every thread of a row group: rows past R
+    // start at +inf, so that their weights are 0 and they never raise a vote
+    for (int i = tid; i < NQ; i += C::NT) mref[i] = i < p.R ? -INFINITY : INFINITY;
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
         tmem_relinquish();
@@ -202,20 +217,20 @@ __global__ void __launch_bounds__(kVNT, 1)
     griddep_wait();
     volatile int* abort_flag = &s_abort;
 
-    // softmax threads (warps 2..5): tensor-memory lane L = key L of a tile, and
-    // (for O^T) head dim L
+    // softmax threads (warps 2 .. 1 + 4*NG): tensor-memory lane L = key L of a
+    // tile and (for O^T) head dim L; row group g2 = rows rb .. rb + 31
     const int q4 = warp & 3;
     const int L = 32 * q4 + lane;
+    const int g2 = (warp - 2) >> 2, rb = kVNQ * ((warp - 2) >> 2);
     const uint32_t tlane = tmem + (static_cast<uint32_t>(32 * q4) << 16);
-    // per row r: reference m[r] (rows past R: +inf, so that their weights are 0
-    // and they never raise a vote), and this thread's sums
-    float m[kVNQ], l[kVNQ], le[kVNQ];
+    // this thread's sums of rows rb + r; the references are mref[mb * NQ + rb + r]
+    float l[kVNQ], le[kVNQ];
 #pragma unroll
     for (int r = 0; r < kVNQ; ++r) {
-        m[r] = r < p.R ? -INFINITY : INFINITY;
         l[r] = 0.f;
         le[r] = 0.f;
     }
+    int mb = 0;
     bool aborted = false;
 
     if (warp == 0) {
@@ -225,7 +240,7 @@ __global__ void __launch_bounds__(kVNT, 1)
             mbar_arrive_expect_tx(bar_q, C::Q_B);
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf)
-                tma_load_2d(sbase + C::OFF_Q + hf * (kVNQ * 128), &tmq, hf * 64, qrow0, bar_q);
+                tma_load_2d(sbase + C::OFF_Q + hf * (NQ * 128), &tmq, hf * 64, qrow0, bar_q);
             int nk = 0;
             bool ok = true;
             for (int t = 0; t < ntiles; ++t) {
@@ -247,7 +262,7 @@ __global__ void __launch_bounds__(kVNT, 1)
             }
             s_issued_k = nk;
         }
-    } else if (warp == 6) {
+    } else if (warp == C::VWARP) {
         // ------------------------------------------------------------ V producer
         // V tile t once its stage's previous PV product is done
         if (lane == 0 && ntiles > 0) {
@@ -302,9 +317,9 @@ __global__ void __launch_bounds__(kVNT, 1)
                     const uint64_t kds = kd0 + static_cast<uint64_t>((s * C::T_B) >> 4);
 #pragma unroll
                     for (int ks = 0; ks < kVD / 16; ++ks)
-                        tc_mma_bf16(tmem + sb * kVNQ,
+                        tc_mma_bf16(tmem + sb * NQ,
                                     kds + static_cast<uint64_t>(((ks >> 2) * (kVTK * 128) + (ks & 3) * 32) >> 4),
-                                    qd0 + static_cast<uint64_t>(((ks >> 2) * (kVNQ * 128) + (ks & 3) * 32) >> 4),
+                                    qd0 + static_cast<uint64_t>(((ks >> 2) * (NQ * 128) + (ks & 3) * 32) >> 4),
                                     C::IDESC_S, ks > 0);
                     tc_commit(bar_ke + 8 * s);    // the K stage is free once the score is done
                     tc_commit(bar_sf + 8 * sb);
@@ -336,10 +351,10 @@ __global__ void __launch_bounds__(kVNT, 1)
             }
         }
     } else {
-        // ------------------------------------------------------------ softmax (warps 2..5), one thread per key
+        // ------------------------------------------------------------ softmax, one thread per (key, row group)
         const float c = p.scale_log2;
         uint8_t* prow0 = smem + C::OFF_P + L * 128;
-        // P^T rows start at zero: columns 32..63 (padding rows) are never written
+        // P^T rows start at zero: the columns of padding rows are never written
 #pragma unroll
         for (int pb = 0; pb < 2; ++pb)
 #pragma unroll
@@ -354,7 +369,7 @@ __global__ void __launch_bounds__(kVNT, 1)
             for (int r = 0; r < kVNQ; ++r) v[r] = 0u;
             if (__all_sync(0xffffffffu, got)) {
                 tc_fence_after();
-                tmem_ld32_sync(tlane + sb * kVNQ, v);
+                tmem_ld32_sync(tlane + sb * NQ + rb, v);
             }
             tc_fence_before();
             __syncwarp();
@@ -370,19 +385,20 @@ __global__ void __launch_bounds__(kVNT, 1)
                 const int over = key - p.n_prefix;   // visible to row r iff key < hi and over <= r % gamma
                 vis = 0u;
 #pragma unroll
-                for (int r = 0; r < kVNQ; ++r) vis |= (key < hi && over <= r % p.gamma) ? (1u << r) : 0u;
+                for (int r = 0; r < kVNQ; ++r) vis |= (key < hi && over <= (rb + r) % p.gamma) ? (1u << r) : 0u;
             }
+            const float* mc = mref + mb * NQ + rb;   // this group's references (shared-memory broadcast)
             // the largest visible score relative to its row's reference (a tree of maxima)
             float g[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) g[i] = -INFINITY;
 #pragma unroll
             for (int r = 0; r < kVNQ; ++r)
-                g[r & 7] = fmaxf(g[r & 7], (vis >> r) & 1u ? fmaf(__uint_as_float(v[r]), c, -m[r]) : -INFINITY);
+                g[r & 7] = fmaxf(g[r & 7], (vis >> r) & 1u ? fmaf(__uint_as_float(v[r]), c, -mc[r]) : -INFINITY);
             const bool viol = fmaxf(fmaxf(fmaxf(g[0], g[1]), fmaxf(g[2], g[3])), fmaxf(fmaxf(g[4], g[5]), fmaxf(g[6], g[7]))) >
                               kVRescale;
             // one vote per tile; a thread whose wait gave up set the abort flag before it
-            const bool any = named_bar_or(kVBar, 128, viol);
+            const bool any = named_bar_or(kVBar, C::NSOFT, viol);
             if (*abort_flag) {
                 aborted = true;
                 break;
@@ -402,16 +418,17 @@ __global__ void __launch_bounds__(kVNT, 1)
                     halve_max<2>(x, lane);
                     halve_max<1>(x, lane);
                     // lane i now holds the warp's maximum of row i (in x[0])
-                    red[q4 * kVNQ + lane] = x[0];
+                    red[(4 * g2 + q4) * kVNQ + lane] = x[0];
                 }
-                named_bar_sync(kVBar, 128);
+                named_bar_sync(kVBar, C::NSOFT);
                 // the same decisions in every thread: whether some row with a finite
                 // reference grows (then what is accumulated must be rescaled)
+                const float* rg = red + 4 * kVNQ * g2;   // this group's four warps' maxima
                 bool rescale_o = false;
 #pragma unroll
                 for (int r = 0; r < kVNQ; ++r) {
-                    const float tm = fmaxf(fmaxf(red[r], red[kVNQ + r]), fmaxf(red[2 * kVNQ + r], red[3 * kVNQ + r]));
-                    rescale_o |= tm > m[r] + kVRescale && m[r] != -INFINITY;
+                    const float tm = fmaxf(fmaxf(rg[r], rg[kVNQ + r]), fmaxf(rg[2 * kVNQ + r], rg[3 * kVNQ + r]));
+                    rescale_o |= tm > mc[r] + kVRescale && mc[r] != -INFINITY;
                 }
                 if (rescale_o && t >= 1) {
                     // S(t) was issued after every PV product but PV(t - 1): wait for that
@@ -423,47 +440,56 @@ __global__ void __launch_bounds__(kVNT, 1)
 #pragma unroll
                         for (int hh = 0; hh < 2; ++hh) {
                             uint32_t ov[16];
-                            tmem_ld16_sync(tlane + C::COL_O + 16 * hh, ov);
+                            tmem_ld16_sync(tlane + C::COL_O + rb + 16 * hh, ov);
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
                                 const int r = 16 * hh + i;
-                                const float tm = fmaxf(fmaxf(red[r], red[kVNQ + r]), fmaxf(red[2 * kVNQ + r], red[3 * kVNQ + r]));
-                                if (tm > m[r] + kVRescale && m[r] != -INFINITY)
-                                    ov[i] = __float_as_uint(__uint_as_float(ov[i]) * fast_exp2(m[r] - tm));
+                                const float tm = fmaxf(fmaxf(rg[r], rg[kVNQ + r]), fmaxf(rg[2 * kVNQ + r], rg[3 * kVNQ + r]));
+                                if (tm > mc[r] + kVRescale && mc[r] != -INFINITY)
+                                    ov[i] = __float_as_uint(__uint_as_float(ov[i]) * fast_exp2(mc[r] - tm));
                             }
-                            tmem_st16_sync(tlane + C::COL_O + 16 * hh, ov);
+                            tmem_st16_sync(tlane + C::COL_O + rb + 16 * hh, ov);
                         }
                     }
                 }
+                // new references into the other buffer (one thread per group writes
+                // them; every thread reads the old ones until the barrier below)
+                float* mn = mref + (mb ^ 1) * NQ + rb;
 #pragma unroll
                 for (int r = 0; r < kVNQ; ++r) {
-                    const float tm = fmaxf(fmaxf(red[r], red[kVNQ + r]), fmaxf(red[2 * kVNQ + r], red[3 * kVNQ + r]));
-                    if (tm > m[r] + kVRescale) {   // m = -inf: the row's first visible keys
-                        const float f = m[r] != -INFINITY ? fast_exp2(m[r] - tm) : 1.f;
-                        m[r] = tm;
+                    const float tm = fmaxf(fmaxf(rg[r], rg[kVNQ + r]), fmaxf(rg[2 * kVNQ + r], rg[3 * kVNQ + r]));
+                    const float mo = mc[r];
+                    float mnew = mo;
+                    if (tm > mo + kVRescale) {   // mo = -inf: the row's first visible keys
+                        const float f = mo != -INFINITY ? fast_exp2(mo - tm) : 1.f;
+                        mnew = tm;
                         l[r] *= f;
                         le[r] *= f;
                     }
+                    if (L == 0) mn[r] = mnew;
                 }
-                // the maxima are read; the next tile's writes wait for this barrier, and
-                // a timeout above stops every thread here together
-                named_bar_sync(kVBar, 128);
+                // the maxima and the old references are read, the new ones written; the
+                // next tile's maxima wait for this barrier, and a timeout above stops
+                // every thread here together
+                named_bar_sync(kVBar, C::NSOFT);
+                mb ^= 1;
                 if (*abort_flag) {
                     aborted = true;
                     break;
                 }
             }
             // weights rounded to bf16 as the PV product uses them; l sums the same
-            // values, le the unrounded ones; P^T row `L` of buffer t & 1, columns 0..31
+            // values, le the unrounded ones; P^T row `L` of buffer t & 1, columns rb .. rb + 31
             uint8_t* prow = prow0 + (t & 1) * C::P_B;
+            const float* mw = mref + mb * NQ + rb;
 #pragma unroll
-            for (int k = 0; k < kVNQ / 8; ++k) {   // 16-byte chunk k: rows 8k..8k+7
+            for (int k = 0; k < kVNQ / 8; ++k) {   // 16-byte chunk 4*g2 + k: rows rb + 8k .. rb + 8k + 7
                 uint32_t pk[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int r = 8 * k + 2 * i;
-                    const float x0 = (vis >> r) & 1u ? fast_exp2(fmaf(__uint_as_float(v[r]), c, -m[r])) : 0.f;
-                    const float x1 = (vis >> (r + 1)) & 1u ? fast_exp2(fmaf(__uint_as_float(v[r + 1]), c, -m[r + 1])) : 0.f;
+                    const float x0 = (vis >> r) & 1u ? fast_exp2(fmaf(__uint_as_float(v[r]), c, -mw[r])) : 0.f;
+                    const float x1 = (vis >> (r + 1)) & 1u ? fast_exp2(fmaf(__uint_as_float(v[r + 1]), c, -mw[r + 1])) : 0.f;
                     le[r] += x0;
                     le[r + 1] += x1;
                     const __nv_bfloat162 w2 = __floats2bfloat162_rn(x0, x1);
@@ -472,7 +498,7 @@ __global__ void __launch_bounds__(kVNT, 1)
                     l[r + 1] += wf.y;
                     pk[i] = *reinterpret_cast<const uint32_t*>(&w2);
                 }
-                *reinterpret_cast<uint4*>(prow + ((k ^ (L & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                *reinterpret_cast<uint4*>(prow + (((4 * g2 + k) ^ (L & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
             tc_fence_before();           // the rescale's tensor-memory stores, then
             fence_proxy_async_smem();    // the weights, visible to the tensor cores
@@ -495,26 +521,26 @@ __global__ void __launch_bounds__(kVNT, 1)
     float* lr = reinterpret_cast<float*>(smem + C::OFF_LR);
     float* cmb = reinterpret_cast<float*>(smem + C::OFF_CMB);
     float4* sum = reinterpret_cast<float4*>(smem + C::OFF_SUM);
-    if (!stop && warp >= 2 && warp <= 5) {
+    if (!stop && warp >= 2 && warp < C::VWARP) {
         // into the K and V stages, which nothing uses any more (every product is
         // done, and each waited for the copy it read): this thread's sums, and its
         // head dim of every output row (O^T lane L), relative to the references
         uint32_t ov[kVNQ];
         if (ntiles > 0) {
-            tmem_ld32_sync(tlane + C::COL_O, ov);
+            tmem_ld32_sync(tlane + C::COL_O + rb, ov);
         } else {
 #pragma unroll
             for (int r = 0; r < kVNQ; ++r) ov[r] = 0u;
         }
 #pragma unroll
         for (int r = 0; r < kVNQ; ++r) {
-            cmb[r * kVD + L] = __uint_as_float(ov[r]);
-            lr[L * C::LR_LD + r] = l[r];
-            lr[(kVTK + L) * C::LR_LD + r] = le[r];
+            cmb[(rb + r) * kVD + L] = __uint_as_float(ov[r]);
+            lr[L * C::LR_LD + rb + r] = l[r];
+            lr[(kVTK + L) * C::LR_LD + rb + r] = le[r];
         }
-        if (L == 0) {   // the references are the same in every thread
+        if (L == 0) {   // the references are the same in every thread of the group
 #pragma unroll
-            for (int r = 0; r < kVNQ; ++r) sum[r].x = m[r];
+            for (int r = 0; r < kVNQ; ++r) sum[rb + r].x = mref[mb * NQ + rb + r];
         }
     }
     // after a timeout, the products issued so far must finish before their
@@ -547,15 +573,27 @@ __global__ void __launch_bounds__(kVNT, 1)
         }
         return;
     }
-    // each row's sums over the 128 threads
-    if (tid < p.R) {
+    // each row's sums over the 128 keys' threads: 8 lanes per row, 16 keys each,
+    // then a reduction over the 8 lanes (rows of a warp: 4; all lanes take part)
+    for (int rr0 = 4 * warp; rr0 < p.R; rr0 += 4 * (C::NT / 32)) {
+        const int rr = rr0 + (lane >> 3), part = lane & 7;
         float a = 0.f, e = 0.f;
-        for (int i = 0; i < kVTK; ++i) {
-            a += lr[i * C::LR_LD + tid];
-            e += lr[(kVTK + i) * C::LR_LD + tid];
+        if (rr < p.R) {
+#pragma unroll 4
+            for (int i = part; i < kVTK; i += 8) {
+                a += lr[i * C::LR_LD + rr];
+                e += lr[(kVTK + i) * C::LR_LD + rr];
+            }
         }
-        sum[tid].y = a;
-        sum[tid].z = e;
+#pragma unroll
+        for (int o = 4; o >= 1; o >>= 1) {
+            a += __shfl_xor_sync(0xffffffffu, a, o);
+            e += __shfl_xor_sync(0xffffffffu, e, o);
+        }
+        if (rr < p.R && part == 0) {
+            sum[rr].y = a;
+            sum[rr].z = e;
+        }
     }
     __syncthreads();
 
@@ -567,7 +605,7 @@ __global__ void __launch_bounds__(kVNT, 1)
     const int SL = kVD >> lcs;                       // head dims a cluster rank owns
     const uint32_t me = p.cs > 1 ? cluster_ctarank() : 0u;
     if (p.cs > 1) cluster_sync_all();
-    for (int e = tid; e < p.R * (kVD / 4); e += kVNT) {
+    for (int e = tid; e < p.R * (kVD / 4); e += C::NT) {
         const int rr = e >> 5, d0 = 4 * (e & 31);
         const float4 a4 = *reinterpret_cast<const float4*>(cmb + rr * kVD + d0);
         const float4 rec = sum[rr];
@@ -605,7 +643,7 @@ __global__ void __launch_bounds__(kVNT, 1)
         const int gcl = cidx >> lcs, gcl0 = c0 >> lcs, ncl_h = nch >> lcs;
         const float* rcv = reinterpret_cast<const float*>(smem + C::OFF_RCV);
         const float4* rml = reinterpret_cast<const float4*>(smem + C::OFF_RML);
-        for (int e = tid; e < p.R * sl4; e += kVNT) {
+        for (int e = tid; e < p.R * sl4; e += C::NT) {
             const int rr = e >> lsl4;
             const int dd = 4 * (e & (sl4 - 1));
             const int d0 = static_cast<int>(rank) * SL + dd;
@@ -660,7 +698,7 @@ __global__ void __launch_bounds__(kVNT, 1)
         __syncthreads();
         if (!s_last) return;
         // the last cluster of the head, for its slice: merge the head's cluster partials
-        for (int e = tid; e < p.R * sl4; e += kVNT) {
+        for (int e = tid; e < p.R * sl4; e += C::NT) {
             const int rr = e >> lsl4;
             const int d0 = static_cast<int>(rank) * SL + 4 * (e & (sl4 - 1));
             float mm = -INFINITY, ll = 0.f, lle = 0.f;
@@ -714,7 +752,7 @@ __global__ void __launch_bounds__(kVNT, 1)
     __syncthreads();
     if (!s_last) return;
     // per (row, 4 dims): the head's nch partials, merged online from L2 in batches of 4
-    for (int e = tid; e < p.R * (kVD / 4); e += kVNT) {
+    for (int e = tid; e < p.R * (kVD / 4); e += C::NT) {
         const int rr = e / (kVD / 4), d0 = 4 * (e - rr * (kVD / 4));
         float mm = -INFINITY, ll = 0.f, lle = 0.f;
         float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -762,7 +800,9 @@ struct VPlan {
 
 // CTAs of this kernel the device holds at once when launched in clusters of cs
 // (occupancy query, cached per device and cluster size; one CTA per SM).
+template <int NG>
 int vtc_capacity(int dev, int num_sms, int cs) {
+    using C = VCfg<NG>;
     static std::atomic<int> cache[64][4];   // 0: not queried yet
     const int ci = cs >= 8 ? 3 : cs >= 4 ? 2 : cs >= 2 ? 1 : 0;
     const bool cached = dev >= 0 && dev < 64;
@@ -773,14 +813,14 @@ int vtc_capacity(int dev, int num_sms, int cs) {
     int cap = 0;
     if (cs <= 1) {
         int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_tc_kernel, kVNT, VCfg::SMEM_ALLOC) ==
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, verify_tc_kernel<NG>, C::NT, C::SMEM_ALLOC) ==
             cudaSuccess)
             cap = per_sm * num_sms;
     } else {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(cs * 16);
-        cfg.blockDim = dim3(kVNT);
-        cfg.dynamicSmemBytes = VCfg::SMEM_ALLOC;
+        cfg.blockDim = dim3(C::NT);
+        cfg.dynamicSmemBytes = C::SMEM_ALLOC;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = cs;
@@ -789,7 +829,7 @@ int vtc_capacity(int dev, int num_sms, int cs) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int ncl = 0;
-        if (cudaOccupancyMaxActiveClusters(&ncl, verify_tc_kernel, &cfg) == cudaSuccess) cap = ncl * cs;
+        if (cudaOccupancyMaxActiveClusters(&ncl, verify_tc_kernel<NG>, &cfg) == cudaSuccess) cap = ncl * cs;
     }
     if (cap <= 0) {
         cudaGetLastError();   // a failed query leaves no sticky error; plan without clusters
@@ -800,11 +840,12 @@ int vtc_capacity(int dev, int num_sms, int cs) {
 }
 
 // One wave of CTAs: for each cluster size, as many clusters per head (at most
-// 4; the last one merges the others' partials) as the device holds at once, and
+// 8; the last one merges the others' partials) as the device holds at once, and
 // the cluster size whose plan covers the most CTAs.  Without clusters the SMs
 // are shared among the heads, but the last CTA of a head then merges all its
-// chunks' partials from L2 alone, which takes longer than a cluster merge: a
-// cluster plan is kept while it covers at least 2/3 as many CTAs.
+// chunks' partials from L2 alone, which takes far longer than a cluster merge
+// (34 partials: about 20 us): a cluster plan is kept while it covers at least
+// half as many CTAs.
 // cap[i]: CTAs held at once in clusters of 1 << i.
 VPlan verify_plan(int BH, int n_total, const int cap[4]) {
     const int max_split = std::max(1, (n_total + kVTK - 1) / kVTK);
@@ -814,11 +855,11 @@ VPlan verify_plan(int BH, int n_total, const int cap[4]) {
     int best = 0;
     for (int i = 3; i >= 1; --i) {
         const int cs = 1 << i;
-        const int k = std::min(4, cap[i] / cs / BH);
+        const int k = std::min(8, cap[i] / cs / BH);
         const int nsplit = std::min(k * cs, (max_split / cs) * cs);
         if (nsplit < cs || BH * nsplit <= best) continue;
         best = BH * nsplit;
-        if (3 * best >= 2 * BH * std::min(std::max(1, cap[0] / BH), max_split)) {
+        if (2 * best >= BH * std::min(std::max(1, cap[0] / BH), max_split)) {
             pl.cs = cs;
             pl.nsplit = nsplit;
         }
@@ -833,16 +874,74 @@ VPlan verify_plan(int BH, int n_total, const int cap[4]) {
 
 size_t verify_tc_ws_bytes(int B, int Hq, int Hkv, int d, int n_total, int gamma, int num_sms) {
     const int R = (Hq / Hkv) * gamma;
-    if (d != kVD || R < kVRmin || R > kVNQ) return 0;
+    if (d != kVD || R < kVRmin || R > kVRmax) return 0;
     (void)n_total;
     // every plan has at most one CTA per SM, or one per head
     const int BH = B * Hkv;
     return attn_ws(nullptr, BH, R, d, std::max(num_sms, BH), 4).bytes;   // records (m, l, l_exact, -)
 }
 
+namespace {
+
+template <int NG>
+int launch_vtc(VParams& p, const AttnLaunch& a, const CUtensorMap* tmk, const CUtensorMap* tmv, int num_sms,
+               const char** why) {
+    using C = VCfg<NG>;
+    const int BH = a.B * a.Hkv;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    static std::atomic<unsigned long long> attr_set{0};
+    if (e == cudaSuccess && !attr_done(attr_set, dev)) {
+        e = cudaFuncSetAttribute(verify_tc_kernel<NG>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
+        if (e == cudaSuccess) attr_mark(attr_set, dev);
+    }
+    if (e != cudaSuccess) {
+        *why = cudaGetErrorString(e);
+        return SDKV_ERR_CUDA;
+    }
+    int cap[4];
+    for (int i = 0; i < 4; ++i) cap[i] = vtc_capacity<NG>(dev, num_sms, 1 << i);
+    const VPlan pl = verify_plan(BH, p.n_total, cap);
+    p.nsplit = pl.nsplit;
+    p.chunk = pl.chunk;
+    p.cs = pl.cs;
+    // the query rows as a [B * Hq * gamma][d] matrix, NQ rows per box from the
+    // head's first (rows past R are another head's or, past the matrix, zero)
+    CUtensorMap tmq;
+    const int rc = encode_rows_tmap(&tmq, a.q, static_cast<int64_t>(a.B) * a.Hq * a.gamma, a.d, C::NQ);
+    if (rc) {
+        *why = "could not encode the query tensor map";
+        return rc;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(BH * pl.nsplit);
+    cfg.blockDim = dim3(C::NT);
+    cfg.dynamicSmemBytes = C::SMEM_ALLOC;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (pl.cs > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = pl.cs;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
+    e = cudaLaunchKernelEx(&cfg, verify_tc_kernel<NG>, p, tmq, *tmk, *tmv);
+    if (e != cudaSuccess) {
+        *why = cudaGetErrorString(e);
+        return SDKV_ERR_CUDA;
+    }
+    return SDKV_OK;
+}
+
+}  // namespace
+
 int launch_verify_tc(const AttnLaunch& a, const CUtensorMap* tmk, const CUtensorMap* tmv, int num_sms,
                      const char** why) {
-    using C = VCfg;
     const int BH = a.B * a.Hkv;
     const int G = a.Hq / a.Hkv;
     VParams p{};
@@ -854,27 +953,10 @@ int launch_verify_tc(const AttnLaunch& a, const CUtensorMap* tmk, const CUtensor
     p.R = G * a.gamma;
     p.n_prefix = a.n_prefix;
     p.n_total = a.n_prefix + a.gamma;
-    if (a.d != kVD || p.R < kVRmin || p.R > kVNQ) {
-        *why = "the tensor-core verify needs d = 128 and 17 <= (Hq/Hkv) * gamma <= 32";
+    if (a.d != kVD || p.R < kVRmin || p.R > kVRmax) {
+        *why = "the tensor-core verify needs d = 128 and 17 <= (Hq/Hkv) * gamma <= 64";
         return SDKV_ERR_UNSUPPORTED;
     }
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    static std::atomic<unsigned long long> attr_set{0};
-    if (e == cudaSuccess && !attr_done(attr_set, dev)) {
-        e = cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
-        if (e == cudaSuccess) attr_mark(attr_set, dev);
-    }
-    if (e != cudaSuccess) {
-        *why = cudaGetErrorString(e);
-        return SDKV_ERR_CUDA;
-    }
-    int cap[4];
-    for (int i = 0; i < 4; ++i) cap[i] = vtc_capacity(dev, num_sms, 1 << i);
-    const VPlan pl = verify_plan(BH, p.n_total, cap);
-    p.nsplit = pl.nsplit;
-    p.chunk = pl.chunk;
-    p.cs = pl.cs;
     p.scale_log2 = a.scale * kLog2e;
     p.o = static_cast<bf16*>(a.o);
     p.lse = a.lse;
@@ -887,39 +969,7 @@ int launch_verify_tc(const AttnLaunch& a, const CUtensorMap* tmk, const CUtensor
     p.tickets = L.tickets;
     p.part_o = L.part_o;
     p.part_ml = L.part_ml;
-    // the query rows as a [B * Hq * gamma][d] matrix, 32 rows per box from the
-    // head's first (rows past R are another head's or, past the matrix, zero)
-    CUtensorMap tmq;
-    int rc = encode_rows_tmap(&tmq, a.q, static_cast<int64_t>(a.B) * a.Hq * a.gamma, a.d, kVNQ);
-    if (rc) {
-        *why = "could not encode the query tensor map";
-        return rc;
-    }
-    {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(BH * pl.nsplit);
-        cfg.blockDim = dim3(kVNT);
-        cfg.dynamicSmemBytes = C::SMEM_ALLOC;
-        cfg.stream = a.stream;
-        cudaLaunchAttribute attr[2];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (pl.cs > 1) {
-            attr[1].id = cudaLaunchAttributeClusterDimension;
-            attr[1].val.clusterDim.x = pl.cs;
-            attr[1].val.clusterDim.y = 1;
-            attr[1].val.clusterDim.z = 1;
-            cfg.numAttrs = 2;
-        }
-        e = cudaLaunchKernelEx(&cfg, verify_tc_kernel, p, tmq, *tmk, *tmv);
-    }
-    if (e != cudaSuccess) {
-        *why = cudaGetErrorString(e);
-        return SDKV_ERR_CUDA;
-    }
-    return SDKV_OK;
+    return p.R <= kVNQ ? launch_vtc<1>(p, a, tmk, tmv, num_sms, why) : launch_vtc<2>(p, a, tmk, tmv, num_sms, why);
 }
 
 }  // namespace sdkv
