@@ -78,7 +78,8 @@ struct VCfg {
     static constexpr int OFF_P = OFF_V + kVVSt * T_B;
     static constexpr int OFF_RED = OFF_P + 2 * P_B;          // [group][4 warps][32 rows] tile maxima
     static constexpr int OFF_M = OFF_RED + NG * 4 * kVNQ * 4;  // [2][NQ] row references (double-buffered)
-    static constexpr int OFF_BAR = OFF_M + 2 * NQ * 4;
+    static constexpr int OFF_F = OFF_M + 2 * NQ * 4;         // [NQ] rescale factors of a raise, [NG] flags
+    static constexpr int OFF_BAR = OFF_F + NQ * 4 + 16;
     static constexpr int NBAR = 2 * kVKSt + 2 * kVVSt + 1 + 2 + 2 + 2 + 1 + 1;
     static constexpr int OFF_TMEM = OFF_BAR + NBAR * 8;
     static constexpr int SMEM = OFF_TMEM + 16;
@@ -153,6 +154,8 @@ __global__ void __launch_bounds__(VCfg<NG>::NT, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEM);
     float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
     float* mref = reinterpret_cast<float*>(smem + C::OFF_M);
+    float* fac = reinterpret_cast<float*>(smem + C::OFF_F);
+    int* fac_any = reinterpret_cast<int*>(smem + C::OFF_F + NQ * 4);
     __shared__ int s_abort;
     __shared__ int s_last;
     __shared__ int s_issued_k, s_issued_v;   // K and V tiles whose copies were issued
@@ -393,8 +396,15 @@ __global__ void __launch_bounds__(VCfg<NG>::NT, 1)
 #pragma unroll
             for (int i = 0; i < 8; ++i) g[i] = -INFINITY;
 #pragma unroll
-            for (int r = 0; r < kVNQ; ++r)
-                g[r & 7] = fmaxf(g[r & 7], (vis >> r) & 1u ? fmaf(__uint_as_float(v[r]), c, -mc[r]) : -INFINITY);
+            for (int k = 0; k < kVNQ / 4; ++k) {   // references 4 at a time (16-byte aligned)
+                const float4 m4 = *reinterpret_cast<const float4*>(mc + 4 * k);
+                const float mk[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = 4 * k + i;
+                    g[r & 7] = fmaxf(g[r & 7], (vis >> r) & 1u ? fmaf(__uint_as_float(v[r]), c, -mk[i]) : -INFINITY);
+                }
+            }
             const bool viol = fmaxf(fmaxf(fmaxf(g[0], g[1]), fmaxf(g[2], g[3])), fmaxf(fmaxf(g[4], g[5]), fmaxf(g[6], g[7]))) >
                               kVRescale;
             // one vote per tile; a thread whose wait gave up set the abort flag before it
@@ -421,62 +431,59 @@ __global__ void __launch_bounds__(VCfg<NG>::NT, 1)
                     red[(4 * g2 + q4) * kVNQ + lane] = x[0];
                 }
                 named_bar_sync(kVBar, C::NSOFT);
-                // the same decisions in every thread: whether some row with a finite
-                // reference grows (then what is accumulated must be rescaled)
-                const float* rg = red + 4 * kVNQ * g2;   // this group's four warps' maxima
-                bool rescale_o = false;
-#pragma unroll
-                for (int r = 0; r < kVNQ; ++r) {
-                    const float tm = fmaxf(fmaxf(rg[r], rg[kVNQ + r]), fmaxf(rg[2 * kVNQ + r], rg[3 * kVNQ + r]));
-                    rescale_o |= tm > mc[r] + kVRescale && mc[r] != -INFINITY;
+                // the group's first warp, lane r: row rb + r's tile maximum, its new
+                // reference (into the other buffer) and its rescale factor
+                if (q4 == 0) {
+                    const float* rg = red + 4 * kVNQ * g2;
+                    const float tm = fmaxf(fmaxf(rg[lane], rg[kVNQ + lane]), fmaxf(rg[2 * kVNQ + lane], rg[3 * kVNQ + lane]));
+                    const float mo = mref[mb * NQ + rb + lane];
+                    const bool grow = tm > mo + kVRescale;   // mo = -inf: the row's first visible keys
+                    const bool scaled = grow && mo != -INFINITY;
+                    fac[rb + lane] = scaled ? fast_exp2(mo - tm) : 1.f;
+                    mref[(mb ^ 1) * NQ + rb + lane] = grow ? tm : mo;
+                    const unsigned any_scaled = __ballot_sync(0xffffffffu, scaled);
+                    if (lane == 0) fac_any[g2] = any_scaled != 0u;
                 }
-                if (rescale_o && t >= 1) {
-                    // S(t) was issued after every PV product but PV(t - 1): wait for that
-                    // one, then scale this warp's 32 dims of O^T, 16 rows at a time
-                    const bool ok = mbar_wait(bar_pv, (t - 1) & 1);
-                    if (!ok) *abort_flag = 1;
-                    if (__all_sync(0xffffffffu, ok)) {
-                        tc_fence_after();
+                // the factors and new references are written; the old references and
+                // the maxima are no longer read
+                named_bar_sync(kVBar, C::NSOFT);
+                mb ^= 1;
+                if (fac_any[g2]) {
+                    float f[kVNQ];
 #pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            uint32_t ov[16];
-                            tmem_ld16_sync(tlane + C::COL_O + rb + 16 * hh, ov);
+                    for (int k = 0; k < kVNQ / 4; ++k) {
+                        const float4 f4 = *reinterpret_cast<const float4*>(fac + rb + 4 * k);
+                        f[4 * k] = f4.x;
+                        f[4 * k + 1] = f4.y;
+                        f[4 * k + 2] = f4.z;
+                        f[4 * k + 3] = f4.w;
+                    }
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const int r = 16 * hh + i;
-                                const float tm = fmaxf(fmaxf(rg[r], rg[kVNQ + r]), fmaxf(rg[2 * kVNQ + r], rg[3 * kVNQ + r]));
-                                if (tm > mc[r] + kVRescale && mc[r] != -INFINITY)
-                                    ov[i] = __float_as_uint(__uint_as_float(ov[i]) * fast_exp2(mc[r] - tm));
+                    for (int r = 0; r < kVNQ; ++r) {
+                        l[r] *= f[r];
+                        le[r] *= f[r];
+                    }
+                    if (t >= 1) {
+                        // S(t) was issued after every PV product but PV(t - 1): wait for that
+                        // one, then scale this warp's 32 dims of O^T, 16 rows at a time
+                        const bool ok = mbar_wait(bar_pv, (t - 1) & 1);
+                        if (!ok) *abort_flag = 1;
+                        if (__all_sync(0xffffffffu, ok)) {
+                            tc_fence_after();
+#pragma unroll
+                            for (int hh = 0; hh < 2; ++hh) {
+                                uint32_t ov[16];
+                                tmem_ld16_sync(tlane + C::COL_O + rb + 16 * hh, ov);
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f[16 * hh + i]);
+                                tmem_st16_sync(tlane + C::COL_O + rb + 16 * hh, ov);
                             }
-                            tmem_st16_sync(tlane + C::COL_O + rb + 16 * hh, ov);
                         }
                     }
                 }
-                // new references into the other buffer (one thread per group writes
-                // them; every thread reads the old ones until the barrier below)
-                float* mn = mref + (mb ^ 1) * NQ + rb;
-#pragma unroll
-                for (int r = 0; r < kVNQ; ++r) {
-                    const float tm = fmaxf(fmaxf(rg[r], rg[kVNQ + r]), fmaxf(rg[2 * kVNQ + r], rg[3 * kVNQ + r]));
-                    const float mo = mc[r];
-                    float mnew = mo;
-                    if (tm > mo + kVRescale) {   // mo = -inf: the row's first visible keys
-                        const float f = mo != -INFINITY ? fast_exp2(mo - tm) : 1.f;
-                        mnew = tm;
-                        l[r] *= f;
-                        le[r] *= f;
-                    }
-                    if (L == 0) mn[r] = mnew;
-                }
-                // the maxima and the old references are read, the new ones written; the
-                // next tile's maxima wait for this barrier, and a timeout above stops
-                // every thread here together
-                named_bar_sync(kVBar, C::NSOFT);
-                mb ^= 1;
-                if (*abort_flag) {
-                    aborted = true;
-                    break;
-                }
+                // a wait that gave up above set the abort flag: every thread leaves at the
+                // next tile's vote (or at the end of the loop), never alone
             }
             // weights rounded to bf16 as the PV product uses them; l sums the same
             // values, le the unrounded ones; P^T row `L` of buffer t & 1, columns rb .. rb + 31
@@ -484,12 +491,15 @@ __global__ void __launch_bounds__(VCfg<NG>::NT, 1)
             const float* mw = mref + mb * NQ + rb;
 #pragma unroll
             for (int k = 0; k < kVNQ / 8; ++k) {   // 16-byte chunk 4*g2 + k: rows rb + 8k .. rb + 8k + 7
+                const float4 ma = *reinterpret_cast<const float4*>(mw + 8 * k);
+                const float4 mb4 = *reinterpret_cast<const float4*>(mw + 8 * k + 4);
+                const float mk[8] = {ma.x, ma.y, ma.z, ma.w, mb4.x, mb4.y, mb4.z, mb4.w};
                 uint32_t pk[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int r = 8 * k + 2 * i;
-                    const float x0 = (vis >> r) & 1u ? fast_exp2(fmaf(__uint_as_float(v[r]), c, -mw[r])) : 0.f;
-                    const float x1 = (vis >> (r + 1)) & 1u ? fast_exp2(fmaf(__uint_as_float(v[r + 1]), c, -mw[r + 1])) : 0.f;
+                    const float x0 = (vis >> r) & 1u ? fast_exp2(fmaf(__uint_as_float(v[r]), c, -mk[2 * i])) : 0.f;
+                    const float x1 = (vis >> (r + 1)) & 1u ? fast_exp2(fmaf(__uint_as_float(v[r + 1]), c, -mk[2 * i + 1])) : 0.f;
                     le[r] += x0;
                     le[r + 1] += x1;
                     const __nv_bfloat162 w2 = __floats2bfloat162_rn(x0, x1);
