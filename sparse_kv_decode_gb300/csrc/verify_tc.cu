@@ -397,6 +397,7 @@ __global__ void __launch_bounds__(VCfg<NG>::NT, 1)
             for (int i = 0; i < 8; ++i) g[i] = -INFINITY;
 #pragma unroll
             for (int k = 0; k < kVNQ / 4; ++k) {   // references 4 at a time (16-byte aligned)
+                if (rb + 4 * k >= p.R) break;      // only padding rows from here (warp-uniform)
                 const float4 m4 = *reinterpret_cast<const float4*>(mc + 4 * k);
                 const float mk[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
@@ -491,6 +492,7 @@ __global__ void __launch_bounds__(VCfg<NG>::NT, 1)
             const float* mw = mref + mb * NQ + rb;
 #pragma unroll
             for (int k = 0; k < kVNQ / 8; ++k) {   // 16-byte chunk 4*g2 + k: rows rb + 8k .. rb + 8k + 7
+                if (rb + 8 * k >= p.R) break;      // only padding rows from here: their weights stay 0
                 const float4 ma = *reinterpret_cast<const float4*>(mw + 8 * k);
                 const float4 mb4 = *reinterpret_cast<const float4*>(mw + 8 * k + 4);
                 const float mk[8] = {ma.x, ma.y, ma.z, ma.w, mb4.x, mb4.y, mb4.z, mb4.w};
