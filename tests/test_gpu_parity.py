@@ -52,6 +52,7 @@ def _status_ok(ws):
     (2, 8, 2, 128, 40, 5),        # 20 rows, one chunk a head
     (3, 6, 3, 64, 77, 3),         # short cache, fewer keys than a tile per split
     (1, 2, 2, 128, 0, 1),         # a single key
+    (1, 16, 2, 64, 900, 4),       # d = 64 with 32 rows (the mma.sync path's row tiles)
 ])
 def test_dense_verify_matches_oracle(B, Hq, Hkv, d, n_prefix, gamma):
     g = torch.Generator().manual_seed(B * 1000 + Hq * 10 + gamma)
@@ -88,11 +89,15 @@ def test_dense_verify_rising_scores(B, Hq, Hkv, n_prefix, gamma):
     assert_lse_close(lse, l_ref, "dense")
 
 
-def test_dense_verify_strided_cache_and_repeat_calls():
+@pytest.mark.parametrize("Hq,gamma", [(8, 3), (16, 5), (28, 5)])
+def test_dense_verify_strided_cache_and_repeat_calls(Hq, gamma):
     # the cache has spare capacity rows (n_cap > n) and heads interleaved with
-    # batch: strides differ from a packed layout; the same workspace is reused
-    g = torch.Generator().manual_seed(5)
-    B, Hq, Hkv, d, n_prefix, gamma, n_cap = 2, 8, 4, 128, 1500, 3, 1600
+    # batch: strides differ from a packed layout; the same workspace is reused,
+    # so the per-head counters must be back at zero after every call.  6, 20
+    # and 35 query rows per KV head: the mma.sync verify and both row-group
+    # counts of the tensor-core one
+    g = torch.Generator().manual_seed(5 + Hq)
+    B, Hkv, d, n_prefix, n_cap = 2, 4, 128, 1500, 1600
     big = _rand((Hkv, B, n_cap, d), g)
     k = big.permute(1, 0, 2, 3)
     v = _rand((Hkv, B, n_cap, d), g).permute(1, 0, 2, 3)
