@@ -346,14 +346,16 @@ def phase_record(us_step, layers, alg_bytes_per_layer, hbm_peak):
             "gbs": gbs, "frac_of_measured_hbm": gbs / hbm_peak, "frac_of_8tbs_nominal": gbs / NOMINAL_HBM_GBS}
 
 
+# The files the split-K attention kernels (the gathered, contiguous and dense
+# decodes whose traffic profiles/dram_traffic.txt records) are compiled from.
+ATTN_SOURCES = ("sparse_kv_decode_gb300/csrc/attn_splitk.cu", "sparse_kv_decode_gb300/csrc/sdkv_common.cuh",
+                "sparse_kv_decode_gb300/csrc/sdkv_internal.h", "include/sdkv.h")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "sparse_kv_decode_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        path = os.path.join(csrc, name)
-        if not os.path.isfile(path):
-            continue
-        with open(path, "rb") as f:
+    for rel in ATTN_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 

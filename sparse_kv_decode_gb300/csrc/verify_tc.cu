@@ -15,33 +15,36 @@
 //   softmax        4 * NG warps, one thread per (key, row group): a warp reads
 //                  its own quarter of the tensor-memory lanes (keys) and, for
 //                  its group, 32 scores per key.  Every row r has one
-//                  reference m_r, the same in all threads; a weight is
-//                  2^(scale*log2e*s - m_r), rounded to bf16 into P^T.  The
-//                  threads vote once per tile (a named barrier with an OR)
-//                  on whether some visible score passed its row's reference
-//                  by more than 2^8; only then (always on the first tile) do
-//                  they reduce the tile's row maxima, raise the references
-//                  and rescale what was accumulated.  So the unscaled weights
-//                  stay <= 256.  Each thread sums its keys' weights per row:
-//                  l of the rounded weights, which O is normalised by (the
-//                  weights O summed), and l_exact of the unrounded ones, for
-//                  the log-sum-exp; the sums are reduced over the threads at
-//                  the end.  Causal mask: query t of a row sees keys <=
-//                  n_prefix + t; interior tiles skip it.
+//                  reference m_r, the same in all threads (shared memory,
+//                  double-buffered); a weight is 2^(scale*log2e*s - m_r),
+//                  rounded to bf16 into P^T.  The threads vote once per tile
+//                  (a named barrier with an OR) on whether some visible score
+//                  passed its row's reference by more than 2^8; only then
+//                  (always on the first tile) do they reduce the tile's row
+//                  maxima, after which one warp per group computes the new
+//                  references and rescale factors and the others read the
+//                  factors back, to rescale what was accumulated.  So the
+//                  unscaled weights stay <= 256.  Each thread sums its keys'
+//                  weights per row: l of the rounded weights, which O is
+//                  normalised by (the weights O summed), and l_exact of the
+//                  unrounded ones, for the log-sum-exp; the sums are reduced
+//                  over the threads at the end.  Causal mask: query t of a
+//                  row sees keys <= n_prefix + t; interior tiles skip it, and
+//                  chunks of rows past R are skipped.
 //   O^T += V^T P^T M = 128 head dims, N = 64 (the rows, padded to a 128-byte
 //                  swizzle row of P^T), K = 128 keys.  A = the V tile
 //                  as TMA wrote it ([keys][dims]: MN-major), B = P^T
 //                  ([keys][rows]: MN-major), both 128-byte swizzle.
 // Warp 0 and the last warp issue the TMA copies of the K and V tiles, each in
 // stages of their own (a K stage frees as soon as its score is done, so K
-// copies run well ahead of the scores); one thread of warp 1 the MMAs,
-// the score of tile t before the PV product of tile t - 1 so that the softmax
-// of a tile overlaps the next score; warps 2 .. 1 + 4 * NG the softmax.  A CTA takes one
-// (sequence, KV head) and one chunk of its keys; the chunks of a head form
-// clusters of up to 8 CTAs (one CTA per SM, all in one wave) whose partials (o, m, l, l_exact)
-// merge through distributed shared memory, and the last cluster of a head
-// (ticket) merges the clusters' partials.  Every wait is bounded, and the
-// softmax warps leave their loop together.
+// copies run well ahead of the scores); one thread of warp 1 the MMAs, the
+// score of tile t before the PV product of tile t - 1 so that the softmax of a
+// tile overlaps the next score; warps 2 .. 1 + 4 * NG the softmax.  A CTA takes
+// one (sequence, KV head) and one chunk of its keys; the chunks of a head form
+// clusters of up to 8 CTAs (one CTA per SM, all in one wave) whose partials
+// (o, m, l, l_exact) merge through distributed shared memory, and the last
+// cluster of a head (ticket) merges the clusters' partials.  Every wait is
+// bounded, and the softmax warps leave their loop together, at a shared vote.
 #include "sdkv_common.cuh"
 #include "sdkv_internal.h"
 
