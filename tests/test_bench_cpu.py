@@ -88,22 +88,26 @@ def test_oracle_step_plan_samples_large_steps_evenly():
 
 def test_traffic_figures_only_for_their_sources_and_workload(tmp_path, monkeypatch):
     import bench
-    csrc = tmp_path / "sparse_kv_decode_gb300" / "csrc"
-    csrc.mkdir(parents=True)
-    (csrc / "k.cu").write_text("// kernel\n")
-    (csrc / "__pycache__").mkdir()            # not a regular file: ignored by the hash
+    for rel in bench.ATTN_SOURCES:
+        f = tmp_path / rel
+        f.parent.mkdir(parents=True, exist_ok=True)
+        f.write_text("// " + rel + "\n")
+    other = tmp_path / "sparse_kv_decode_gb300" / "csrc" / "other_kernel.cu"
+    other.write_text("// another kernel\n")
     (tmp_path / "profiles").mkdir()
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     h = bench.kernel_source_hash()
     (tmp_path / "profiles" / "dram_traffic.txt").write_text(
         "# phase  bytes_per_call  csrc_hash  workload\n"
-        "score   1.5e+08   %s   llama8b_32k\n"
-        "sparse  4.0e+07   0123456789abcdef   llama8b_32k\n" % h)
-    assert bench.traffic_from_profiles("score", "llama8b_32k") == 1.5e8
-    assert bench.traffic_from_profiles("score", "llama8b_128k") is None   # another workload
-    assert bench.traffic_from_profiles("sparse", "llama8b_32k") is None   # stale sources
-    (csrc / "k.cu").write_text("// kernel, changed\n")
-    assert bench.traffic_from_profiles("score", "llama8b_32k") is None
+        "sparse  4.0e+07   %s   llama8b_32k\n"
+        "dense   1.3e+08   0123456789abcdef   llama8b_32k\n" % h)
+    assert bench.traffic_from_profiles("sparse", "llama8b_32k") == 4.0e7
+    assert bench.traffic_from_profiles("sparse", "llama8b_128k") is None   # another workload
+    assert bench.traffic_from_profiles("dense", "llama8b_32k") is None     # stale sources
+    other.write_text("// another kernel, changed\n")                       # not an attention source
+    assert bench.traffic_from_profiles("sparse", "llama8b_32k") == 4.0e7
+    (tmp_path / bench.ATTN_SOURCES[0]).write_text("// attention kernel, changed\n")
+    assert bench.traffic_from_profiles("sparse", "llama8b_32k") is None
 
 
 def _free_port():
