@@ -53,6 +53,8 @@ def _status_ok(ws):
     (3, 6, 3, 64, 77, 3),         # short cache, fewer keys than a tile per split
     (1, 2, 2, 128, 0, 1),         # a single key
     (1, 16, 2, 64, 900, 4),       # d = 64 with 32 rows (the mma.sync path's row tiles)
+    (1, 17, 1, 128, 2500, 1),     # 17 rows: a one-query decode on the tensor-core verify
+    (1, 22, 2, 128, 1800, 3),     # 33 rows: the smallest case with two row groups
 ])
 def test_dense_verify_matches_oracle(B, Hq, Hkv, d, n_prefix, gamma):
     g = torch.Generator().manual_seed(B * 1000 + Hq * 10 + gamma)
