@@ -174,7 +174,10 @@ int sdkv_select_topk(const float* scores, int32_t B, int32_t Hkv, int32_t n,
  *     o[b][hq]   = sum_{j in S} softmax_j(scale q . k_j) v_j
  *     lse[b][hq] = log sum_{j in S} exp(scale q . k_j)        (natural log)
  * An empty list gives o = 0 and lse = -inf.  Split-K over chunks of the lists
- * with a log-sum-exp combine; fp32 accumulation, bf16 output.
+ * with a log-sum-exp combine; with many lists (more than the clusters of one
+ * wave cover, Hq/Hkv <= 16, B*Hkv <= 2048) each CTA takes an equal span of the
+ * concatenated lists instead, several short lists at once.  fp32 accumulation,
+ * bf16 output.
  *
  *   q        device bf16 [B][Hq][d], contiguous
  *   k, v     device bf16 caches (see conventions), kv_strides shared

@@ -1110,7 +1110,8 @@ size_t dense_ws_bytes(int B, int Hq, int Hkv, int d, int n_total, int gamma, int
 size_t sparse_ws_bytes(int B, int Hq, int Hkv, int d, int num_sms) {
     const int BH = B * Hkv;
     const int R = Hq / Hkv;
-    return attn_ws_layout(nullptr, BH, R, d, sparse_grid_target(num_sms) + BH).bytes;
+    const int chunks = std::max(sparse_grid_target(num_sms) + BH, 2 * packed_decode_grid_max(num_sms));
+    return attn_ws_layout(nullptr, BH, R, d, chunks).bytes;
 }
 
 int launch_dense_verify(const AttnLaunch& a, const CUtensorMap* tmk, const CUtensorMap* tmv, int num_sms,
@@ -1191,6 +1192,9 @@ int list_decode_launch(AttnParams& p, const AttnLaunch& a, const CUtensorMap& tm
             break;
         }
     }
+    // many lists that no cluster plan covers: pack them by list position
+    if (KIND == kGather && p.cs == 1 && a.gamma == 1 && packed_decode_takes(a.B, a.Hq, a.Hkv, a.d))
+        return launch_packed_decode(a, num_sms, why);
     p.ncl = 1;
     const int max_chunks = sparse_max_chunks(p.BH, p.grid_target, p.cs);
     WsLayout L = attn_ws_layout(a.ws, p.BH, p.R, a.d, max_chunks);

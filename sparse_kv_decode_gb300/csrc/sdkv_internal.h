@@ -61,6 +61,11 @@ size_t sparse_ws_bytes(int B, int Hq, int Hkv, int d, int num_sms);
 int launch_dense_verify(const AttnLaunch& a, const CUtensorMap* tmk, const CUtensorMap* tmv,
                         int num_sms, const char** why);
 int launch_sparse_decode(const AttnLaunch& a, int num_sms, const char** why);
+// gathered decode packed by list position (packed_decode.cu): many short lists,
+// Hq/Hkv <= 16, B*Hkv <= 2048, one decode position; 2 partial slots per CTA
+bool packed_decode_takes(int B, int Hq, int Hkv, int d);
+int packed_decode_grid_max(int num_sms);
+int launch_packed_decode(const AttnLaunch& a, int num_sms, const char** why);
 // decode over the lists' rows compacted into contiguous [rows][d] buffers (2-D tensor maps)
 int launch_sparse_decode_compact(const AttnLaunch& a, const CUtensorMap* tmk, const CUtensorMap* tmv, int num_sms,
                                  const char** why);

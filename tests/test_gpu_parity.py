@@ -225,6 +225,80 @@ def test_sparse_ragged_mha_lists_cross_ranges():
     _status_ok(ws)
 
 
+def _packed_lens(kind, BH, n, rng):
+    if kind == "sparsemm":     # most lists 50..250 entries, one in ten 1000..n, a few empty
+        lens = np.where(rng.random(BH) < 0.1, rng.integers(1000, n + 1, BH), rng.integers(50, 251, BH))
+        lens[rng.integers(0, BH, 3)] = 0
+    elif kind == "uniform":
+        lens = rng.integers(0, 401, BH)
+    elif kind == "tiny":       # 0..3 entries: spans hold tens of lists, several passes of 16 / R
+        lens = rng.integers(0, 4, BH)
+    elif kind == "empty":
+        lens = np.zeros(BH, np.int64)
+    elif kind == "one_long":   # one list over the whole cache among empty ones: cut by many spans
+        lens = np.zeros(BH, np.int64)
+        lens[BH // 3] = n
+    return [int(x) for x in lens]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,d,n,kind", [
+    (8, 32, 32, 128, 4000, "sparsemm"),   # MHA, 256 lists: one query row per list, 16 lists a pass
+    (4, 64, 32, 64, 900, "uniform"),      # 2 rows per list, head dim 64
+    (16, 32, 8, 128, 1500, "uniform"),    # GQA 4: 4 lists a pass
+    (25, 12, 4, 64, 700, "uniform"),      # 3 rows per list: 5 lists a pass, one padding row
+    (80, 16, 1, 128, 600, "uniform"),     # 16 rows per list: one list a pass
+    (32, 32, 32, 64, 64, "tiny"),         # 1024 lists of 0..3 entries
+    (4, 25, 25, 128, 300, "empty"),       # every list empty
+    (2, 50, 50, 128, 9000, "one_long"),   # one list cut by ~70 spans, merged by the last of them
+])
+def test_sparse_packed_lists_match_oracle(B, Hq, Hkv, d, n, kind):
+    # more lists than the clusters of one wave cover: the CTAs take equal spans of
+    # the concatenated lists, several short lists per pass; lists cut by span ends
+    # are merged through the per-list tickets, which are back at zero after a call
+    seed = 60 + B + Hkv + d
+    g = torch.Generator().manual_seed(seed)
+    k = _rand((B, Hkv, n, d), g)
+    v = _rand((B, Hkv, n, d), g, 0.5)   # |o| < 4 even for lists of a few entries: bf16 output rounds < 1e-2
+    q = _rand((B, Hq, d), g, 1.5)
+    rng = np.random.default_rng(seed)
+    lens = _packed_lens(kind, B * Hkv, n, rng)
+    offs_d, offs = csr(lens, DEV)
+    _, idx = workloads.random_lists(B, Hkv, n, lens, seed=seed)
+    if idx.numel() == 0:
+        idx = torch.zeros(1, dtype=torch.int32)   # the index array must exist even when no list has entries
+    ws = sk.new_workspace(sk.workspace_size(sk.OP_SPARSE_DECODE, B, Hq, Hkv, d, 0, 0), DEV)
+    o_ref, l_ref = oracle.sparse_decode(q, k, v, offs, idx.numpy())
+    qd, kd, vd, idxd = q.to(DEV), k.to(DEV), v.to(DEV), idx.to(DEV)
+    for _ in range(2):
+        o, lse = sk.sparse_decode_attn(qd, kd, vd, offs_d, idxd, scale_of(d), ws=ws)
+        assert_attn_close(o, o_ref, "packed %s" % kind)
+        assert_lse_close(lse, l_ref, "packed %s" % kind)
+    _status_ok(ws)
+
+
+def test_sparse_packed_lists_with_an_offset_base():
+    # offsets[0] > 0: the lists sit at the end of a longer index array
+    seed = 71
+    g = torch.Generator().manual_seed(seed)
+    B, Hq, Hkv, d, n, base = 4, 32, 32, 128, 1000, 37
+    k = _rand((B, Hkv, n, d), g)
+    v = _rand((B, Hkv, n, d), g, 0.5)
+    q = _rand((B, Hq, d), g, 1.5)
+    rng = np.random.default_rng(seed)
+    lens = _packed_lens("sparsemm", B * Hkv, n, rng)
+    _, offs = csr(lens, "cpu")
+    _, idx = workloads.random_lists(B, Hkv, n, lens, seed=seed)
+    junk = torch.full((base,), n + 5, dtype=torch.int32)   # never read: outside every list
+    idx_all = torch.cat([junk, idx])
+    offs_d = torch.tensor((offs + base).astype(np.int32), device=DEV)
+    ws = sk.new_workspace(sk.workspace_size(sk.OP_SPARSE_DECODE, B, Hq, Hkv, d, 0, 0), DEV)
+    o, lse = sk.sparse_decode_attn(q.to(DEV), k.to(DEV), v.to(DEV), offs_d, idx_all.to(DEV), scale_of(d), ws=ws)
+    o_ref, l_ref = oracle.sparse_decode(q, k, v, offs, idx.numpy())
+    assert_attn_close(o, o_ref, "packed offset base")
+    assert_lse_close(lse, l_ref, "packed offset base")
+    _status_ok(ws)
+
+
 def test_dense_many_heads_per_range():
     # 256 KV heads of 302 rows: CTA ranges hold parts of two or three heads
     g = torch.Generator().manual_seed(23)
