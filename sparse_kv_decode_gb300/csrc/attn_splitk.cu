@@ -836,7 +836,7 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, KIND>::NT)
     float* wts = rs + R * 4;                                              // [batch][R]
     float* mls = wts + ((batch * R + 3) & ~3);                            // [batch][R][2]
     uint8_t* stage = reinterpret_cast<uint8_t*>(mls + ((batch * R * 2 + 3) & ~3));   // [batch][R][D]
-    const uint32_t stage_s = smem_u32(stage), mls_s = smem_u32(mls);
+    const uint32_t stage_s = smem_u32(stage);
     for (int e = tid; e < R * D; e += C::NCT) acc[e] = 0.f;
     for (int e = tid; e < R; e += C::NCT) {
         rs[4 * e] = -INFINITY;
@@ -848,7 +848,8 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, KIND>::NT)
         const int n16 = nb * R * (D / 4);
         for (int e = tid; e < n16; e += C::NCT) cp_async_16(stage_s + e * 16, src + static_cast<size_t>(e) * 16);
         const float* msrc = p.part_ml + static_cast<size_t>(c0 + s0) * R * 2;
-        for (int e = tid; e < nb * R; e += C::NCT) cp_async_8(mls_s + e * 8, msrc + 2 * e);
+        for (int e = tid; e < nb * R; e += C::NCT)   // L2 loads: other CTAs wrote these records
+            reinterpret_cast<float2*>(mls)[e] = __ldcg(reinterpret_cast<const float2*>(msrc) + e);
         cp_async_wait_all();
         named_bar_sync(1, C::NCT);
         for (int row = cw; row < R; row += C::NCW) {
@@ -1110,8 +1111,9 @@ size_t dense_ws_bytes(int B, int Hq, int Hkv, int d, int n_total, int gamma, int
 size_t sparse_ws_bytes(int B, int Hq, int Hkv, int d, int num_sms) {
     const int BH = B * Hkv;
     const int R = Hq / Hkv;
-    const int chunks = std::max(sparse_grid_target(num_sms) + BH, 2 * packed_decode_grid_max(num_sms));
-    return attn_ws_layout(nullptr, BH, R, d, chunks).bytes;
+    // the packed decode's partials: 2 per CTA, 16-byte (m, l) records
+    return std::max(attn_ws_layout(nullptr, BH, R, d, sparse_grid_target(num_sms) + BH).bytes,
+                    attn_ws_layout(nullptr, BH, R, d, 2 * packed_decode_grid_max(num_sms), 4).bytes);
 }
 
 int launch_dense_verify(const AttnLaunch& a, const CUtensorMap* tmk, const CUtensorMap* tmv, int num_sms,

@@ -41,7 +41,7 @@ struct PackParams {
     int* status;
     int* tickets;
     float* part_o;     // [2 * grid][R][D]: slot 2c holds the list cut by span c's start, 2c + 1 the one cut by its end
-    float* part_ml;    // [2 * grid][R][2]
+    float* part_ml;    // [2 * grid][R][4]: (m, l, -, -), 16-byte records
 };
 
 template <int D>
@@ -474,7 +474,7 @@ __global__ void __launch_bounds__(PackCfg<D>::NT) packed_decode_kernel(const __g
                         const size_t slot = 2 * static_cast<size_t>(cta) + cut;
                         *reinterpret_cast<float4*>(p.part_o + (slot * R + j) * D + d0) = a4;
                         if (d0 == 0)
-                            *reinterpret_cast<float2*>(p.part_ml + (slot * R + j) * 2) = make_float2(M, L);
+                            *reinterpret_cast<float4*>(p.part_ml + (slot * R + j) * 4) = make_float4(M, L, 0.f, 0.f);
                     }
                 }
             }
@@ -515,9 +515,13 @@ __global__ void __launch_bounds__(PackCfg<D>::NT) packed_decode_kernel(const __g
     const int lst = s_cut[ci][0], ls = s_cut[ci][1], le = s_cut[ci][2];
     const int ca = span_of(ls), cb = span_of(static_cast<long long>(le) - 1);
     const int b = lst / p.Hkv, h = lst - b * p.Hkv;
+    // Each thread merges one float4 of the output over the partials, loading
+    // them from L2 eight at a time (all in flight together); when the output has
+    // fewer float4 than the group has threads, SF threads share an item, each
+    // taking every SF-th partial, and combine through shared memory.
     const int R4 = R * (D / 4);                          // float4 of a list's output
     const int per_round = min(R4, nth);
-    const int SF = nth / per_round;                      // threads that share one float4 of the output
+    const int SF = nth / per_round;
     float* red = reinterpret_cast<float*>(smem + C::OFF_K) + ci * (C::NCT * 6);   // [SF][per_round][6]
     for (int base = 0; base < R4; base += per_round) {
         const int item = base + lt % per_round, qq = lt / per_round;
@@ -526,37 +530,45 @@ __global__ void __launch_bounds__(PackCfg<D>::NT) packed_decode_kernel(const __g
         float mm = -INFINITY, ll = 0.f;
         float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
         if (act) {
+            const float* po = p.part_o + static_cast<size_t>(j) * D + d0;
+            const float* pm = p.part_ml + static_cast<size_t>(j) * 4;
             for (int c0 = ca + qq; c0 <= cb; c0 += 8 * SF) {
-                float2 v2[8];
+                float4 v4[8];   // (m, l, -, -)
                 float4 o4[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {   // all loads of the batch in flight together
+                for (int u = 0; u < 8; ++u) {
                     const int c = c0 + u * SF;
-                    v2[u] = make_float2(-INFINITY, 0.f);
+                    v4[u] = make_float4(-INFINITY, 0.f, 0.f, 0.f);
                     o4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (c <= cb) {
-                        const size_t slot = 2 * static_cast<size_t>(c) + ((ls < off0 + c * cl) ? 0 : 1);
-                        v2[u] = __ldcg(reinterpret_cast<const float2*>(p.part_ml + (slot * R + j) * 2));
-                        o4[u] = __ldcg(reinterpret_cast<const float4*>(p.part_o + (slot * R + j) * D + d0));
+                        const size_t slot = 2 * static_cast<size_t>(c) + ((c > ca) ? 0 : 1);
+                        v4[u] = __ldcg(reinterpret_cast<const float4*>(pm + slot * R * 4));
+                        o4[u] = __ldcg(reinterpret_cast<const float4*>(po + slot * R * D));
                     }
                 }
+                float M = mm;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) M = fmaxf(M, v4[u].x);
+                if (M == -INFINITY) continue;
+                const float f = (mm == -INFINITY) ? 0.f : fast_exp2(mm - M);
+                ll *= f;
+                a4.x *= f;
+                a4.y *= f;
+                a4.z *= f;
+                a4.w *= f;
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    if (v2[u].x == -INFINITY) continue;
-                    const float mnew = fmaxf(mm, v2[u].x);
-                    const float fa = (mm == -INFINITY) ? 0.f : fast_exp2(mm - mnew);
-                    const float fb = fast_exp2(v2[u].x - mnew);
-                    ll = ll * fa + v2[u].y * fb;
-                    a4.x = a4.x * fa + o4[u].x * fb;
-                    a4.y = a4.y * fa + o4[u].y * fb;
-                    a4.z = a4.z * fa + o4[u].z * fb;
-                    a4.w = a4.w * fa + o4[u].w * fb;
-                    mm = mnew;
+                    const float w = (v4[u].x == -INFINITY) ? 0.f : fast_exp2(v4[u].x - M);
+                    ll = fmaf(w, v4[u].y, ll);
+                    a4.x = fmaf(w, o4[u].x, a4.x);
+                    a4.y = fmaf(w, o4[u].y, a4.y);
+                    a4.z = fmaf(w, o4[u].z, a4.z);
+                    a4.w = fmaf(w, o4[u].w, a4.w);
                 }
+                mm = M;
             }
         }
         if (SF > 1) {
-            // the SF threads of an item merged interleaved subsets of the partials
             if (act) {
                 float* r6 = red + (qq * per_round + lt % per_round) * 6;
                 r6[0] = mm;
@@ -573,18 +585,25 @@ __global__ void __launch_bounds__(PackCfg<D>::NT) packed_decode_kernel(const __g
             else
                 named_bar_sync(1, C::NCT);
             if (act && qq == 0) {
-                for (int q2 = 1; q2 < SF; ++q2) {
-                    const float* r6 = red + (q2 * per_round + lt % per_round) * 6;
-                    if (r6[0] == -INFINITY) continue;
-                    const float mnew = fmaxf(mm, r6[0]);
-                    const float fa = (mm == -INFINITY) ? 0.f : fast_exp2(mm - mnew);
-                    const float fb = fast_exp2(r6[0] - mnew);
-                    ll = ll * fa + r6[1] * fb;
-                    a4.x = a4.x * fa + r6[2] * fb;
-                    a4.y = a4.y * fa + r6[3] * fb;
-                    a4.z = a4.z * fa + r6[4] * fb;
-                    a4.w = a4.w * fa + r6[5] * fb;
-                    mm = mnew;
+                float M = mm;
+                for (int q2 = 1; q2 < SF; ++q2) M = fmaxf(M, red[(q2 * per_round + lt % per_round) * 6]);
+                if (M != -INFINITY) {
+                    const float f = (mm == -INFINITY) ? 0.f : fast_exp2(mm - M);
+                    ll *= f;
+                    a4.x *= f;
+                    a4.y *= f;
+                    a4.z *= f;
+                    a4.w *= f;
+                    for (int q2 = 1; q2 < SF; ++q2) {
+                        const float* r6 = red + (q2 * per_round + lt % per_round) * 6;
+                        const float w = (r6[0] == -INFINITY) ? 0.f : fast_exp2(r6[0] - M);
+                        ll = fmaf(w, r6[1], ll);
+                        a4.x = fmaf(w, r6[2], a4.x);
+                        a4.y = fmaf(w, r6[3], a4.y);
+                        a4.z = fmaf(w, r6[4], a4.z);
+                        a4.w = fmaf(w, r6[5], a4.w);
+                    }
+                    mm = M;
                 }
             }
         }
@@ -664,7 +683,7 @@ int launch_packed(const AttnLaunch& a, int num_sms, const char** why) {
     p.n_idx = a.n_idx;
     p.n_cap = a.n_cap;
     p.min_span = 2 * PackCfg<D>::TK;
-    const AttnWs ws = attn_ws(a.ws, p.BH, p.G, D, 2 * grid, 2);
+    const AttnWs ws = attn_ws(a.ws, p.BH, p.G, D, 2 * grid, 4);
     if (a.ws_bytes < ws.bytes) {
         *why = "workspace smaller than sdkv_workspace_size(SDKV_OP_SPARSE_DECODE, ...)";
         return SDKV_ERR_WORKSPACE;

@@ -225,9 +225,6 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int* ptr, int v) {
 __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ void cp_async_8(uint32_t dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
-}
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Bring a tile of a tensor into L2 (no shared-memory destination, no completion).
