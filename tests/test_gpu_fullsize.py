@@ -118,6 +118,25 @@ def test_sparsemm_ragged_full_layer():
     big = int(np.argmax(layer0))
     small = int(np.argmin(layer0))
     _check_heads(w, t, out, w.n, [(0, big), (3, small), (7, 5)])
+    # the sparse decode of every one of the 256 lists (the packed kernel's spans cut
+    # the long lists and pack the short ones), over the GPU's own lists
+    G = w.group
+    idx_all = out["idx"].cpu().numpy()
+    offs = out["offs"]
+    o_ref = np.zeros((w.batch, w.hq, w.d))
+    l_ref = np.zeros((w.batch, w.hq))
+    for i in range(w.batch * w.hkv):
+        b, h = divmod(i, w.hkv)
+        lst = idx_all[offs[i]:offs[i + 1]]
+        sel = torch.as_tensor(lst.astype(np.int64), device=DEV)
+        kk = t["k"][b, h].index_select(0, sel).cpu()[None, None]
+        vv = t["v"][b, h].index_select(0, sel).cpu()[None, None]
+        q = t["q"][b:b + 1, h * G:(h + 1) * G].cpu()
+        o1, l1 = oracle.sparse_decode(q, kk, vv, np.array([0, len(lst)]), np.arange(len(lst)))
+        o_ref[b, h * G:(h + 1) * G] = o1[0]
+        l_ref[b, h * G:(h + 1) * G] = l1[0]
+    assert_attn_close(out["o_sp"], o_ref, "sparse, every list")
+    assert_lse_close(out["l_sp"], l_ref, "sparse lse, every list")
 
 
 def test_video_full_layer_with_draft_steps():
