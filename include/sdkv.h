@@ -183,7 +183,9 @@ int sdkv_select_topk(const float* scores, int32_t B, int32_t Hkv, int32_t n,
  *   k, v     device bf16 caches (see conventions), kv_strides shared
  *   n_cap    rows per head present in k and v; list entries must lie in
  *            [0, n_cap) (others set SDKV_DEV_BAD_INDEX and read row 0)
- *   offsets, indices  device int32 CSR lists per (b, h), as from sdkv_select_topk
+ *   offsets, indices  device int32 CSR lists per (b, h), as from sdkv_select_topk;
+ *            offsets non-decreasing (a decrease sets SDKV_DEV_BAD_LIST and leaves
+ *            o and lse unspecified)
  *   n_idx    number of int32 entries the `indices` array holds (its length), or
  *            0.  With n_idx > 0 the kernel, while the previous kernel on
  *            `stream` finishes, prefetches the offsets and indices[0, n_idx)

@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(PackCfg<D>::NT) packed_decode_kernel(const __g
     const uint32_t bar_full = sbase + C::OFF_BAR;
     const uint32_t bar_empty = bar_full + STAGES * 8;
 
-    __shared__ int s_cnt[2];        // lists wholly before this span; lists starting before its end
+    __shared__ int s_cnt[3];        // lists wholly before this span; lists starting before its end; a bad list
     __shared__ int s_cut[2][3];     // lists cut by the span's start / end: (list, start, end); list -1: none
     __shared__ int s_tab[17];       // boundaries of the current pass's lists, clipped to the span
     __shared__ int s_abort;
@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(PackCfg<D>::NT) packed_decode_kernel(const __g
         }
         fence_mbar_init();
         s_abort = 0;
-        s_cnt[0] = s_cnt[1] = 0;
+        s_cnt[0] = s_cnt[1] = s_cnt[2] = 0;
     }
     {
         // Before the grid dependency resolves: the offsets and this CTA's share of
@@ -140,10 +140,8 @@ __global__ void __launch_bounds__(PackCfg<D>::NT) packed_decode_kernel(const __g
     __syncthreads();
     const int off0 = offc[0];
     long long total = static_cast<long long>(offc[p.BH]) - off0;
-    if (total < 0) {
-        if (tid == 0) flag_status(p.status, SDKV_DEV_BAD_LIST);
-        total = 0;
-    }
+    const bool total_bad = total < 0;
+    if (total_bad) total = 0;
     const int ncta = gridDim.x, cta = blockIdx.x;
     long long cl = (total + ncta - 1) / ncta;
     cl = max(static_cast<long long>(p.min_span), (cl + 15) & ~15ll);
@@ -169,15 +167,22 @@ __global__ void __launch_bounds__(PackCfg<D>::NT) packed_decode_kernel(const __g
             n_first += (e <= lo_c && s < lo_c) ? 1 : 0;
             n_end += (s < hi_c) ? 1 : 0;
         }
-        if (bad) flag_status(p.status, SDKV_DEV_BAD_LIST);
+        bad = __any_sync(0xffffffffu, bad) || total_bad;
         n_first = __reduce_add_sync(0xffffffffu, n_first);
         n_end = __reduce_add_sync(0xffffffffu, n_end);
         if (lane == 0) {
             atomicAdd(&s_cnt[0], n_first);
             atomicAdd(&s_cnt[1], n_end);
+            if (bad) s_cnt[2] = 1;
         }
     }
     __syncthreads();
+    // Decreasing offsets: every CTA reads all of them, so every CTA sees it and
+    // leaves before touching a ticket (the outputs are left unwritten)
+    if (s_cnt[2]) {
+        if (tid == 0) flag_status(p.status, SDKV_DEV_BAD_LIST);
+        return;
+    }
     const int first = s_cnt[0], endl = s_cnt[1];
     if (first >= endl) return;   // nothing in this span (uniform)
     if (tid == 0) {

@@ -342,6 +342,38 @@ def test_sparse_bad_index_is_flagged_not_faulted():
     assert sk.workspace_status(ws) == 0      # cleared by the read
 
 
+def test_sparse_packed_bad_index_and_bad_list_are_flagged_not_faulted():
+    # 128 lists (the packed decode): an entry outside [0, n_cap) is flagged and
+    # read as row 0; decreasing offsets are flagged before any per-list ticket is
+    # taken, so the same workspace then serves a valid call correctly
+    g = torch.Generator().manual_seed(19)
+    B, Hq, Hkv, d, n = 4, 32, 32, 128, 300
+    k = _rand((B, Hkv, n, d), g)
+    v = _rand((B, Hkv, n, d), g, 0.5)
+    q = _rand((B, Hq, d), g)
+    lens = [3 + (i % 200) for i in range(B * Hkv)]
+    offs_d, offs = csr(lens, DEV)
+    _, idx = workloads.random_lists(B, Hkv, n, lens, seed=19)
+    ws = sk.new_workspace(sk.workspace_size(sk.OP_SPARSE_DECODE, B, Hq, Hkv, d, 0, 0), DEV)
+    kd, vd, qd = k.to(DEV), v.to(DEV), q.to(DEV)
+    bad_idx = idx.clone()
+    bad_idx[5] = n + 7
+    bad_idx[int(offs[40]) + 1] = -4
+    sk.sparse_decode_attn(qd, kd, vd, offs_d, bad_idx.to(DEV), scale_of(d), ws=ws)
+    assert sk.workspace_status(ws) == 2      # SDKV_DEV_BAD_INDEX
+    bad_offs = offs.copy()
+    bad_offs[10] = bad_offs[11] + 5          # list 9 runs past list 10's start: list 10 has negative length
+    assert bad_offs[10] <= offs[-1]
+    sk.sparse_decode_attn(qd, kd, vd, torch.tensor(bad_offs.astype(np.int32), device=DEV), idx.to(DEV),
+                          scale_of(d), ws=ws)
+    assert sk.workspace_status(ws) == 3      # SDKV_DEV_BAD_LIST
+    o, lse = sk.sparse_decode_attn(qd, kd, vd, offs_d, idx.to(DEV), scale_of(d), ws=ws)
+    o_ref, l_ref = oracle.sparse_decode(q, k, v, offs, idx.numpy())
+    assert_attn_close(o, o_ref, "packed after bad calls")
+    assert_lse_close(lse, l_ref, "packed after bad calls")
+    _status_ok(ws)
+
+
 # ---------------------------------------------------------------------------
 # a2 window scoring
 # ---------------------------------------------------------------------------
