@@ -523,10 +523,11 @@ __global__ void __launch_bounds__(PackCfg<D>::NT) packed_decode_kernel(const __g
     // Each thread merges one float4 of the output over the partials, loading
     // them from L2 eight at a time (all in flight together); when the output has
     // fewer float4 than the group has threads, SF threads share an item, each
-    // taking every SF-th partial, and combine through shared memory.
+    // taking every SF-th partial, and combine through shared memory; with at
+    // most eight partials one thread loads them all at once, and no combine.
     const int R4 = R * (D / 4);                          // float4 of a list's output
     const int per_round = min(R4, nth);
-    const int SF = nth / per_round;
+    const int SF = (cb - ca + 1 <= 8) ? 1 : nth / per_round;
     float* red = reinterpret_cast<float*>(smem + C::OFF_K) + ci * (C::NCT * 6);   // [SF][per_round][6]
     for (int base = 0; base < R4; base += per_round) {
         const int item = base + lt % per_round, qq = lt / per_round;
