@@ -848,8 +848,16 @@ __global__ void __launch_bounds__(AttnCfg<D, MT, KW, TK, STAGES, KIND>::NT)
         const int n16 = nb * R * (D / 4);
         for (int e = tid; e < n16; e += C::NCT) cp_async_16(stage_s + e * 16, src + static_cast<size_t>(e) * 16);
         const float* msrc = p.part_ml + static_cast<size_t>(c0 + s0) * R * 2;
-        for (int e = tid; e < nb * R; e += C::NCT)   // L2 loads: other CTAs wrote these records
-            reinterpret_cast<float2*>(mls)[e] = __ldcg(reinterpret_cast<const float2*>(msrc) + e);
+        // L2 loads (other CTAs wrote these records), four per thread in flight together
+        for (int e0 = tid; e0 < nb * R; e0 += 4 * C::NCT) {
+            float2 v2[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (e0 + u * C::NCT < nb * R) v2[u] = __ldcg(reinterpret_cast<const float2*>(msrc) + e0 + u * C::NCT);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (e0 + u * C::NCT < nb * R) reinterpret_cast<float2*>(mls)[e0 + u * C::NCT] = v2[u];
+        }
         cp_async_wait_all();
         named_bar_sync(1, C::NCT);
         for (int row = cw; row < R; row += C::NCW) {
