@@ -247,6 +247,8 @@ def _packed_lens(kind, BH, n, rng):
     (16, 32, 8, 128, 1500, "uniform"),    # GQA 4: 4 lists a pass
     (25, 12, 4, 64, 700, "uniform"),      # 3 rows per list: 5 lists a pass, one padding row
     (80, 16, 1, 128, 600, "uniform"),     # 16 rows per list: one list a pass
+    (12, 64, 8, 64, 1200, "sparsemm"),    # GQA 8 at d = 64: 2 lists a pass
+    (20, 20, 4, 128, 900, "uniform"),     # 5 rows per list: 3 lists a pass, one padding row
     (32, 32, 32, 64, 64, "tiny"),         # 1024 lists of 0..3 entries
     (4, 25, 25, 128, 300, "empty"),       # every list empty
     (2, 50, 50, 128, 9000, "one_long"),   # one list cut by ~70 spans, merged by the last of them
