@@ -893,7 +893,8 @@ def run_sdkv(args, world, rank, local):
     sp = breakdown["sparse"]
     roofline = {"bound": "hbm", "achieved": sp["gbs"], "peak": hbm_peak, "unit": "GB/s",
                 "frac": sp["gbs"] / hbm_peak, "traffic": traffic_from_profiles("sparse", w.name),
-                "kernel": "sdkv_sparse_decode_attn (attn_splitk_kernel, gathered)", "peak_kind": peak_kind,
+                "kernel": "sdkv_sparse_decode_attn (gathered decode: attn_splitk_kernel, or packed_decode_kernel "
+                          "for many lists)", "peak_kind": peak_kind,
                 "alg_bytes_per_launch": sp["alg_bytes_per_layer"], "us_per_launch": sp["us_per_layer"]}
     line = {
         "metric": METRIC, "value": us_step, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": warm,
