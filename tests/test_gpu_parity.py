@@ -344,6 +344,29 @@ def test_sparse_bad_index_is_flagged_not_faulted():
     assert sk.workspace_status(ws) == 0      # cleared by the read
 
 
+@pytest.mark.parametrize("B,Hq", [(4, 32), (2, 64)])
+def test_sparse_strided_cache_chunked_and_packed(B, Hq):
+    # heads interleaved with batch and spare rows: the gathers use the caller's
+    # strides (128 one-row lists: the packed decode; 64 lists of GQA 2: the chunked one)
+    g = torch.Generator().manual_seed(31 + Hq)
+    Hkv, d, n_cap = 32, 128, 700
+    k = _rand((Hkv, B, n_cap, d), g).permute(1, 0, 2, 3)
+    v = _rand((Hkv, B, n_cap, d), g, 0.5).permute(1, 0, 2, 3)
+    q = _rand((B, Hq, d), g)
+    rng = np.random.default_rng(31 + Hq)
+    lens = rng.integers(0, 400, B * Hkv).tolist()
+    offs_d, offs = csr(lens, DEV)
+    _, idx = workloads.random_lists(B, Hkv, n_cap, lens, seed=31 + Hq)
+    kd, vd = k.to(DEV), v.to(DEV)
+    assert kd.stride() == k.stride()
+    ws = sk.new_workspace(sk.workspace_size(sk.OP_SPARSE_DECODE, B, Hq, Hkv, d, 0, 0), DEV)
+    o, lse = sk.sparse_decode_attn(q.to(DEV), kd, vd, offs_d, idx.to(DEV), scale_of(d), ws=ws)
+    o_ref, l_ref = oracle.sparse_decode(q, k, v, offs, idx.numpy())
+    assert_attn_close(o, o_ref, "sparse strided")
+    assert_lse_close(lse, l_ref, "sparse strided")
+    _status_ok(ws)
+
+
 def test_sparse_packed_bad_index_and_bad_list_are_flagged_not_faulted():
     # 128 lists (the packed decode): an entry outside [0, n_cap) is flagged and
     # read as row 0; decreasing offsets are flagged before any per-list ticket is
